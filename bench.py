@@ -1,0 +1,605 @@
+"""Benchmark: masked varlen attention forward on GB300, one JSON line.
+
+Step = one pass of the whole path over one batch: the range-table fill
+(``fill_query_ranges``) and the attention forward (``attn_fwd_varlen``) on the
+mm_prefix sliding-layer workload (4 x 4096-token prefills, 16 q / 8 KV heads,
+D 256, causal 1024-token window OR-ed with 8 bidirectional 256-token ranges per
+request), inputs resident in HBM, L2 flushed (256 MiB write) between steps.
+
+value  = effective TFLOP/s over unmasked score entries:
+         4 * D * Hq * (exact number of visible (query, key) pairs) / step time.
+e2e    = the same metric through the public API from pinned HOST tensors, the
+         host->device input copies and device->host output copy inside the
+         timed region.
+roofline: the attention kernel's algorithmic FLOPs per launch / its average
+         CUDA-event duration, against the measured bf16 tensor peak.
+cpu_baseline: the float64 CPU oracle on a bounded sample of query rows of
+         the same workload, on this host's cores.
+
+``--impl reference`` times that oracle (the only reference implementation
+that exists for this path) on the same metric.  Multi-GPU (torchrun): every
+rank runs its own replica of the workload on its own GPU (no collective on
+the data path); value = all ranks' FLOPs / max-over-ranks time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import multiprocessing as mp
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "unmasked-attention TFLOP/s (bf16) & % tensor peak; prefill tokens/s"
+WORKLOAD = "mm_prefix_sliding"
+WORKLOAD_DESC = ("mm_prefix sliding layer: 4 x 4096-token prefill, ctx 0, 16 q / 8 KV heads, D 256, bf16 "
+                 "N(0,1), causal 1024-token window OR 8 bidirectional 256-token ranges per request "
+                 "(range table filled on the GPU each step)")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+
+
+# ----------------------------------------------------------------- helpers
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def visible_counts_per_row(w, table):
+    """Exact visible-key count of every packed query row, from the two closed
+    intervals of the mask rule (causal/window base, window-clamped range).
+    Measurement accounting only; tests pin it against the oracle's dense mask."""
+    cu_q, cu_k = w.cu_seqlens()
+    counts = np.zeros(w.total_q, dtype=np.int64)
+    wl, wr = w.window_left, w.window_right
+    for b in range(w.num_reqs):
+        q0, q1 = int(cu_q[b]), int(cu_q[b + 1])
+        k_len = int(cu_k[b + 1] - cu_k[b])
+        ctx = k_len - (q1 - q0)
+        p = ctx + np.arange(q1 - q0, dtype=np.int64)
+        lo = np.maximum(p - wl, 0) if wl >= 0 else np.zeros_like(p)
+        if w.causal:
+            hi = p.copy()
+        else:
+            hi = (p + wr) if wr >= 0 else np.full_like(p, k_len - 1)
+        hi = np.minimum(hi, k_len - 1)
+        n = np.maximum(hi - lo + 1, 0)
+        if table is not None:
+            rs = table[q0:q1, 0].astype(np.int64)
+            re = table[q0:q1, 1].astype(np.int64)
+            rlo = np.maximum(rs, p - wl) if wl >= 0 else rs
+            rlo = np.maximum(rlo, 0)
+            rhi = np.minimum(re, k_len - 1)
+            rn = np.maximum(rhi - rlo + 1, 0)
+            ov = np.maximum(np.minimum(hi, rhi) - np.maximum(lo, rlo) + 1, 0)
+            ov = np.where((n > 0) & (rn > 0), ov, 0)
+            n = n + rn - ov
+        counts[q0:q1] = n
+    return counts
+
+
+def source_hash(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def load_traffic(kernel_src):
+    """DRAM traffic per launch from the committed ncu summary, or None when
+    the kernel source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if d.get("source_sha256_16") != source_hash(kernel_src):
+        return None
+    return d.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "20",
+                 "-i", str(self.gpu)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._reader = threading.Thread(target=self._read, daemon=True)
+            self._reader.start()
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        time.sleep(0.1)
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for t, line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((t, float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if self.t0 is not None and self.t0 - 0.05 <= r[0] <= self.t1 + 0.05]
+        use = inside if inside else rows
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in use for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+                "reasons": reasons, "samples": len(inside), "samples_total": len(rows)}
+
+
+# ----------------------------------------------------------------- oracle timing
+_W = {}
+
+
+def _worker_init(w_name):
+    """Spawned worker: the workload's shapes and the oracle's range table.
+    Inputs are drawn per request on first use (same N(0,1) recipe as the GPU
+    run, a per-request generator), so a worker never holds the whole batch."""
+    from masked_varlen_prefill_gb300 import workloads
+    from oracle import range_table as ort
+
+    w = workloads.workload(w_name)
+    cu_q, cu_k = w.cu_seqlens()
+    table = None
+    if w.ranges is not None:
+        table = np.full((w.total_q, 2), -1, dtype=np.int32)
+        ort.fill_by_spans(table, ort.ranges_from_padded(w.ranges), cu_q, np.asarray(w.k_lens))
+    _W.update(w=w, cu_q=cu_q, cu_k=cu_k, table=table)
+
+
+def _request_inputs(b):
+    import torch
+
+    w = _W["w"]
+    if _W.get("req") != b:
+        g = torch.Generator().manual_seed(w.seed * 100003 + b)
+        ql, kl = w.q_lens[b], w.k_lens[b]
+        _W["req"] = b
+        _W["qb"] = torch.randn(ql, w.num_heads_q, w.head_dim, generator=g).to(torch.bfloat16).double().numpy()
+        _W["kb"] = torch.randn(kl, w.num_heads_kv, w.head_dim, generator=g).to(torch.bfloat16).double().numpy()
+        _W["vb"] = torch.randn(kl, w.num_heads_kv, w.head_dim, generator=g).to(torch.bfloat16).double().numpy()
+        _W["sk"] = (torch.randn(w.num_heads_q, generator=g).double().numpy() if w.sink_mode else None)
+    return _W["qb"], _W["kb"], _W["vb"], _W["sk"]
+
+
+def _oracle_task(args):
+    """One timed oracle call: ``rows`` of request ``b``, every head.  Input
+    drawing happens before the clock starts; returns the oracle's seconds."""
+    b, rows = args
+    from oracle import attention as oatt
+
+    w, cu_q, cu_k, table = _W["w"], _W["cu_q"], _W["cu_k"], _W["table"]
+    rows = np.asarray(rows, dtype=np.int64)
+    if rows.size == 0:
+        return 0.0
+    qb, kb, vb, sk = _request_inputs(b)
+    q0 = int(cu_q[b])
+    ctx = w.k_lens[b] - w.q_lens[b]
+    t = time.perf_counter()
+    oatt.attend_rows(rows, qb, kb, vb, ctx, w.causal, w.window_left, w.window_right,
+                     None if table is None else table[q0 + rows], sk, w.sink_mode, w.scale)
+    return time.perf_counter() - t
+
+
+def oracle_sample_plan(w, rows_per_req):
+    """(request, rows) tasks: ``rows_per_req`` random query rows per request in
+    chunks of 32 rows."""
+    cu_q, _ = w.cu_seqlens()
+    rng = np.random.default_rng(7)
+    tasks = []
+    for b in range(w.num_reqs):
+        ql = int(cu_q[b + 1] - cu_q[b])
+        rows = np.sort(rng.choice(ql, size=min(rows_per_req, ql), replace=False))
+        for chunk in np.array_split(rows, max(1, len(rows) // 32)):
+            tasks.append((b, [int(x) for x in chunk]))
+    return tasks
+
+
+def time_oracle(w, counts, rows_per_req, pool, cores):
+    """The oracle over the sample: summed oracle seconds across workers, the
+    wall time of the parallel run, the sample's FLOPs and rows.  Throughput is
+    the sample's FLOPs over the wall time with ``cores`` workers busy."""
+    tasks = oracle_sample_plan(w, rows_per_req)
+    tasks.sort(key=lambda t: t[0])
+    cu_q, _ = w.cu_seqlens()
+    vis = sum(int(counts[int(cu_q[b]) + r]) for (b, rows) in tasks for r in rows)
+    flops = 4.0 * w.head_dim * w.num_heads_q * vis
+    chunk = max(1, math.ceil(len(tasks) / cores))
+    secs = pool.map(_oracle_task, tasks, chunksize=chunk)
+    cpu_s = float(sum(secs))
+    wall = max(cpu_s / cores, max(secs) if secs else 0.0)
+    return wall, flops, sum(len(r) for _, r in tasks), cpu_s
+
+
+def make_pool(cores, w_name):
+    """Spawned process pool, one single-threaded-BLAS worker per core, each
+    holding the workload's inputs; returns once every worker is ready."""
+    saved = {v: os.environ.get(v) for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS")}
+    for var in saved:
+        os.environ[var] = "1"
+    try:
+        pool = mp.get_context("spawn").Pool(cores, initializer=_worker_init, initargs=(w_name,))
+    finally:
+        for var, val in saved.items():
+            if val is None:
+                os.environ.pop(var, None)
+            else:
+                os.environ[var] = val
+    pool.map(_oracle_task, [(0, [])] * (4 * cores), chunksize=1)  # wait for every initializer
+    return pool
+
+
+# ----------------------------------------------------------------- distributed
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(value, world):
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def aggregate(per_rank_flops, max_seconds):
+    """Whole-job throughput: all ranks' work over the slowest rank's time."""
+    return per_rank_flops / max_seconds / 1e12
+
+
+# ----------------------------------------------------------------- main arms
+def run_reference(args, world, rank):
+    from masked_varlen_prefill_gb300 import workloads
+    from oracle import range_table as ort
+
+    if rank != 0:
+        return 0
+    w = workloads.workload(args.workload)
+    cu_q, _ = w.cu_seqlens()
+    table = None
+    if w.ranges is not None:
+        table = np.full((w.total_q, 2), -1, dtype=np.int32)
+        ort.fill_by_spans(table, ort.ranges_from_padded(w.ranges), cu_q, np.asarray(w.k_lens))
+    counts = visible_counts_per_row(w, table)
+    cores = os.cpu_count() or 1
+    pool = make_pool(cores, args.workload)
+    rows_per_req = 64
+    for _ in range(args.warmup):
+        time_oracle(w, counts, rows_per_req, pool, cores)
+    total_t, total_f, nrows = 0.0, 0.0, 0
+    for _ in range(args.steps):
+        t, f, n, _ = time_oracle(w, counts, rows_per_req, pool, cores)
+        total_t += t
+        total_f += f
+        nrows += n
+    pool.close()
+    value = total_f / total_t / 1e12
+    sample = (f"{nrows // max(1, args.steps)} query rows per step (up to {rows_per_req} per request, all heads) "
+              f"of the {args.workload} workload, float64 dense oracle")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD_DESC if args.workload == WORKLOAD else args.workload,
+                       "parallelism": "replicas"},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def _leading_decode(w):
+    n = 0
+    while n < w.num_reqs and w.q_lens[n] == 1:
+        n += 1
+    return n
+
+
+def run_gpu(args, world, rank, local):
+    import torch
+
+    import masked_varlen_prefill_gb300 as mvp
+    from masked_varlen_prefill_gb300 import workloads
+
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    mvp.load_library()
+    peaks, peak_src = load_peaks()
+
+    # CPU baseline pool first (spawned, rank 0 only)
+    pool = None
+    cores = os.cpu_count() or 1
+    if rank == 0 and not args.no_cpu_baseline:
+        pool = make_pool(cores, args.workload)
+
+    w = workloads.workload(args.workload)
+    n_dec = _leading_decode(w)
+    q, k, v, sinks = workloads.make_tensors(w, device=dev)
+    cu_q_np, cu_k_np = w.cu_seqlens()
+    cu_q = torch.from_numpy(cu_q_np).to(dev)
+    cu_k = torch.from_numpy(cu_k_np).to(dev)
+    seq_lens = torch.tensor(w.k_lens, dtype=torch.int32, device=dev)
+    ranges = torch.from_numpy(w.ranges).to(dev) if w.ranges is not None else None
+    table = torch.empty((w.total_q, 2), dtype=torch.int32, device=dev) if ranges is not None else None
+    covered = torch.empty(1, dtype=torch.int32, device=dev) if ranges is not None else None
+    out = torch.empty_like(q)
+    max_q, max_k = max(w.q_lens), max(w.k_lens)
+    ws = None
+    if n_dec > 0:
+        nbytes = mvp.attn_workspace_size(n_dec, w.num_heads_q, w.head_dim, max_k)
+        ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev) if nbytes else None
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    kw = dict(causal=w.causal, window_left=w.window_left, window_right=w.window_right, sinks=sinks,
+              sink_mode=w.sink_mode, scale=w.scale, workspace=ws)
+
+    def fill():
+        if ranges is None:
+            return 0
+        mvp.fill_query_ranges(ranges, cu_q, seq_lens, table, num_tokens=w.total_q, rows_written=covered)
+        return mvp.last_launch_count()
+
+    def attn(lo=0, hi=None):
+        """Attention over requests [lo, hi) of the batch (default: all)."""
+        hi = w.num_reqs if hi is None else hi
+        if lo == 0 and hi == w.num_reqs:
+            mvp.attn_fwd_varlen(q, k, v, out, cu_q, cu_k, max_q, max_k, range_table=table,
+                                range_covered=covered, num_decode_reqs=n_dec, **kw)
+        else:
+            nd = max(0, min(n_dec, hi) - lo)
+            mvp.attn_fwd_varlen(q, k, v, out, cu_q[lo:hi + 1], cu_k[lo:hi + 1], max(w.q_lens[lo:hi]),
+                                max(w.k_lens[lo:hi]), range_table=table, range_covered=covered,
+                                num_decode_reqs=nd, **kw)
+        return mvp.last_launch_count()
+
+    marks = {}
+
+    def step():
+        n = fill()
+        marks["mid"].record(stream)
+        return n + attn()
+
+    marks["mid"] = torch.cuda.Event(enable_timing=True)
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if mvp.get_last_device_error() != 0:
+        raise RuntimeError("device timeout during warm-up")
+
+    # accounting (host), from the GPU-filled table, which the tests pin bit-exact
+    counts = visible_counts_per_row(w, None if table is None else table.cpu().numpy())
+    visible = int(counts.sum())
+    flops = 4.0 * w.head_dim * w.num_heads_q * visible
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    launches = 0
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.mark("t0")
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        marks["mid"] = mids[i]
+        launches += step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    sampler.mark("t1")
+    barrier(world)
+    sampler.stop()
+    if mvp.get_last_device_error() != 0:
+        raise RuntimeError("device timeout during timed steps")
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    attn_ms = [m.elapsed_time(e) for m, e in zip(mids, ends)]
+    fill_ms = [s.elapsed_time(m) for s, m in zip(starts, mids)]
+    local_s = sum(step_ms) / 1e3
+    max_s = reduce_max(local_s, world)
+    value = aggregate(flops * args.steps * world, max_s)
+    ms_per_step = 1e3 * max_s / args.steps
+    tokens_per_s = w.total_q * args.steps * world / max_s
+
+    def time_sub(lo, hi, reps):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for a, b in ev:
+            flush.zero_()
+            a.record(stream)
+            attn(lo, hi)
+            b.record(stream)
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in ev) / reps / 1e3
+
+    # ------------------------------------------------------------- roofline
+    peak_t = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    peak_b = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    cu_q_l = [int(x) for x in cu_q_np]
+    dec_vis = int(counts[:cu_q_l[n_dec]].sum()) if n_dec else 0
+    pre_flops = 4.0 * w.head_dim * w.num_heads_q * (visible - dec_vis)
+    sub = {}
+    if 0 < n_dec < w.num_reqs:
+        for _ in range(2):
+            time_sub(0, n_dec, 1)
+            time_sub(n_dec, w.num_reqs, 1)
+        dec_s = time_sub(0, n_dec, max(3, args.steps // 4))
+        pre_s = time_sub(n_dec, w.num_reqs, max(3, args.steps // 4))
+    elif n_dec == w.num_reqs:
+        dec_s, pre_s = sum(attn_ms) / len(attn_ms) / 1e3, 0.0
+    else:
+        dec_s, pre_s = 0.0, sum(attn_ms) / len(attn_ms) / 1e3
+    dec_bytes = (dec_vis * w.num_heads_kv * w.head_dim * 2 * 2 + n_dec * w.num_heads_q * w.head_dim * 2 * 2)
+    if n_dec:
+        sub["decode"] = {"ms": 1e3 * dec_s, "rows": n_dec, "algorithmic_bytes": dec_bytes,
+                         "GB_per_s": dec_bytes / dec_s / 1e9, "frac_hbm": dec_bytes / dec_s / 1e9 / peak_b}
+    if pre_s > 0:
+        sub["prefill"] = {"ms": 1e3 * pre_s, "TFLOP_per_s": pre_flops / pre_s / 1e12,
+                          "frac_tensor": pre_flops / pre_s / 1e12 / peak_t}
+    kernel_dir = os.path.join(ROOT, "masked_varlen_prefill_gb300", "csrc")
+    if pre_s >= dec_s:
+        achieved = pre_flops / pre_s / 1e12
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_t, "unit": "TFLOP/s",
+                    "frac": achieved / peak_t,
+                    "traffic": load_traffic(os.path.join(kernel_dir, "attn_prefill.cu")),
+                    "kernel": f"attn_prefill_kernel (D={w.head_dim})",
+                    "peak_source": f"bf16_tflops (burst) of {peak_src}", "kernel_ms_per_launch": 1e3 * pre_s}
+    else:
+        achieved = dec_bytes / dec_s / 1e9
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": peak_b, "unit": "GB/s",
+                    "frac": achieved / peak_b, "traffic": None, "kernel": f"attn_decode_kernel (D={w.head_dim})",
+                    "peak_source": f"hbm_gbs of {peak_src}", "kernel_ms_per_launch": 1e3 * dec_s}
+    roofline["fill_ms_per_launch"] = sum(fill_ms) / len(fill_ms) if ranges is not None else 0.0
+
+    # ------------------------------------------------------------- e2e (host buffers)
+    e2e = None
+    if not args.no_e2e:
+        dev_in = [q, k, v, cu_q, cu_k] + ([seq_lens, ranges] if ranges is not None else []) + \
+                 ([sinks] if sinks is not None else [])
+        host_in = [t.cpu().pin_memory() for t in dev_in]
+        host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        h2d = sum(t.numel() * t.element_size() for t in host_in)
+        d2h = host_out.numel() * host_out.element_size()
+
+        def e2e_step():
+            for d, h in zip(dev_in, host_in):
+                d.copy_(h, non_blocking=True)
+            fill()
+            attn()
+            host_out.copy_(out, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        e_s = [torch.cuda.Event(enable_timing=True) for _ in range(args.e2e_steps)]
+        e_e = [torch.cuda.Event(enable_timing=True) for _ in range(args.e2e_steps)]
+        barrier(world)
+        for i in range(args.e2e_steps):
+            e_s[i].record(stream)
+            e2e_step()
+            e_e[i].record(stream)
+        torch.cuda.synchronize()
+        e2e_s = reduce_max(sum(a.elapsed_time(b) for a, b in zip(e_s, e_e)) / 1e3, world)
+        e2e = {"value": aggregate(flops * args.e2e_steps * world, e2e_s), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": args.e2e_steps,
+               "ms_per_step": 1e3 * e2e_s / args.e2e_steps}
+
+    # ------------------------------------------------------------- CPU baseline
+    cpu_baseline = None
+    if pool is not None:
+        t_cpu, f_cpu, n_rows, cpu_s = time_oracle(w, counts, args.cpu_rows_per_req, pool, cores)
+        pool.close()
+        cpu_baseline = {"value": f_cpu / t_cpu / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                        "sample": f"{n_rows} query rows (up to {args.cpu_rows_per_req} per request, all heads) of "
+                                  f"the {args.workload} workload, float64 dense oracle, {cpu_s:.1f} core-seconds "
+                                  f"over {cores} single-threaded workers"}
+
+    if rank == 0:
+        desc = WORKLOAD_DESC if args.workload == WORKLOAD else args.workload
+        line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": desc, "global_batch": w.num_reqs * world, "seq_len": max_q,
+                           "l2": "flushed between steps (256 MiB write, outside the events)",
+                           "parallelism": "replicas" if world > 1 else "single GPU"},
+                "pct_tensor_peak": 100.0 * value / peak_t, "tokens_per_s": tokens_per_s,
+                "visible_entries_per_step": visible, "sub_batches": sub,
+                "roofline": roofline, "cpu_baseline": cpu_baseline, "e2e": e2e,
+                "gpu_launches": launches, "clocks": sampler.summary()}
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD,
+                    help="workload name (default: the headline mm_prefix sliding layer)")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-rows-per-req", type=int, default=768)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    return run_gpu(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,169 @@
+/*
+ * mvp.h -- masked varlen prefill attention for GB300 (sm_103a), C ABI.
+ *
+ * Two operations, as described by the vLLM pages this library restates:
+ *
+ *   mvp_fill_query_ranges  -- vLLM PR #50294 review ("FA4 mm_prefix range
+ *       scan -> O(1) table lookup"), "Implementation breakdown" step 1 and the
+ *       fill_mm_prefix_query_ranges listing: per packed query row, the closed
+ *       [start, end] of the bidirectional range holding that row's absolute
+ *       position, or (-1, -1).
+ *   mvp_attn_fwd_varlen    -- the forward pass of variable-length MHA/GQA
+ *       softmax attention under serving masks: causal with a chunked-prefill
+ *       context offset (step14_4 "Causal Mask optimisation" tutorial, key j is
+ *       masked iff j > start_pos + i), sliding windows (PR #50294 mask_mod and
+ *       forward() wiring; PR #49815 symmetric window), the range table OR-ed in
+ *       (PR #50294 mask_mod), and per-head sinks in two modes (PR #49815
+ *       "_fwd_kernel sinks branch": key-0 bias or null logit).
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers are DEVICE pointers unless a parameter says otherwise.  The
+ *     caller owns every buffer; the library never frees caller memory.
+ *   - Work is enqueued on `stream` (a cudaStream_t, NULL = legacy default
+ *     stream) and the call returns without synchronising.
+ *   - Argument errors are detected on the host before anything is launched;
+ *     nothing is written then.  Return values are mvp_status codes.
+ *   - The library keeps one 4-byte device error word per device (allocated on
+ *     the first call on that device).  Kernels that hit a bounded-wait
+ *     timeout record a code there and unwind instead of hanging;
+ *     mvp_get_last_device_error() reads and clears it.
+ */
+#ifndef MVP_H_
+#define MVP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MVP_OK = 0,
+  MVP_ERR_ARG = -1,          /* null pointer, bad size, inconsistent shape      */
+  MVP_ERR_CAPACITY = -2,     /* out_capacity < num_tokens (the page asserts)    */
+  MVP_ERR_UNSUPPORTED = -3,  /* head_dim / head ratio / alignment not supported */
+  MVP_ERR_CUDA = -4,         /* a CUDA runtime call or launch failed            */
+  MVP_ERR_DEVICE_TIMEOUT = -5 /* a kernel recorded a bounded-wait timeout       */
+} mvp_status;
+
+typedef enum {
+  MVP_SINK_NONE = 0,
+  MVP_SINK_KEY0_BIAS = 1,  /* s[i,0] += sink[h] when key 0 is visible (MiMo)       */
+  MVP_SINK_NULL_LOGIT = 2  /* exp(sink[h]) joins the denominator only (GPT-OSS)   */
+} mvp_sink_mode;
+
+/*
+ * Range table fill.  Source: vLLM PR #50294 review, "Key source snippets",
+ * fill_mm_prefix_query_ranges, and "Implementation breakdown" step 1.
+ *
+ * ranges          int32 [num_reqs, max_ranges, 2], row-major.  Absolute closed
+ *                 (start, end) token positions of each request's
+ *                 bidirectional ranges; entries with start >= end are
+ *                 degenerate and skipped (use (0, 0) for padding).  Within a
+ *                 request, valid ranges must not overlap; if they do, the
+ *                 last listed range that holds a query position wins.
+ * query_start_loc int32 [num_reqs + 1], packed query row offsets (ascending,
+ *                 query_start_loc[0] == 0, query_start_loc[num_reqs] ==
+ *                 num_tokens).
+ * seq_lens        int32 [num_reqs], total key length of each request; the
+ *                 request's first scheduled query sits at absolute position
+ *                 seq_lens[b] - (query_start_loc[b+1] - query_start_loc[b]).
+ * num_tokens      host int, == query_start_loc[num_reqs] (the caller knows it
+ *                 on the host, as the page's builder does).
+ * out             int32 [out_capacity, 2]: rows [0, num_tokens) are ALL
+ *                 written: (start, end) of the range holding the row's
+ *                 absolute position, clipped to nothing (the range itself is
+ *                 stored unclipped), or (-1, -1).  Rows >= num_tokens are
+ *                 not touched.
+ * rows_written    int32 device scalar or NULL: set to num_tokens if at least
+ *                 one row got a range, else 0 (the page's return value; 0
+ *                 means the attention call may skip the range test).
+ * Errors: MVP_ERR_ARG (null pointer with num_tokens > 0, negative sizes),
+ *         MVP_ERR_CAPACITY (out_capacity < num_tokens), MVP_ERR_CUDA.
+ * num_tokens == 0: nothing is launched except the rows_written reset.
+ */
+int mvp_fill_query_ranges(const int32_t* ranges, int num_reqs, int max_ranges,
+                          const int32_t* query_start_loc, const int32_t* seq_lens,
+                          int num_tokens, int32_t* out, int out_capacity,
+                          int32_t* rows_written, void* stream);
+
+/*
+ * Bytes of caller-provided workspace that mvp_attn_fwd_varlen can use to
+ * split long single-token (decode) rows across several CTAs.  num_reqs is the
+ * number of requests the decode kernel covers (num_decode_reqs, or the whole
+ * batch when that is -1).  0 is valid everywhere: without workspace every
+ * decode row is handled by one CTA per KV head.
+ */
+size_t mvp_attn_workspace_size(int num_reqs, int num_heads_q, int head_dim, int max_k_len);
+
+/*
+ * Masked varlen attention forward.  The visible set of query row i of request
+ * b (absolute position p = ctx_b + i, ctx_b = context_lens[b] or
+ * k_len_b - q_len_b) for key j in [0, k_len_b):
+ *   base(p,j) = (causal ? j <= p : (window_right < 0 || j <= p + window_right))
+ *               && (window_left < 0 || j >= p - window_left)
+ *   rng(p,j)  = table_row.start <= j <= table_row.end
+ *               && (window_left < 0 || j >= p - window_left)
+ *   visible   = base || rng
+ * A "W-token causal window" is window_left = W - 1 (PR #50294 forward():
+ * the kept distance is < 1 + window); a symmetric window |i - j| <= w is
+ * causal = 0, window_left = window_right = w (PR #49815).
+ * Scores s = scale * q.k with KV head h / (num_heads_q / num_heads_kv).
+ * Sinks (fp32 [num_heads_q], natural-log units): KEY0_BIAS adds sink[h] to
+ * s[.,0] when key 0 is visible; NULL_LOGIT adds exp(sink[h]) to the softmax
+ * denominator.  out = sum_j softmax_j * v_j; lse = ln(denominator) (sink
+ * included).  A row with nothing visible gets out = 0, lse = -inf (sink in
+ * null-logit mode).
+ *
+ * q      bf16 [total_q, num_heads_q, head_dim], contiguous, 16-byte aligned.
+ * k, v   bf16 [total_k, num_heads_kv, head_dim], contiguous, 16-byte aligned.
+ * out    bf16 [total_q, num_heads_q, head_dim] (written for every row).
+ * lse    fp32 [num_heads_q, total_q] or NULL.
+ * cu_seqlens_q, cu_seqlens_k  int32 [num_reqs + 1] packed offsets.
+ * context_lens int32 [num_reqs] or NULL (NULL: k_len - q_len).
+ * max_q_len, max_k_len  host upper bounds of the per-request lengths (used to
+ *                 size the grid; rows beyond them are not computed).
+ * num_decode_reqs -1: the batch may mix single-token (decode) requests and
+ *                 longer ones anywhere; both kernels cover every request and
+ *                 each skips the other's.  k >= 0: the caller guarantees that
+ *                 requests [0, k) are exactly those with q_len == 1 (the
+ *                 decode-first order vLLM's scheduler uses); then the decode
+ *                 kernel covers only [0, k), the prefill kernel only
+ *                 [k, num_reqs), and a side with no requests is not launched.
+ * head_dim       64, 128, 256 or 512.  num_heads_q % num_heads_kv == 0.
+ * range_table    int32 [total_q, 2] from mvp_fill_query_ranges, or NULL.
+ * range_covered  int32 device scalar (rows_written of the fill) or NULL; when
+ *                it reads 0 the table is ignored.
+ * workspace      device scratch of workspace_bytes (may be NULL / 0); see
+ *                mvp_attn_workspace_size.
+ * Errors: MVP_ERR_ARG, MVP_ERR_UNSUPPORTED (head_dim, alignment, head ratio),
+ *         MVP_ERR_CUDA.  Requests with q_len == 0 produce no rows.
+ */
+int mvp_attn_fwd_varlen(const void* q, const void* k, const void* v, void* out, float* lse,
+                        const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                        const int32_t* context_lens, int num_reqs, int total_q, int total_k,
+                        int max_q_len, int max_k_len, int num_decode_reqs, int num_heads_q,
+                        int num_heads_kv,
+                        int head_dim, const int32_t* range_table, const int32_t* range_covered,
+                        int causal, int window_left, int window_right, const float* sinks,
+                        int sink_mode, float scale, void* workspace, size_t workspace_bytes,
+                        void* stream);
+
+/* Synchronises `stream`, returns MVP_ERR_DEVICE_TIMEOUT if a kernel recorded a
+ * timeout since the last call (and clears it), MVP_ERR_CUDA on a CUDA error,
+ * else MVP_OK. */
+int mvp_get_last_device_error(void* stream);
+
+/* Static string for a status code. */
+const char* mvp_status_str(int status);
+
+/* Number of kernel launches the last successful mvp_attn_fwd_varlen /
+ * mvp_fill_query_ranges call enqueued on this thread (for launch accounting). */
+int mvp_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MVP_H_ */

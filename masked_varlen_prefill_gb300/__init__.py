@@ -1,0 +1,30 @@
+"""Masked varlen prefill attention for GB300 (sm_103a).
+
+Thin Python binding over the C-ABI library ``lib/libmvp.so`` (declared in
+``include/mvp.h``).  The functions below only marshal arguments (torch CUDA
+tensors -> device pointers, sizes, the current stream) and raise on a non-zero
+status; every step of the computation runs in the library's CUDA kernels.
+There is no CPU fallback: if the library is missing, importing the binding's
+functions raises.
+"""
+
+from ._lib import (  # noqa: F401
+    MVP_ERR_ARG,
+    MVP_ERR_CAPACITY,
+    MVP_ERR_CUDA,
+    MVP_ERR_DEVICE_TIMEOUT,
+    MVP_ERR_UNSUPPORTED,
+    MVP_OK,
+    SINK_KEY0_BIAS,
+    SINK_NONE,
+    SINK_NULL_LOGIT,
+    MvpError,
+    attn_fwd_varlen,
+    attn_fwd_varlen_host,
+    attn_workspace_size,
+    fill_query_ranges,
+    get_last_device_error,
+    last_launch_count,
+    library_path,
+    load_library,
+)

@@ -1,0 +1,194 @@
+"""ctypes binding of ``lib/libmvp.so``: argument marshalling only."""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+MVP_OK = 0
+MVP_ERR_ARG = -1
+MVP_ERR_CAPACITY = -2
+MVP_ERR_UNSUPPORTED = -3
+MVP_ERR_CUDA = -4
+MVP_ERR_DEVICE_TIMEOUT = -5
+
+SINK_NONE = 0
+SINK_KEY0_BIAS = 1
+SINK_NULL_LOGIT = 2
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "lib", "libmvp.so")
+_lib = None
+_lock = threading.Lock()
+
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+_f = ctypes.c_float
+_sz = ctypes.c_size_t
+
+_SIGNATURES = {
+    "mvp_fill_query_ranges": (_i, [_vp, _i, _i, _vp, _vp, _i, _vp, _i, _vp, _vp]),
+    "mvp_attn_workspace_size": (_sz, [_i, _i, _i, _i]),
+    "mvp_attn_fwd_varlen": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i,
+                                 _vp, _vp, _i, _i, _i, _vp, _i, _f, _vp, _sz, _vp]),
+    "mvp_get_last_device_error": (_i, [_vp]),
+    "mvp_status_str": (ctypes.c_char_p, [_i]),
+    "mvp_last_launch_count": (_i, []),
+}
+
+
+class MvpError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        msg = load_library().mvp_status_str(status).decode()
+        super().__init__(f"{fn} failed: {msg} ({status})")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load the C-ABI library; raise if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise RuntimeError(
+                    f"{_LIB_PATH} is missing: build it with `python -m masked_varlen_prefill_gb300._build` "
+                    "(there is no CPU fallback)")
+            lib = ctypes.CDLL(_LIB_PATH)
+            for name, (res, args) in _SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check_cuda(name, t, dtype, device):
+    if t is None:
+        return
+    if not t.is_cuda or t.device != device:
+        raise ValueError(f"{name} must be a CUDA tensor on {device}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def fill_query_ranges(ranges, query_start_loc, seq_lens, out, num_tokens, rows_written=None, stream=None):
+    """Per-row range table (see ``mvp_fill_query_ranges`` in include/mvp.h).
+
+    ranges int32 [B, R, 2] (or None), query_start_loc int32 [B+1], seq_lens
+    int32 [B], out int32 [capacity, 2], rows_written int32 [1] or None;
+    num_tokens is a host int (== query_start_loc[-1]).
+    """
+    lib = load_library()
+    dev = out.device
+    for n, t in (("ranges", ranges), ("query_start_loc", query_start_loc), ("seq_lens", seq_lens),
+                 ("out", out), ("rows_written", rows_written)):
+        _check_cuda(n, t, torch.int32, dev)
+    num_reqs = seq_lens.shape[0]
+    max_ranges = 0 if ranges is None else ranges.shape[1]
+    if ranges is not None and (ranges.dim() != 3 or ranges.shape[0] != num_reqs or ranges.shape[2] != 2):
+        raise ValueError("ranges must be [num_reqs, max_ranges, 2]")
+    st = lib.mvp_fill_query_ranges(_ptr(ranges), num_reqs, max_ranges, _ptr(query_start_loc), _ptr(seq_lens),
+                                   int(num_tokens), _ptr(out), out.shape[0], _ptr(rows_written),
+                                   _stream(stream, dev))
+    if st != MVP_OK:
+        raise MvpError("mvp_fill_query_ranges", st)
+
+
+def attn_workspace_size(num_reqs, num_heads_q, head_dim, max_k_len) -> int:
+    return int(load_library().mvp_attn_workspace_size(num_reqs, num_heads_q, head_dim, max_k_len))
+
+
+def attn_fwd_varlen(q, k, v, out, cu_seqlens_q, cu_seqlens_k, max_q_len, max_k_len, *, lse=None,
+                    context_lens=None, range_table=None, range_covered=None, causal=True, window_left=-1,
+                    window_right=-1, sinks=None, sink_mode=SINK_NONE, scale=None, workspace=None,
+                    num_decode_reqs=-1, stream=None):
+    """Masked varlen attention forward (see ``mvp_attn_fwd_varlen``).
+
+    q [total_q, Hq, D], k/v [total_k, Hkv, D] bf16; out like q; lse fp32
+    [Hq, total_q] or None; cu_seqlens int32 [B+1]; the rest as in the header.
+    """
+    lib = load_library()
+    dev = q.device
+    for n, t in (("q", q), ("k", k), ("v", v), ("out", out)):
+        _check_cuda(n, t, torch.bfloat16, dev)
+    for n, t in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k), ("context_lens", context_lens),
+                 ("range_table", range_table), ("range_covered", range_covered)):
+        _check_cuda(n, t, torch.int32, dev)
+    _check_cuda("lse", lse, torch.float32, dev)
+    _check_cuda("sinks", sinks, torch.float32, dev)
+    if workspace is not None and (not workspace.is_cuda or not workspace.is_contiguous()):
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    if q.dim() != 3 or k.dim() != 3 or v.shape != k.shape or out.shape != q.shape:
+        raise ValueError("q/out must be [total_q, Hq, D] and k/v [total_k, Hkv, D]")
+    total_q, hq, d = q.shape
+    total_k, hkv, dk = k.shape
+    if dk != d:
+        raise ValueError("q and k head_dim differ")
+    num_reqs = cu_seqlens_q.shape[0] - 1
+    if scale is None:
+        scale = d ** -0.5
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.mvp_attn_fwd_varlen(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+        _ptr(context_lens), num_reqs, total_q, total_k, int(max_q_len), int(max_k_len), int(num_decode_reqs),
+        hq, hkv, d,
+        _ptr(range_table), _ptr(range_covered), int(bool(causal)), int(window_left), int(window_right),
+        _ptr(sinks), int(sink_mode), float(scale), _ptr(workspace), ws_bytes, _stream(stream, dev))
+    if st != MVP_OK:
+        raise MvpError("mvp_attn_fwd_varlen", st)
+
+
+def attn_fwd_varlen_host(q, k, v, cu_seqlens_q, cu_seqlens_k, max_q_len, max_k_len, *, device_buffers,
+                         want_lse=False, **kw):
+    """End-to-end call from HOST tensors: copy inputs into the given device
+    buffers, run ``attn_fwd_varlen`` and copy the output back to a pinned host
+    tensor.  ``device_buffers`` is a dict with preallocated 'q','k','v','out'
+    (and 'lse', 'cu_q', 'cu_k', plus any other device inputs already named in
+    ``kw``).  Returns the host output (and host lse)."""
+    dq, dk, dv, dout = (device_buffers[n] for n in ("q", "k", "v", "out"))
+    dq.copy_(q, non_blocking=True)
+    dk.copy_(k, non_blocking=True)
+    dv.copy_(v, non_blocking=True)
+    dcu_q = device_buffers["cu_q"]
+    dcu_k = device_buffers["cu_k"]
+    dcu_q.copy_(cu_seqlens_q, non_blocking=True)
+    dcu_k.copy_(cu_seqlens_k, non_blocking=True)
+    lse = device_buffers.get("lse") if want_lse else None
+    attn_fwd_varlen(dq, dk, dv, dout, dcu_q, dcu_k, max_q_len, max_k_len, lse=lse, **kw)
+    host_out = device_buffers["host_out"]
+    host_out.copy_(dout, non_blocking=True)
+    if lse is not None:
+        device_buffers["host_lse"].copy_(lse, non_blocking=True)
+    return host_out
+
+
+def get_last_device_error(stream=None) -> int:
+    """Synchronise and return (and clear) the library's device error status."""
+    lib = load_library()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    return int(lib.mvp_get_last_device_error(_stream(stream, dev)))
+
+
+def last_launch_count() -> int:
+    return int(load_library().mvp_last_launch_count())

@@ -1,0 +1,270 @@
+// C-ABI host layer: argument validation, TMA tensor-map encoding, launch
+// planning.  Declarations and argument contracts are in include/mvp.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <climits>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/mvp.h"
+#include "mvp_internal.cuh"
+
+namespace mvp {
+namespace {
+
+// One error word per device, living in this module's device memory: kernels
+// write a timeout code there (ptx.cuh), mvp_get_last_device_error reads it.
+__device__ int g_device_error_word;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mutex;
+int* g_err_ptr[kMaxDevices] = {};
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+thread_local int g_last_launches = 0;
+
+cudaError_t device_state(int** err_ptr) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (g_encode == nullptr) {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || fn == nullptr) return cudaErrorSymbolNotFound;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  if (g_err_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_device_error_word);
+    if (e != cudaSuccess) return e;
+    g_err_ptr[dev] = static_cast<int*>(ptr);
+  }
+  *err_ptr = g_err_ptr[dev];
+  return cudaSuccess;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// 3-D bf16 tensor [rows, heads, dim] (dim innermost) -> tiled TMA map.
+bool encode_3d(CUtensorMap* map, const void* base, int dim, int heads, int rows, int box_x, int box_y,
+               int box_z, bool swizzle128) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(dim), static_cast<cuuint64_t>(heads),
+                        static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(dim) * 2, static_cast<cuuint64_t>(heads) * dim * 2};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(box_x), static_cast<cuuint32_t>(box_y),
+                       static_cast<cuuint32_t>(box_z)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int largest_pow2_divisor(int g, int cap) {
+  int p = 1;
+  while (p * 2 <= cap && g % (p * 2) == 0) p *= 2;
+  return p;
+}
+
+constexpr int kDecodeChunk = 2048;
+constexpr int kMaxSplits = 64;
+
+}  // namespace
+}  // namespace mvp
+
+using namespace mvp;
+
+extern "C" {
+
+const char* mvp_status_str(int status) {
+  switch (status) {
+    case MVP_OK: return "ok";
+    case MVP_ERR_ARG: return "invalid argument";
+    case MVP_ERR_CAPACITY: return "output capacity too small";
+    case MVP_ERR_UNSUPPORTED: return "unsupported shape or alignment";
+    case MVP_ERR_CUDA: return "CUDA error";
+    case MVP_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int mvp_last_launch_count(void) { return g_last_launches; }
+
+int mvp_fill_query_ranges(const int32_t* ranges, int num_reqs, int max_ranges, const int32_t* query_start_loc,
+                          const int32_t* seq_lens, int num_tokens, int32_t* out, int out_capacity,
+                          int32_t* rows_written, void* stream) {
+  g_last_launches = 0;
+  if (num_reqs < 0 || max_ranges < 0 || num_tokens < 0 || out_capacity < 0) return MVP_ERR_ARG;
+  if (num_tokens > 0) {
+    if (num_reqs < 1 || query_start_loc == nullptr || seq_lens == nullptr || out == nullptr) return MVP_ERR_ARG;
+    if (max_ranges > 0 && ranges == nullptr) return MVP_ERR_ARG;
+    if (num_tokens > out_capacity) return MVP_ERR_CAPACITY;
+    if ((reinterpret_cast<uintptr_t>(out) & 7u) != 0) return MVP_ERR_UNSUPPORTED;
+    if (ranges != nullptr && (reinterpret_cast<uintptr_t>(ranges) & 7u) != 0) return MVP_ERR_UNSUPPORTED;
+  }
+  FillParams p;
+  p.ranges = ranges;
+  p.qsl = query_start_loc;
+  p.seq_lens = seq_lens;
+  p.out = out;
+  p.rows_written = rows_written;
+  p.num_reqs = num_reqs;
+  p.max_ranges = ranges ? max_ranges : 0;
+  p.num_tokens = num_tokens;
+  cudaError_t e = launch_fill(p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return MVP_ERR_CUDA;
+  g_last_launches = num_tokens > 0 ? 1 : 0;  // kernels only (the flag reset is a memset)
+  return MVP_OK;
+}
+
+size_t mvp_attn_workspace_size(int num_reqs, int num_heads_q, int head_dim, int max_k_len) {
+  if (num_reqs <= 0 || num_heads_q <= 0 || head_dim <= 0 || max_k_len <= 0) return 0;
+  int splits = (max_k_len + kDecodeChunk - 1) / kDecodeChunk;
+  if (splits > kMaxSplits) splits = kMaxSplits;
+  if (splits < 2) return 0;
+  return static_cast<size_t>(num_reqs) * num_heads_q * splits * (head_dim + 2) * sizeof(float);
+}
+
+int mvp_attn_fwd_varlen(const void* q, const void* k, const void* v, void* out, float* lse,
+                        const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, const int32_t* context_lens,
+                        int num_reqs, int total_q, int total_k, int max_q_len, int max_k_len,
+                        int num_decode_reqs, int num_heads_q, int num_heads_kv, int head_dim, const int32_t* range_table, const int32_t* range_covered,
+                        int causal, int window_left, int window_right, const float* sinks, int sink_mode,
+                        float scale, void* workspace, size_t workspace_bytes, void* stream) {
+  g_last_launches = 0;
+  // ------------------------------------------------------------ validation
+  if (num_reqs < 1 || num_reqs > 65535 || total_q < 0 || total_k < 0) return MVP_ERR_ARG;
+  if (num_heads_q < 1 || num_heads_kv < 1 || num_heads_q % num_heads_kv != 0) return MVP_ERR_ARG;
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256 && head_dim != 512) return MVP_ERR_UNSUPPORTED;
+  if (sink_mode < 0 || sink_mode > 2) return MVP_ERR_ARG;
+  if (sink_mode != 0 && sinks == nullptr) return MVP_ERR_ARG;
+  if (window_left < -1 || window_right < -1) return MVP_ERR_ARG;
+  if (causal != 0 && causal != 1) return MVP_ERR_ARG;
+  if (num_decode_reqs < -1 || num_decode_reqs > num_reqs) return MVP_ERR_ARG;
+  if (!(scale == scale)) return MVP_ERR_ARG;  // NaN
+  if (total_q == 0) return MVP_OK;
+  if (total_k < 1 || max_q_len < 1 || max_k_len < 1) return MVP_ERR_ARG;
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || cu_seqlens_q == nullptr ||
+      cu_seqlens_k == nullptr)
+    return MVP_ERR_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return MVP_ERR_UNSUPPORTED;
+  if (range_table != nullptr && (reinterpret_cast<uintptr_t>(range_table) & 7u) != 0) return MVP_ERR_UNSUPPORTED;
+  if (static_cast<long long>(total_q) * num_heads_q * head_dim >= (1LL << 40)) return MVP_ERR_UNSUPPORTED;
+
+  int* err = nullptr;
+  if (device_state(&err) != cudaSuccess) return MVP_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  MaskParams m;
+  m.cu_q = cu_seqlens_q;
+  m.cu_k = cu_seqlens_k;
+  m.ctx_lens = context_lens;
+  m.table = range_table;
+  m.covered = range_table ? range_covered : nullptr;
+  m.sinks = sink_mode ? sinks : nullptr;
+  m.causal = causal;
+  m.window_left = window_left;
+  m.window_right = causal ? 0 : window_right;
+  m.sink_mode = sink_mode;
+  m.scale_log2 = scale * 1.4426950408889634f;
+
+  const int group = num_heads_q / num_heads_kv;
+  int launches = 0;
+
+  const int prefill_first = num_decode_reqs < 0 ? 0 : num_decode_reqs;
+  const int decode_count = num_decode_reqs < 0 ? num_reqs : num_decode_reqs;
+
+  // ------------------------------------------------------------ prefill rows
+  if (max_q_len > 1 && prefill_first < num_reqs) {
+    const PrefillShape shape = prefill_tile_shape(head_dim);
+    const int gpack = largest_pow2_divisor(group, 8);
+    const int bmp = 128 / gpack;
+    PrefillParams pp;
+    pp.m = m;
+    pp.out = out;
+    pp.lse = lse;
+    pp.err = err;
+    pp.num_reqs = num_reqs;
+    pp.total_q = total_q;
+    pp.hq = num_heads_q;
+    pp.hkv = num_heads_kv;
+    pp.gpack = gpack;
+    pp.n_hgroups = group / gpack;
+    pp.n_qtiles = (max_q_len + bmp - 1) / bmp;
+    pp.skip_decode = 1;
+    pp.req_offset = prefill_first;
+    if (static_cast<long long>(num_heads_kv) * pp.n_hgroups * shape.dv_split > 65535) return MVP_ERR_UNSUPPORTED;
+    CUtensorMap mq, mk, mv;
+    if (!encode_3d(&mq, q, head_dim, num_heads_q, total_q, 64, gpack, bmp, true) ||
+        !encode_3d(&mk, k, head_dim, num_heads_kv, total_k, 64, 1, shape.bn, true) ||
+        !encode_3d(&mv, v, head_dim, num_heads_kv, total_k, 64, 1, shape.bn, true))
+      return MVP_ERR_UNSUPPORTED;
+    if (launch_prefill(head_dim, pp, mq, mk, mv, st) != cudaSuccess) return MVP_ERR_CUDA;
+    ++launches;
+  }
+
+  // ------------------------------------------------------------ decode rows
+  if (decode_count > 0) {
+    DecodeParams dp;
+    dp.m = m;
+    dp.q = q;
+    dp.out = out;
+    dp.lse = lse;
+    dp.err = err;
+    dp.num_reqs = decode_count;
+    dp.total_q = total_q;
+    dp.hq = num_heads_q;
+    dp.hkv = num_heads_kv;
+    dp.group = group;
+    long long span = max_k_len;
+    if (causal && window_left >= 0 && range_table == nullptr && context_lens == nullptr)
+      span = (window_left + 1LL < span) ? window_left + 1LL : span;
+    int splits = static_cast<int>((span + kDecodeChunk - 1) / kDecodeChunk);
+    if (splits > kMaxSplits) splits = kMaxSplits;
+    const size_t per_split = static_cast<size_t>(decode_count) * num_heads_q * (head_dim + 2) * sizeof(float);
+    if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 15u) != 0) splits = 1;
+    else if (static_cast<size_t>(splits) * per_split > workspace_bytes)
+      splits = static_cast<int>(workspace_bytes / per_split);
+    if (splits < 2) splits = 1;
+    const int kt = decode_keys_per_tile(head_dim);
+    long long chunk = (span + splits - 1) / splits;
+    chunk = ((chunk + kt - 1) / kt) * kt;
+    if (chunk > INT_MAX) chunk = INT_MAX;
+    dp.n_splits = splits;
+    dp.chunk = static_cast<int>(chunk);
+    dp.partial = splits > 1 ? static_cast<float*>(workspace) : nullptr;
+    const int per_cta = decode_heads_per_cta(head_dim, group);
+    if (static_cast<long long>(num_heads_kv) * ((group + per_cta - 1) / per_cta) > 65535) return MVP_ERR_UNSUPPORTED;
+    CUtensorMap mk, mv;
+    const int box = decode_box_inner(head_dim);
+    if (!encode_3d(&mk, k, head_dim, num_heads_kv, total_k, box, 1, kt, false) ||
+        !encode_3d(&mv, v, head_dim, num_heads_kv, total_k, box, 1, kt, false))
+      return MVP_ERR_UNSUPPORTED;
+    if (launch_decode(head_dim, dp, mk, mv, st, &launches) != cudaSuccess) return MVP_ERR_CUDA;
+  }
+  g_last_launches = launches;
+  return MVP_OK;
+}
+
+int mvp_get_last_device_error(void* stream) {
+  int* err = nullptr;
+  if (device_state(&err) != cudaSuccess) return MVP_ERR_CUDA;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MVP_ERR_CUDA;
+  int value = 0;
+  if (cudaMemcpy(&value, err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MVP_ERR_CUDA;
+  if (value != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return MVP_ERR_CUDA;
+    return MVP_ERR_DEVICE_TIMEOUT;
+  }
+  return MVP_OK;
+}
+
+}  // extern "C"

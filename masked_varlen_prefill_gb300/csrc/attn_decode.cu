@@ -1,0 +1,446 @@
+// Masked varlen attention forward, single-token (decode) rows, sm_103a.
+//
+// The step14_4 "Causal Mask optimisation" tutorial observes that a decode
+// query (seq_len == 1) needs no mask construction: it sees a contiguous run
+// of keys.  Here such a row's visible keys are the interval
+// [max(0, p - window_left), p] (plus, in general, the range part of
+// mask.cuh), read once per KV head for all the query heads that share it.
+//
+// This path is HBM-bound (each key is 2 * D bf16 of K and V used by G query
+// heads), so it is SIMT, not tensor-core work:
+// * A CTA handles one (request, KV head, key split).  A producer warp streams
+//   KT-key tiles of K and V into a 3-stage shared-memory ring with TMA; four
+//   compute warps read them back conflict-free (lane l owns D/32 consecutive
+//   dimensions of every key row).
+// * A warp takes KG = 32 / G keys at a time: each lane forms partial dot
+//   products for every (key, head) pair over its dimensions, and a shuffle
+//   reduce-scatter leaves lane l with the full score of pair l.  The online
+//   base-2 softmax and the p * V accumulation follow.
+// * Long rows are split across CTAs (split-KV); partial (acc, max, sum)
+//   triples are merged by decode_combine_kernel.  Without workspace every row
+//   is a single split and the CTA writes the final output itself.
+#include <cuda_bf16.h>
+
+#include "mask.cuh"
+#include "mvp_internal.cuh"
+#include "ptx.cuh"
+
+namespace mvp {
+
+namespace {
+
+constexpr int kNW = 4;                      // compute warps
+constexpr int kThreads = (kNW + 1) * 32;    // + producer warp
+constexpr int kStages = 3;
+constexpr unsigned kFull = 0xffffffffu;
+
+__host__ __device__ constexpr int kt_for(int d) { return d == 64 ? 128 : (d == 128 ? 64 : 32); }
+__host__ __device__ constexpr int box_for(int d) { return d > 256 ? 256 : d; }
+
+template <int D>
+struct DCfg {
+  static constexpr int DPL = D / 32;          // dims per lane
+  static constexpr int KT = kt_for(D);        // keys per tile
+  static constexpr int BOX = box_for(D);
+  static constexpr int NBOX = D / BOX;
+  static constexpr int TILE = KT * D * 2;     // bytes of one K (or V) tile
+  static constexpr int SMEM = kStages * 2 * TILE + 1024;
+};
+
+struct __align__(8) DBarriers {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  int abort_flag;
+};
+
+template <int DPL>
+__device__ __forceinline__ void load_row(const uint8_t* p, float (&x)[DPL]) {
+  if constexpr (DPL == 2) {
+    const uint32_t u = *reinterpret_cast<const uint32_t*>(p);
+    x[0] = __uint_as_float(u << 16);
+    x[1] = __uint_as_float(u & 0xffff0000u);
+  } else if constexpr (DPL == 4) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    x[0] = __uint_as_float(u.x << 16); x[1] = __uint_as_float(u.x & 0xffff0000u);
+    x[2] = __uint_as_float(u.y << 16); x[3] = __uint_as_float(u.y & 0xffff0000u);
+  } else {
+#pragma unroll
+    for (int c = 0; c < DPL / 8; ++c) {
+      const uint4 u = *reinterpret_cast<const uint4*>(p + c * 16);
+      x[8 * c + 0] = __uint_as_float(u.x << 16); x[8 * c + 1] = __uint_as_float(u.x & 0xffff0000u);
+      x[8 * c + 2] = __uint_as_float(u.y << 16); x[8 * c + 3] = __uint_as_float(u.y & 0xffff0000u);
+      x[8 * c + 4] = __uint_as_float(u.z << 16); x[8 * c + 5] = __uint_as_float(u.z & 0xffff0000u);
+      x[8 * c + 6] = __uint_as_float(u.w << 16); x[8 * c + 7] = __uint_as_float(u.w & 0xffff0000u);
+    }
+  }
+}
+
+// Byte offset of (key kk, this lane's dims) inside a tile stored as NBOX
+// boxes of [KT][BOX] bf16.
+template <int D>
+__device__ __forceinline__ int row_off(int kk, int lane) {
+  using C = DCfg<D>;
+  const int dim0 = lane * C::DPL;
+  const int box = dim0 / C::BOX;
+  return box * (C::KT * C::BOX * 2) + kk * (C::BOX * 2) + (dim0 % C::BOX) * 2;
+}
+
+template <int D, int GP>
+__global__ void __launch_bounds__(kThreads)
+    attn_decode_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+                       const DecodeParams p) {
+  using C = DCfg<D>;
+  constexpr int DPL = C::DPL;
+  constexpr int KG = 32 / GP;        // keys per warp step
+  constexpr int NG = C::KT / KG;     // warp steps per tile
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ DBarriers sb;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int sp = blockIdx.x;
+  const int b = blockIdx.y;
+  const int n_sub = (p.group + GP - 1) / GP;
+  const int hkv = blockIdx.z / n_sub;
+  const int sub = blockIdx.z % n_sub;
+  const int hq0 = hkv * p.group + sub * GP;       // first q head of this CTA
+  const int heads_here = min(GP, p.group - sub * GP);
+
+  const int q0 = __ldg(p.m.cu_q + b);
+  const int q_len = __ldg(p.m.cu_q + b + 1) - q0;
+  if (q_len != 1) return;
+  const int k0 = __ldg(p.m.cu_k + b);
+  const int k_len = __ldg(p.m.cu_k + b + 1) - k0;
+  const int pos = p.m.ctx_lens ? __ldg(p.m.ctx_lens + b) : (k_len - 1);
+  const RowVis vis = row_visibility(p.m, pos, k_len, table_active(p.m) ? q0 : -1);
+  int lo, hi;
+  vis.hull(lo, hi);
+  const int c_lo = lo + sp * p.chunk;
+  const int c_hi = (lo <= hi) ? min(hi, c_lo + p.chunk - 1) : -1;
+  const int n_keys = (lo <= hi && c_lo <= c_hi) ? (c_hi - c_lo + 1) : 0;
+  const int n_tiles = (n_keys + C::KT - 1) / C::KT;
+  const bool single = p.partial == nullptr;
+  if (n_keys == 0 && !single) {
+    // An empty split still publishes a neutral partial for the combine.
+    float* part = p.partial + ((static_cast<size_t>(b) * p.hq + hq0) * p.n_splits + sp) * (D + 2);
+    for (int g = 0; g < heads_here; ++g) {
+      float* pg = part + static_cast<size_t>(g) * p.n_splits * (D + 2);
+      for (int d = threadIdx.x; d < D + 2; d += blockDim.x) pg[d] = (d == D) ? -INFINITY : 0.f;
+    }
+    return;
+  }
+  if (n_keys == 0 && sp > 0) return;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sb.full[s], 1);
+      mbar_init(&sb.empty[s], kNW);
+    }
+    sb.abort_flag = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+
+  if (warp == kNW) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0 && n_tiles > 0) {
+      tma_prefetch_desc(&map_k);
+      tma_prefetch_desc(&map_v);
+      int issued = 0;
+      bool ok = true;
+      for (int t = 0; t < n_tiles; ++t) {
+        const int s = t % kStages;
+        if (t >= kStages &&
+            !mbar_wait(&sb.empty[s], ((t / kStages) - 1) & 1, &sb.abort_flag, p.err, kDevTimeoutLoad)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&sb.full[s], 2 * C::TILE);
+        uint8_t* ks = smem + s * 2 * C::TILE;
+        uint8_t* vs = ks + C::TILE;
+        const int row = k0 + c_lo + t * C::KT;
+#pragma unroll
+        for (int x = 0; x < C::NBOX; ++x) {
+          tma_load_3d(ks + x * (C::KT * C::BOX * 2), &map_k, &sb.full[s], x * C::BOX, hkv, row);
+          tma_load_3d(vs + x * (C::KT * C::BOX * 2), &map_v, &sb.full[s], x * C::BOX, hkv, row);
+        }
+        ++issued;
+      }
+      if (!ok) sb.abort_flag = 1;
+      volatile int own_flag = 0;
+      for (int s = 0; s < kStages && s < issued; ++s) {
+        const int last = ((issued - 1 - s) / kStages) * kStages + s;
+        mbar_wait(&sb.full[s], (last / kStages) & 1, &own_flag, nullptr, 0);
+      }
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------------ compute
+  // q for this lane's dims, every head of the CTA, pre-scaled to log2 units.
+  float qf[GP][DPL];
+#pragma unroll
+  for (int g = 0; g < GP; ++g) {
+    float tmp[DPL];
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) tmp[d] = 0.f;
+    if (g < heads_here) {
+      const uint8_t* src = reinterpret_cast<const uint8_t*>(p.q) +
+                           ((static_cast<size_t>(q0) * p.hq + hq0 + g) * D + lane * DPL) * 2;
+      load_row<DPL>(src, tmp);
+    }
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) qf[g][d] = tmp[d] * p.m.scale_log2;
+  }
+  const int my_g = lane % GP;
+  const bool key0_mode = p.m.sink_mode == 1 && p.m.sinks != nullptr;
+  float my_sink = 0.f;
+  if (key0_mode && my_g < heads_here) my_sink = __ldg(p.m.sinks + hq0 + my_g) * 1.4426950408889634f;
+
+  float m[GP], acc[GP][DPL];
+  float l_part = 0.f;
+#pragma unroll
+  for (int g = 0; g < GP; ++g) {
+    m[g] = -INFINITY;
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) acc[g][d] = 0.f;
+  }
+
+  bool ok = true;
+  for (int t = 0; t < n_tiles && ok; ++t) {
+    const int s = t % kStages;
+    if (!mbar_wait(&sb.full[s], (t / kStages) & 1, &sb.abort_flag, p.err, kDevTimeoutLoad)) {
+      ok = false;
+      break;
+    }
+    const uint8_t* ks = smem + s * 2 * C::TILE;
+    const uint8_t* vs = ks + C::TILE;
+    for (int gi = warp; gi < NG; gi += kNW) {
+      float v[32];
+#pragma unroll
+      for (int kk = 0; kk < KG; ++kk) {
+        float kr[DPL];
+        load_row<DPL>(ks + row_off<D>(gi * KG + kk, lane), kr);
+#pragma unroll
+        for (int g = 0; g < GP; ++g) {
+          float a = 0.f;
+#pragma unroll
+          for (int d = 0; d < DPL; ++d) a = fmaf(qf[g][d], kr[d], a);
+          v[kk * GP + g] = a;
+        }
+      }
+      // reduce-scatter: lane l ends with the full sum of pair l
+#pragma unroll
+      for (int o = 16, n = 16; o >= 1; o >>= 1, n >>= 1) {
+        const bool upper = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < n; ++i) {
+          const float send = upper ? v[i] : v[i + n];
+          const float keep = upper ? v[i + n] : v[i];
+          v[i] = keep + __shfl_xor_sync(kFull, send, o);
+        }
+      }
+      const int key = c_lo + t * C::KT + gi * KG + lane / GP;
+      float x = v[0];
+      if (key0_mode && key == 0) x += my_sink;
+      const bool visible = key <= c_hi && vis.visible(key);
+      x = visible ? x : -INFINITY;
+      // per-head max over this step's keys
+      float mx = x;
+#pragma unroll
+      for (int o = GP; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+      float alpha[GP];
+#pragma unroll
+      for (int g = 0; g < GP; ++g) {
+        const float gm = __shfl_sync(kFull, mx, g);
+        const float mn = fmaxf(m[g], gm);
+        alpha[g] = (mn == -INFINITY) ? 1.f : ex2_approx(m[g] - mn);
+        m[g] = mn;
+      }
+      float my_m = m[0];
+#pragma unroll
+      for (int g = 1; g < GP; ++g) my_m = (my_g == g) ? m[g] : my_m;
+      float my_alpha = alpha[0];
+#pragma unroll
+      for (int g = 1; g < GP; ++g) my_alpha = (my_g == g) ? alpha[g] : my_alpha;
+      const float pr = (x == -INFINITY) ? 0.f : ex2_approx(x - my_m);
+      l_part = l_part * my_alpha + pr;
+#pragma unroll
+      for (int g = 0; g < GP; ++g)
+#pragma unroll
+        for (int d = 0; d < DPL; ++d) acc[g][d] *= alpha[g];
+#pragma unroll
+      for (int kk = 0; kk < KG; ++kk) {
+        float vr[DPL];
+        load_row<DPL>(vs + row_off<D>(gi * KG + kk, lane), vr);
+#pragma unroll
+        for (int g = 0; g < GP; ++g) {
+          const float pg = __shfl_sync(kFull, pr, kk * GP + g);
+#pragma unroll
+          for (int d = 0; d < DPL; ++d) acc[g][d] = fmaf(pg, vr[d], acc[g][d]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sb.empty[s]);
+  }
+
+  // per-head sums: lanes holding the same head
+#pragma unroll
+  for (int o = GP; o < 32; o <<= 1) l_part += __shfl_xor_sync(kFull, l_part, o);
+
+  // ------------------------------------------------------------------ merge warps
+  // Stage buffers are free once every tile was consumed by every warp.
+  asm volatile("bar.sync 1, %0;" ::"r"(kNW * 32) : "memory");
+  float* sm = reinterpret_cast<float*>(smem);                 // [kNW][GP][D]
+  float* sml = sm + kNW * GP * D;                              // [kNW][GP][2]
+#pragma unroll
+  for (int g = 0; g < GP; ++g)
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) sm[(warp * GP + g) * D + lane * DPL + d] = acc[g][d];
+  if (lane < GP) {
+    float mm = m[0];
+#pragma unroll
+    for (int g = 1; g < GP; ++g) mm = (lane == g) ? m[g] : mm;
+    sml[(warp * GP + lane) * 2 + 0] = mm;
+    sml[(warp * GP + lane) * 2 + 1] = l_part;  // lane g holds head g's sum
+  }
+  asm volatile("bar.sync 1, %0;" ::"r"(kNW * 32) : "memory");
+
+  const bool null_mode = p.m.sink_mode == 2 && p.m.sinks != nullptr;
+  for (int idx = threadIdx.x; idx < heads_here * D; idx += kNW * 32) {
+    const int g = idx / D, d = idx % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kNW; ++w) M = fmaxf(M, sml[(w * GP + g) * 2]);
+    float a = 0.f, L = 0.f;
+#pragma unroll
+    for (int w = 0; w < kNW; ++w) {
+      const float mw = sml[(w * GP + g) * 2];
+      const float f = (mw == -INFINITY) ? 0.f : ex2_approx(mw - M);
+      a += f * sm[(w * GP + g) * D + d];
+      L += f * sml[(w * GP + g) * 2 + 1];
+    }
+    const int h = hq0 + g;
+    if (!single) {
+      float* part = p.partial + ((static_cast<size_t>(b) * p.hq + h) * p.n_splits + sp) * (D + 2);
+      part[d] = a;
+      if (d == 0) {
+        part[D] = M;
+        part[D + 1] = L;
+      }
+    } else {
+      if (null_mode) {
+        const float sk = __ldg(p.m.sinks + h) * 1.4426950408889634f;
+        const float M2 = fmaxf(M, sk);
+        const float f = (M == -INFINITY) ? 0.f : ex2_approx(M - M2);
+        a *= f;
+        L = L * f + ex2_approx(sk - M2);
+        M = M2;
+      }
+      const float inv = (L > 0.f) ? 1.f / L : 0.f;
+      reinterpret_cast<__nv_bfloat16*>(p.out)[(static_cast<size_t>(q0) * p.hq + h) * D + d] =
+          __float2bfloat16_rn(a * inv);
+      if (d == 0 && p.lse != nullptr) {
+        const float mu = (M == -INFINITY) ? 0.f : M;
+        p.lse[static_cast<size_t>(h) * p.total_q + q0] =
+            (L > 0.f) ? (mu + lg2_approx(L)) * 0.6931471805599453f : -INFINITY;
+      }
+    }
+  }
+  (void)ok;
+}
+
+// One warp per (request, q head): merge the split partials of a decode row.
+template <int D>
+__global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams p) {
+  const int warp_global = blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (warp_global >= p.num_reqs * p.hq) return;
+  const int b = warp_global / p.hq;
+  const int h = warp_global % p.hq;
+  const int q0 = __ldg(p.m.cu_q + b);
+  if (__ldg(p.m.cu_q + b + 1) - q0 != 1) return;
+  const float* part = p.partial + (static_cast<size_t>(b) * p.hq + h) * p.n_splits * (D + 2);
+  float M = -INFINITY;
+  for (int s = 0; s < p.n_splits; ++s) M = fmaxf(M, part[s * (D + 2) + D]);
+  const bool null_mode = p.m.sink_mode == 2 && p.m.sinks != nullptr;
+  float sk = 0.f;
+  if (null_mode) {
+    sk = __ldg(p.m.sinks + h) * 1.4426950408889634f;
+    M = fmaxf(M, sk);
+  }
+  float L = null_mode ? ex2_approx(sk - M) : 0.f;
+  for (int s = 0; s < p.n_splits; ++s) {
+    const float ms = part[s * (D + 2) + D];
+    if (ms != -INFINITY) L += part[s * (D + 2) + D + 1] * ex2_approx(ms - M);
+  }
+  const float inv = (L > 0.f) ? 1.f / L : 0.f;
+  for (int d = lane; d < D; d += 32) {
+    float a = 0.f;
+    for (int s = 0; s < p.n_splits; ++s) {
+      const float ms = part[s * (D + 2) + D];
+      if (ms != -INFINITY) a += part[s * (D + 2) + d] * ex2_approx(ms - M);
+    }
+    reinterpret_cast<__nv_bfloat16*>(p.out)[(static_cast<size_t>(q0) * p.hq + h) * D + d] =
+        __float2bfloat16_rn(a * inv);
+  }
+  if (lane == 0 && p.lse != nullptr) {
+    const float mu = (M == -INFINITY) ? 0.f : M;
+    p.lse[static_cast<size_t>(h) * p.total_q + q0] =
+        (L > 0.f) ? (mu + lg2_approx(L)) * 0.6931471805599453f : -INFINITY;
+  }
+}
+
+template <int D, int GP>
+cudaError_t launch_dg(const DecodeParams& p, const CUtensorMap& mk, const CUtensorMap& mv, cudaStream_t stream) {
+  auto kern = attn_decode_kernel<D, GP>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DCfg<D>::SMEM);
+  if (e != cudaSuccess) return e;
+  const int n_sub = (p.group + GP - 1) / GP;
+  dim3 grid(p.n_splits, p.num_reqs, p.hkv * n_sub);
+  kern<<<grid, kThreads, DCfg<D>::SMEM, stream>>>(mk, mv, p);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_d(const DecodeParams& p, const CUtensorMap& mk, const CUtensorMap& mv, cudaStream_t stream,
+                     int* launches) {
+  // Heads per CTA: the group padded to a power of two, capped so that q and
+  // the accumulators (2 * GP * D / 32 floats per lane) stay in registers.
+  cudaError_t e;
+  if (p.group == 1) e = launch_dg<D, 1>(p, mk, mv, stream);
+  else if (p.group == 2) e = launch_dg<D, 2>(p, mk, mv, stream);
+  else if (p.group <= 4 || D >= 512) e = launch_dg<D, 4>(p, mk, mv, stream);
+  else if constexpr (D < 512) e = launch_dg<D, 8>(p, mk, mv, stream);
+  else e = cudaErrorInvalidValue;
+  if (e != cudaSuccess) return e;
+  ++*launches;
+  if (p.partial != nullptr) {
+    const int warps = p.num_reqs * p.hq;
+    decode_combine_kernel<D><<<(warps + 3) / 4, 128, 0, stream>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    ++*launches;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace
+
+int decode_keys_per_tile(int head_dim) { return kt_for(head_dim); }
+int decode_box_inner(int head_dim) { return box_for(head_dim); }
+
+cudaError_t launch_decode(int head_dim, const DecodeParams& p, const CUtensorMap& mk, const CUtensorMap& mv,
+                          cudaStream_t stream, int* launches) {
+  switch (head_dim) {
+    case 64: return launch_d<64>(p, mk, mv, stream, launches);
+    case 128: return launch_d<128>(p, mk, mv, stream, launches);
+    case 256: return launch_d<256>(p, mk, mv, stream, launches);
+    case 512: return launch_d<512>(p, mk, mv, stream, launches);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace mvp

@@ -1,0 +1,92 @@
+// Per-query-row visibility as two closed key intervals.
+//
+// For a query at absolute position p of a request with k_len keys:
+//   base  = keys allowed by the causal / sliding-window rule
+//           (step14_4 tutorial: j > p is masked when causal; vLLM PR #50294
+//           mask_mod: the window keeps j >= p - window_left; PR #49815: a
+//           symmetric window also keeps j <= p + window_right)
+//   range = the row's closed [start, end] from the range table, clamped on
+//           the past side by the same window (PR #50294 mask_mod)
+// visible = base OR range.  When the table row comes from the fill (its range
+// holds p), the two intervals touch at p, so the union is one interval; an
+// arbitrary caller table may give two disjoint intervals, which the per-key
+// test below still handles exactly.
+#pragma once
+
+#include <climits>
+#include <cstdint>
+
+#include "mvp_internal.cuh"
+
+namespace mvp {
+
+struct RowVis {
+  int b_lo, b_hi;  // base interval (empty when b_lo > b_hi)
+  int r_lo, r_hi;  // range interval (empty when r_lo > r_hi)
+
+  __device__ __forceinline__ bool visible(int j) const {
+    return (j >= b_lo && j <= b_hi) || (j >= r_lo && j <= r_hi);
+  }
+  __device__ __forceinline__ bool base_empty() const { return b_lo > b_hi; }
+  __device__ __forceinline__ bool range_empty() const { return r_lo > r_hi; }
+  // Smallest interval holding every visible key (empty: lo > hi).
+  __device__ __forceinline__ void hull(int& lo, int& hi) const {
+    lo = INT_MAX;
+    hi = INT_MIN;
+    if (!base_empty()) { lo = b_lo; hi = b_hi; }
+    if (!range_empty()) { lo = min(lo, r_lo); hi = max(hi, r_hi); }
+  }
+  // An interval of keys that are ALL visible (conservative when the two
+  // intervals are disjoint: then only the base interval is reported).
+  __device__ __forceinline__ void core(int& lo, int& hi) const {
+    const bool be = base_empty(), re = range_empty();
+    if (be && re) { lo = INT_MAX; hi = INT_MIN; return; }
+    if (be) { lo = r_lo; hi = r_hi; return; }
+    if (re) { lo = b_lo; hi = b_hi; return; }
+    if (r_lo <= b_hi + 1 && b_lo <= r_hi + 1) { lo = min(b_lo, r_lo); hi = max(b_hi, r_hi); return; }
+    lo = b_lo;
+    hi = b_hi;
+  }
+};
+
+__device__ __forceinline__ RowVis empty_row() {
+  RowVis v;
+  v.b_lo = 1; v.b_hi = 0; v.r_lo = 1; v.r_hi = 0;
+  return v;
+}
+
+// p: absolute query position; k_len: keys of the request; table_row: packed
+// row index of this query, or -1 when the range part is off.
+__device__ __forceinline__ RowVis row_visibility(const MaskParams& m, int p, int k_len, int table_row) {
+  RowVis v;
+  const long long wl = m.window_left, wr = m.window_right;
+  long long lo = (wl >= 0) ? (long long)p - wl : 0;
+  if (lo < 0) lo = 0;
+  long long hi;
+  if (m.causal) hi = p;
+  else hi = (wr >= 0) ? (long long)p + wr : (long long)k_len - 1;
+  if (hi > k_len - 1) hi = k_len - 1;
+  v.b_lo = (int)lo;
+  v.b_hi = (int)hi;
+  v.r_lo = 1;
+  v.r_hi = 0;
+  if (table_row >= 0) {
+    const int2 e = __ldg(reinterpret_cast<const int2*>(m.table) + table_row);
+    long long rl = e.x;
+    if (wl >= 0 && (long long)p - wl > rl) rl = (long long)p - wl;
+    if (rl < 0) rl = 0;
+    long long rh = e.y;
+    if (rh > k_len - 1) rh = k_len - 1;
+    v.r_lo = (int)rl;
+    v.r_hi = (int)rh;
+  }
+  return v;
+}
+
+__device__ __forceinline__ bool table_active(const MaskParams& m) {
+  if (m.table == nullptr) return false;
+  if (m.covered == nullptr) return true;
+  return *reinterpret_cast<const volatile int32_t*>(m.covered) != 0;
+}
+
+}  // namespace mvp

@@ -1,0 +1,99 @@
+// Internal launch interfaces shared by the C-ABI layer and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace mvp {
+
+// ----------------------------------------------------------------- fill
+struct FillParams {
+  const int32_t* ranges;    // [num_reqs, max_ranges, 2]
+  const int32_t* qsl;       // [num_reqs + 1]
+  const int32_t* seq_lens;  // [num_reqs]
+  int32_t* out;             // [num_tokens, 2]
+  int32_t* rows_written;    // device scalar or null
+  int num_reqs;
+  int max_ranges;
+  int num_tokens;
+};
+
+cudaError_t launch_fill(const FillParams& p, cudaStream_t stream);
+
+// ----------------------------------------------------------------- masks
+// Per-row visible set = base interval U range interval (closed, in key
+// coordinates of the request).  Shared by the prefill and decode kernels.
+struct MaskParams {
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  const int32_t* ctx_lens;   // or null
+  const int32_t* table;      // [total_q, 2] or null
+  const int32_t* covered;    // device scalar or null
+  const float* sinks;        // [hq] or null
+  int causal;
+  int window_left;           // -1 = unbounded
+  int window_right;          // -1 = unbounded (non-causal only)
+  int sink_mode;
+  float scale_log2;          // scale * log2(e)
+};
+
+// ----------------------------------------------------------------- prefill
+struct PrefillParams {
+  MaskParams m;
+  void* out;          // bf16 [total_q, hq, D]
+  float* lse;         // [hq, total_q] or null
+  int* err;           // device error word
+  int num_reqs;
+  int total_q;
+  int hq;
+  int hkv;
+  int gpack;          // q heads packed into one 128-row tile (power of two)
+  int n_hgroups;      // (hq / hkv) / gpack
+  int n_qtiles;       // ceil(max_q_len / (128 / gpack))
+  int skip_decode;    // requests with q_len == 1 are left to the decode kernel
+  int req_offset;     // first request of the grid (grid.y covers the rest)
+};
+
+// head_dim in {64, 128, 256, 512}.  Tensor maps are encoded by the caller
+// (see api.cu) for the tile shapes prefill_tile_shape() reports.
+struct PrefillShape {
+  int bn;        // keys per tile
+  int dv_cta;    // value columns per CTA
+  int dv_split;  // CTAs per (q tile, head group) along the value dimension
+};
+PrefillShape prefill_tile_shape(int head_dim);
+
+cudaError_t launch_prefill(int head_dim, const PrefillParams& p, const CUtensorMap& map_q,
+                           const CUtensorMap& map_k, const CUtensorMap& map_v, cudaStream_t stream);
+
+// ----------------------------------------------------------------- decode
+struct DecodeParams {
+  MaskParams m;
+  const void* q;        // bf16 [total_q, hq, D]
+  void* out;            // bf16 [total_q, hq, D]
+  float* lse;           // [hq, total_q] or null
+  float* partial;       // [num_reqs, hq, n_splits, D + 2] or null (single split)
+  int* err;
+  int num_reqs;         // requests covered by the decode grid: [0, num_reqs)
+  int total_q;
+  int hq;
+  int hkv;
+  int group;            // hq / hkv
+  int n_splits;
+  int chunk;            // keys per split
+};
+
+cudaError_t launch_decode(int head_dim, const DecodeParams& p, const CUtensorMap& map_k,
+                          const CUtensorMap& map_v, cudaStream_t stream, int* launches);
+int decode_keys_per_tile(int head_dim);
+int decode_box_inner(int head_dim);
+// Heads one decode CTA handles for a GQA group of `group` query heads.
+inline int decode_heads_per_cta(int head_dim, int group) {
+  if (group == 1) return 1;
+  if (group == 2) return 2;
+  if (group <= 4 || head_dim >= 512) return 4;
+  return 8;
+}
+
+}  // namespace mvp

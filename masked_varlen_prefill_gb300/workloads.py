@@ -264,3 +264,46 @@ def random_tiny(seed: int) -> Workload:
     ranges = pad_ranges(per_req) if rng.integers(0, 2) else None
     return Workload(f"tiny{seed}", seed, q_lens, k_lens, hq, hkv, d, causal, wl, wr, mode, ranges,
                     scale=float(rng.choice([0.5, 1.0 / math.sqrt(d)])))
+
+
+def random_case(seed: int, max_q: int = 300, max_ctx: int = 600) -> Workload:
+    """A random case of a shape the GPU kernels support (D 64..512, GQA
+    groups 1..8), covering every mask / sink flag combination, q_len 0 and 1
+    members, ragged lengths and ranges longer than the window."""
+    rng = np.random.default_rng(10_000 + seed)
+    d = int(rng.choice([64, 128, 256, 512]))
+    hkv = int(rng.choice([1, 2]))
+    group = int(rng.choice([1, 2, 3, 4, 8]))
+    if d == 512:
+        group = min(group, 4)
+    b = int(rng.integers(1, 5))
+    q_lens, k_lens = [], []
+    for _ in range(b):
+        kind = rng.integers(0, 6)
+        ql = 0 if kind == 0 else (1 if kind == 1 else int(rng.integers(2, max_q + 1)))
+        ctx = int(rng.integers(0, max_ctx + 1)) if rng.integers(0, 2) else 0
+        q_lens.append(ql)
+        k_lens.append(ql + ctx)
+    if sum(q_lens) == 0:
+        q_lens[0] = 5
+        k_lens[0] += 5
+    causal = bool(rng.integers(0, 3) > 0)
+    wl = int(rng.choice([-1, 0, 7, 63, 130, 400]))
+    wr = int(rng.choice([-1, 0, 5, 77])) if not causal else 0
+    mode = int(rng.integers(0, 3))
+    ranges = None
+    if rng.integers(0, 2):
+        per_req = []
+        for ql, kl in zip(q_lens, k_lens):
+            rl, cur = [], int(rng.integers(0, max(1, kl // 2 + 1)))
+            for _ in range(int(rng.integers(0, 6))):
+                length = int(rng.integers(1, 200))
+                e = cur + length - 1
+                if rng.integers(0, 8) == 0:
+                    e = cur - int(rng.integers(0, 3))
+                rl.append((cur, e))
+                cur = cur + length + int(rng.integers(1, 40))
+            per_req.append(rl)
+        ranges = pad_ranges(per_req)
+    return Workload(f"rand{seed}", 20_000 + seed, q_lens, k_lens, hkv * group, hkv, d, causal, wl, wr,
+                    mode, ranges, scale=float(rng.choice([1.0 / math.sqrt(d), 0.05])))

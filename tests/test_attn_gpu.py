@@ -1,0 +1,141 @@
+"""Attention forward through the C-ABI vs the float64 oracle (GPU).
+
+* scaled versions of every workload, compared element by element;
+* random shapes over every flag combination (D 64..512, GQA 1..8, q_len 0/1,
+  ragged tails, windows shorter than a tile, ranges longer than the window);
+* the full-size workloads in the launch configuration the benchmark times,
+  compared on sampled rows that the oracle computes one by one.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from masked_varlen_prefill_gb300 import workloads
+
+from . import gpu_helpers as gh
+
+pytestmark = pytest.mark.gpu
+
+
+def _parity_full(w, use_workspace=True, num_decode_reqs=-1):
+    q, k, v, sinks = gh.make_inputs(w)
+    out, lse, table, covered = gh.run_gpu(w, q, k, v, sinks, use_workspace=use_workspace,
+                                          num_decode_reqs=num_decode_reqs)
+    ref_table, n = gh.oracle_table(w)
+    if ref_table is not None:
+        got = table[:w.total_q].cpu().numpy()
+        if n:
+            assert np.array_equal(got, ref_table), "range table"
+        else:
+            assert (got == -1).all()
+        assert int(covered.item()) == n
+    ro, rl = gh.oracle_full(w, q, k, v, sinks, ref_table)
+    return gh.compare(out, lse, ro, rl, what=w.name)
+
+
+@pytest.mark.parametrize("name", workloads.WORKLOADS)
+def test_scaled_workloads(name):
+    _parity_full(workloads.scaled_workload(name))
+
+
+@pytest.mark.parametrize("seed", range(48))
+def test_random_cases(seed):
+    _parity_full(workloads.random_case(seed))
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_cases_without_workspace(seed):
+    _parity_full(workloads.random_case(100 + seed), use_workspace=False)
+
+
+@pytest.mark.parametrize("d", [64, 128, 256, 512])
+@pytest.mark.parametrize("group", [1, 2, 4])
+def test_head_dims_and_groups(d, group):
+    w = workloads.Workload(f"d{d}g{group}", 7 + d + group, [200, 1, 77, 130], [450, 900, 77, 300],
+                           2 * group, 2, d, True, 150, 0, workloads.SINK_NULL_LOGIT, None)
+    _parity_full(w)
+
+
+def test_key0_bias_with_key0_outside_window():
+    # rows beyond the window never see key 0: the bias must not touch them
+    w = workloads.Workload("k0", 3, [300], [300], 4, 2, 128, False, 20, 20, workloads.SINK_KEY0_BIAS, None)
+    _parity_full(w)
+
+
+def test_ranges_longer_than_window():
+    per = [[(10, 400), (420, 421), (600, 999)]]
+    w = workloads.Workload("longrange", 5, [700], [1000], 4, 2, 128, True, 31, 0, workloads.SINK_NONE,
+                           workloads.pad_ranges(per))
+    _parity_full(w)
+
+
+def test_empty_and_single_rows():
+    w = workloads.Workload("edges", 9, [0, 1, 0, 129, 1], [0, 1, 5, 129, 2000], 8, 2, 128, True, -1, 0,
+                           workloads.SINK_NULL_LOGIT, None)
+    _parity_full(w)
+
+
+def test_window_zero_one_key_per_row():
+    w = workloads.Workload("w0", 11, [257], [257], 2, 1, 256, True, 0, 0, workloads.SINK_KEY0_BIAS, None)
+    _parity_full(w)
+
+
+@pytest.mark.parametrize("name", ["mixed_serving_a", "mixed_serving_b"])
+def test_decode_first_batches(name):
+    # decode requests first: each kernel covers only its own requests
+    w = workloads.scaled_workload(name)
+    n_dec = sum(1 for x in w.q_lens if x == 1)
+    assert w.q_lens[:n_dec] == [1] * n_dec
+    _parity_full(w, num_decode_reqs=n_dec)
+    _parity_full(w, num_decode_reqs=n_dec, use_workspace=False)
+
+
+def test_prefill_only_and_decode_only_batches():
+    w = workloads.scaled_workload("mm_prefix_sliding")
+    w.q_lens, w.k_lens = [517, 300, 129], [517, 300, 129]
+    w.ranges = w.ranges[[0, 1, 3]]
+    _parity_full(w, num_decode_reqs=0)
+    d = workloads.Workload("dec", 5, [1] * 7, [1, 2, 700, 5000, 64, 9000, 333], 8, 2, 128, True, 1000, 0,
+                           workloads.SINK_KEY0_BIAS, None)
+    _parity_full(d, num_decode_reqs=7)
+    _parity_full(d, num_decode_reqs=-1)
+
+
+FULL = ["tiny_window_sinks", "mm_prefix_sliding", "global_causal_d512", "chunked_prefill_ranges",
+        "mixed_serving_a", "mixed_serving_b"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled_rows(name):
+    """Full-size workload, bench launch configuration (workspace on), sampled
+    rows: first/last rows of requests, tile boundaries, random interior rows,
+    every decode row of a few requests."""
+    w = workloads.workload(name)
+    q, k, v, sinks = gh.make_inputs(w)
+    n_dec = 0
+    while n_dec < w.num_reqs and w.q_lens[n_dec] == 1:
+        n_dec += 1
+    out, lse, table, covered = gh.run_gpu(w, q, k, v, sinks, num_decode_reqs=n_dec)
+    ref_table, n = gh.oracle_table(w)
+    if ref_table is not None:
+        got = table[:w.total_q].cpu().numpy()
+        assert np.array_equal(got, ref_table) if n else (got == -1).all()
+    cu_q, _ = w.cu_seqlens()
+    rng = np.random.default_rng(1234)
+    rows = set()
+    for b in range(w.num_reqs):
+        q0, q1 = int(cu_q[b]), int(cu_q[b + 1])
+        if q1 == q0:
+            continue
+        if q1 - q0 == 1:
+            if rng.random() < 0.06:
+                rows.add(q0)
+            continue
+        rows.update([q0, q1 - 1, min(q1 - 1, q0 + 63), min(q1 - 1, q0 + 64), min(q1 - 1, q0 + 127)])
+        rows.update(int(x) for x in rng.integers(q0, q1, size=6))
+    rows = sorted(rows)
+    ro, rl = gh.oracle_rows(w, q, k, v, sinks, ref_table, rows)
+    gh.compare(out, lse, ro, rl, rows=rows, what=name)
+    # every output is finite (no NaN from unwritten rows)
+    assert torch.isfinite(out.float()).all()

@@ -1,0 +1,97 @@
+"""The C-ABI library: it loads, exports what include/mvp.h declares, and
+rejects bad arguments on the host before touching a GPU (no GPU needed)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import masked_varlen_prefill_gb300 as mvp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            names.update(re.findall(r"\b(mvp_\w+)\s*\(", src))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(mvp.library_path()):
+        from masked_varlen_prefill_gb300 import _build
+
+        _build.build()
+    return mvp.load_library()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert "mvp_fill_query_ranges" in names and "mvp_attn_fwd_varlen" in names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code in (0, -1, -2, -3, -4, -5):
+        assert lib.mvp_status_str(code).decode() != "unknown status"
+    assert lib.mvp_status_str(99).decode() == "unknown status"
+
+
+def _attn(lib, **over):
+    args = dict(q=1 << 20, k=1 << 20, v=1 << 20, out=1 << 20, lse=None, cu_q=1 << 20, cu_k=1 << 20, ctx=None,
+                num_reqs=1, total_q=4, total_k=4, max_q=4, max_k=4, ndec=-1, hq=4, hkv=2, d=128, table=None,
+                covered=None, causal=1, wl=-1, wr=-1, sinks=None, sink_mode=0, scale=0.1, ws=None, ws_bytes=0,
+                stream=None)
+    args.update(over)
+    return lib.mvp_attn_fwd_varlen(*[args[k] for k in (
+        "q", "k", "v", "out", "lse", "cu_q", "cu_k", "ctx", "num_reqs", "total_q", "total_k", "max_q", "max_k", "ndec",
+        "hq", "hkv", "d", "table", "covered", "causal", "wl", "wr", "sinks", "sink_mode", "scale", "ws",
+        "ws_bytes", "stream")])
+
+
+def test_argument_errors_return_before_any_launch(lib):
+    # None of these reach a CUDA call: validation runs first on the host.
+    assert _attn(lib, d=96) == mvp.MVP_ERR_UNSUPPORTED
+    assert _attn(lib, hq=3, hkv=2) == mvp.MVP_ERR_ARG
+    assert _attn(lib, num_reqs=0) == mvp.MVP_ERR_ARG
+    assert _attn(lib, sink_mode=1, sinks=None) == mvp.MVP_ERR_ARG
+    assert _attn(lib, sink_mode=3) == mvp.MVP_ERR_ARG
+    assert _attn(lib, wl=-2) == mvp.MVP_ERR_ARG
+    assert _attn(lib, causal=2) == mvp.MVP_ERR_ARG
+    assert _attn(lib, q=None) == mvp.MVP_ERR_ARG
+    assert _attn(lib, q=(1 << 20) + 8) == mvp.MVP_ERR_UNSUPPORTED  # not 16-byte aligned
+    assert _attn(lib, total_k=0) == mvp.MVP_ERR_ARG
+    assert _attn(lib, scale=float("nan")) == mvp.MVP_ERR_ARG
+    assert _attn(lib, ndec=2) == mvp.MVP_ERR_ARG  # more decode requests than requests
+    assert _attn(lib, ndec=-2) == mvp.MVP_ERR_ARG
+    assert _attn(lib, total_q=0) == mvp.MVP_OK  # nothing to do
+
+
+def test_fill_argument_errors(lib):
+    f = lib.mvp_fill_query_ranges
+    assert f(None, 1, 1, 1 << 20, 1 << 20, 10, 1 << 20, 4, None, None) == mvp.MVP_ERR_ARG  # ranges null
+    assert f(1 << 20, 1, 1, 1 << 20, 1 << 20, 10, 1 << 20, 4, None, None) == mvp.MVP_ERR_CAPACITY
+    assert f(1 << 20, 1, 1, None, 1 << 20, 10, 1 << 20, 40, None, None) == mvp.MVP_ERR_ARG
+    assert f(1 << 20, -1, 1, 1 << 20, 1 << 20, 10, 1 << 20, 40, None, None) == mvp.MVP_ERR_ARG
+
+
+def test_workspace_size(lib):
+    assert mvp.attn_workspace_size(4, 16, 256, 1000) == 0  # one split: no workspace needed
+    n = mvp.attn_workspace_size(260, 32, 128, 32769)
+    assert n == 260 * 32 * 17 * 130 * 4
+
+
+def test_binding_has_no_cpu_path():
+    """The product modules never import the oracle."""
+    pkg = os.path.join(ROOT, "masked_varlen_prefill_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                src = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in src and "from oracle" not in src, f
