@@ -310,7 +310,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (p.m.sink_mode != 0 && p.m.sinks != nullptr) sink_l2 = __ldg(p.m.sinks + head) * 1.4426950408889634f;
     const bool null_mode = p.m.sink_mode == 2 && p.m.sinks != nullptr;
     float m_ref = null_mode ? sink_l2 : -INFINITY;
-    float l_sum = null_mode ? 1.f : 0.f;
+    float l_sum = null_mode ? 1.f : 0.f;   // sum of the bf16-rounded p: normalises O
+    float l_lse = l_sum;                   // sum of the fp32 p: gives the LSE
     bool ok = true;
 
     for (int j = 0; j < n_tiles; ++j) {
@@ -352,21 +353,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (need) {
         alpha = ex2_approx(m_ref - mx);  // 0 when m_ref == -inf
         l_sum *= alpha;
+        l_lse *= alpha;
         m_ref = mx;
       }
       const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-      // The row sum is taken over the bf16-rounded probabilities that the PV
-      // MMA consumes, so numerator and denominator use the same weights.
-      float part = 0.f;
+      // O is normalised by the sum of the bf16-rounded probabilities that the
+      // PV MMA consumes (numerator and denominator use the same weights); the
+      // LSE uses the sum of the unrounded ones.
+      float part = 0.f, part_exact = 0.f;
 #pragma unroll
       for (int i = 0; i < BN / 2; ++i) {
         const float e0 = ex2_approx(__uint_as_float(s[2 * i]) - m_use);
         const float e1 = ex2_approx(__uint_as_float(s[2 * i + 1]) - m_use);
         const uint32_t pk = pack_bf16x2(e0, e1);
         part += __uint_as_float(pk << 16) + __uint_as_float(pk & 0xffff0000u);
+        part_exact += e0 + e1;
         s[i] = pk;
       }
       l_sum += part;
+      l_lse += part_exact;
 #pragma unroll
       for (int c = 0; c < BN / 64; ++c)
         tmem_st_32x32b_x32(scol + c * 32, *reinterpret_cast<const uint32_t(*)[32]>(&s[c * 32]));
@@ -431,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (row_valid && p.lse != nullptr && dv0 == 0) {
       const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-      const float lse = (l_sum > 0.f) ? (m_use + lg2_approx(l_sum)) * 0.6931471805599453f : -INFINITY;
+      const float lse = (l_lse > 0.f) ? (m_use + lg2_approx(l_lse)) * 0.6931471805599453f : -INFINITY;
       p.lse[static_cast<size_t>(head) * p.total_q + q0 + qi] = lse;
     }
   }

@@ -17,6 +17,12 @@ from oracle import range_table as ort
 
 OUT_ATOL = 1e-2
 LSE_RTOL = 1e-3
+# bf16 keeps 8 significant bits: a correctly rounded bf16 output can differ
+# from the exact value by half an ulp, i.e. up to 2^-9 |x|, and the bf16
+# probabilities of the P.V product add about as much again.  For |out| above
+# 2.56 that exceeds 1e-2 no matter how the kernel computes, so shapes that
+# produce such outputs (a few visible keys per row) use max(1e-2, 2^-8 |ref|).
+BF16_REL = 2.0 ** -8
 
 
 def device_meta(w, dev):
@@ -107,15 +113,23 @@ def _attend_selected(local, qb, kb, vb, ctx, w, rr, sk):
                             w.sink_mode, w.scale)
 
 
-def compare(out_gpu, lse_gpu, out_ref, lse_ref, rows=None, what=""):
-    """Assert the tolerances; returns (max_abs_out, max_rel_lse)."""
+def compare(out_gpu, lse_gpu, out_ref, lse_ref, rows=None, what="", strict=True):
+    """Assert the tolerances; returns (max_abs_out, max_rel_lse).
+
+    strict: out max-abs <= 1e-2 everywhere (the workload shapes).  Otherwise
+    each element may also use the bf16 bound 2^-8 |ref| when that is larger."""
     og = out_gpu.float().cpu().numpy()
     lg = None if lse_gpu is None else lse_gpu.cpu().numpy()
     where = ""
+
+    def excess(got, ref):
+        tol = OUT_ATOL if strict else np.maximum(OUT_ATOL, BF16_REL * np.abs(ref))
+        return np.abs(got - ref) / tol * OUT_ATOL  # error rescaled to the 1e-2 scale
+
     if rows is None:
-        err_o = np.abs(og - out_ref).max() if og.size else 0.0
+        err_o = excess(og, out_ref).max() if og.size else 0.0
         if og.size:
-            idx = np.unravel_index(int(np.argmax(np.abs(og - out_ref))), og.shape)
+            idx = np.unravel_index(int(np.argmax(excess(og, out_ref))), og.shape)
             where = f" at (row, head, dim)={tuple(int(i) for i in idx)} gpu={og[idx]:.5f} ref={out_ref[idx]:.5f}"
         assert np.isfinite(og).all(), f"{what}: non-finite output"
         if lg is not None:
@@ -129,9 +143,9 @@ def compare(out_gpu, lse_gpu, out_ref, lse_ref, rows=None, what=""):
         err_o, err_l = 0.0, 0.0
         for r in out_ref:
             assert np.isfinite(og[r]).all(), f"{what}: non-finite output row {r}"
-            e = float(np.abs(og[r] - out_ref[r]).max())
+            e = float(excess(og[r], out_ref[r]).max())
             if e > err_o:
-                idx = np.unravel_index(int(np.argmax(np.abs(og[r] - out_ref[r]))), og[r].shape)
+                idx = np.unravel_index(int(np.argmax(excess(og[r], out_ref[r]))), og[r].shape)
                 where = f" at row {r} (head, dim)={tuple(int(i) for i in idx)} gpu={og[r][idx]:.5f} ref={out_ref[r][idx]:.5f}"
             err_o = max(err_o, e)
             if lg is not None:
@@ -141,7 +155,8 @@ def compare(out_gpu, lse_gpu, out_ref, lse_ref, rows=None, what=""):
                 f = np.isfinite(ref)
                 if f.any():
                     err_l = max(err_l, float((np.abs(got[f] - ref[f]) / np.maximum(np.abs(ref[f]), 1.0)).max()))
-    assert err_o <= OUT_ATOL, f"{what}: out max-abs {err_o:.3e} > {OUT_ATOL}{where}"
+    kind = "max-abs" if strict else "scaled error (1e-2 or 2^-8|ref|)"
+    assert err_o <= OUT_ATOL, f"{what}: out {kind} {err_o:.3e} > {OUT_ATOL}{where}"
     assert err_l <= LSE_RTOL, f"{what}: lse rel {err_l:.3e} > {LSE_RTOL}"
     return err_o, err_l
 
