@@ -150,6 +150,38 @@ int mvp_attn_fwd_varlen(const void* q, const void* k, const void* v, void* out, 
                         int sink_mode, float scale, void* workspace, size_t workspace_bytes,
                         void* stream);
 
+/*
+ * Allocation-free variant of mvp_attn_fwd_varlen.  The pages have no
+ * counterpart of this call; it exists for callers that cannot allocate device
+ * memory where they run attention (an engine whose free memory is already
+ * committed to its KV-cache pool, a plugin inside a framework that owns the
+ * allocator, a path that must not synchronise on an allocation) and so cannot
+ * pass the split-KV workspace.  Arguments and results are exactly those of
+ * mvp_attn_fwd_varlen without workspace/workspace_bytes: the split-KV partials
+ * go to a fixed 16 MiB array in the library's own device memory
+ * (mvp_static_scratch_bytes()), which every GPU that loads the library holds
+ * until the process exits.  The call allocates nothing.
+ *   - A batch whose partials would not fit (mvp_attn_workspace_size(decode
+ *     requests, ...) > mvp_static_scratch_bytes()) is rejected with
+ *     MVP_ERR_CAPACITY before anything is launched.
+ *   - The first call on a device looks up the array's device address (and the
+ *     library's other per-device state); make that first call before any
+ *     stream capture.
+ *   - All calls share the array and it keeps the last call's contents; nothing
+ *     in it needs to start at zero.  Calls whose kernels overlap on the GPU
+ *     (unordered streams) race on it.
+ */
+int mvp_attn_fwd_varlen_static_ws(const void* q, const void* k, const void* v, void* out, float* lse,
+                                  const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                  const int32_t* context_lens, int num_reqs, int total_q, int total_k,
+                                  int max_q_len, int max_k_len, int num_decode_reqs, int num_heads_q,
+                                  int num_heads_kv, int head_dim, const int32_t* range_table,
+                                  const int32_t* range_covered, int causal, int window_left, int window_right,
+                                  const float* sinks, int sink_mode, float scale, void* stream);
+
+/* Size in bytes of the fixed scratch array used by mvp_attn_fwd_varlen_static_ws. */
+size_t mvp_static_scratch_bytes(void);
+
 /* Synchronises `stream`, returns MVP_ERR_DEVICE_TIMEOUT if a kernel recorded a
  * timeout since the last call (and clears it), MVP_ERR_CUDA on a CUDA error,
  * else MVP_OK. */

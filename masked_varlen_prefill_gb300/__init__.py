@@ -21,6 +21,7 @@ from ._lib import (  # noqa: F401
     MvpError,
     attn_fwd_varlen,
     attn_fwd_varlen_host,
+    attn_fwd_varlen_static_ws,
     attn_workspace_size,
     fill_query_ranges,
     get_last_device_error,

@@ -34,6 +34,9 @@ _SIGNATURES = {
     "mvp_attn_workspace_size": (_sz, [_i, _i, _i, _i]),
     "mvp_attn_fwd_varlen": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i,
                                  _vp, _vp, _i, _i, _i, _vp, _i, _f, _vp, _sz, _vp]),
+    "mvp_attn_fwd_varlen_static_ws": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
+                                           _i, _i, _vp, _vp, _i, _i, _i, _vp, _i, _f, _vp]),
+    "mvp_static_scratch_bytes": (_sz, []),
     "mvp_get_last_device_error": (_i, [_vp]),
     "mvp_status_str": (ctypes.c_char_p, [_i]),
     "mvp_last_launch_count": (_i, []),
@@ -157,6 +160,36 @@ def attn_fwd_varlen(q, k, v, out, cu_seqlens_q, cu_seqlens_k, max_q_len, max_k_l
         _ptr(sinks), int(sink_mode), float(scale), _ptr(workspace), ws_bytes, _stream(stream, dev))
     if st != MVP_OK:
         raise MvpError("mvp_attn_fwd_varlen", st)
+
+
+def attn_fwd_varlen_static_ws(q, k, v, out, cu_seqlens_q, cu_seqlens_k, max_q_len, max_k_len, *, lse=None,
+                              context_lens=None, range_table=None, range_covered=None, causal=True,
+                              window_left=-1, window_right=-1, sinks=None, sink_mode=SINK_NONE, scale=None,
+                              num_decode_reqs=-1, stream=None):
+    """Like ``attn_fwd_varlen`` but without a workspace argument, for callers
+    that cannot allocate device memory at the call site: the split-KV partials
+    use the library's fixed scratch array (``mvp_attn_fwd_varlen_static_ws``
+    in include/mvp.h; calls that overlap on the GPU race on it)."""
+    lib = load_library()
+    dev = q.device
+    for n, t in (("q", q), ("k", k), ("v", v), ("out", out)):
+        _check_cuda(n, t, torch.bfloat16, dev)
+    for n, t in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k), ("context_lens", context_lens),
+                 ("range_table", range_table), ("range_covered", range_covered)):
+        _check_cuda(n, t, torch.int32, dev)
+    _check_cuda("lse", lse, torch.float32, dev)
+    _check_cuda("sinks", sinks, torch.float32, dev)
+    total_q, hq, d = q.shape
+    total_k, hkv, _ = k.shape
+    if scale is None:
+        scale = d ** -0.5
+    st = lib.mvp_attn_fwd_varlen_static_ws(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+        _ptr(context_lens), cu_seqlens_q.shape[0] - 1, total_q, total_k, int(max_q_len), int(max_k_len),
+        int(num_decode_reqs), hq, hkv, d, _ptr(range_table), _ptr(range_covered), int(bool(causal)),
+        int(window_left), int(window_right), _ptr(sinks), int(sink_mode), float(scale), _stream(stream, dev))
+    if st != MVP_OK:
+        raise MvpError("mvp_attn_fwd_varlen_static_ws", st)
 
 
 def attn_fwd_varlen_host(q, k, v, cu_seqlens_q, cu_seqlens_k, max_q_len, max_k_len, *, device_buffers,
