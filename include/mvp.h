@@ -137,6 +137,7 @@ size_t mvp_attn_workspace_size(int num_reqs, int num_heads_q, int head_dim, int 
  *                it reads 0 the table is ignored.
  * workspace      device scratch of workspace_bytes (may be NULL / 0); see
  *                mvp_attn_workspace_size.
+ * scale          softmax scale, finite and > 0 (MVP_ERR_ARG otherwise).
  * Errors: MVP_ERR_ARG, MVP_ERR_UNSUPPORTED (head_dim, alignment, head ratio),
  *         MVP_ERR_CUDA.  Requests with q_len == 0 produce no rows.
  */

@@ -148,7 +148,7 @@ int mvp_attn_fwd_varlen(const void* q, const void* k, const void* v, void* out, 
   if (window_left < -1 || window_right < -1) return MVP_ERR_ARG;
   if (causal != 0 && causal != 1) return MVP_ERR_ARG;
   if (num_decode_reqs < -1 || num_decode_reqs > num_reqs) return MVP_ERR_ARG;
-  if (!(scale == scale)) return MVP_ERR_ARG;  // NaN
+  if (!(scale > 0.f) || scale > 3.0e38f) return MVP_ERR_ARG;  // NaN, <= 0, inf
   if (total_q == 0) return MVP_OK;
   if (total_k < 1 || max_q_len < 1 || max_k_len < 1) return MVP_ERR_ARG;
   if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || cu_seqlens_q == nullptr ||
@@ -174,6 +174,7 @@ int mvp_attn_fwd_varlen(const void* q, const void* k, const void* v, void* out, 
   m.window_right = causal ? 0 : window_right;
   m.sink_mode = sink_mode;
   m.scale_log2 = scale * 1.4426950408889634f;
+  m.scale = scale;
 
   const int group = num_heads_q / num_heads_kv;
   int launches = 0;
@@ -204,7 +205,7 @@ int mvp_attn_fwd_varlen(const void* q, const void* k, const void* v, void* out, 
     CUtensorMap mq, mk, mv;
     if (!encode_3d(&mq, q, head_dim, num_heads_q, total_q, 64, gpack, bmp, true) ||
         !encode_3d(&mk, k, head_dim, num_heads_kv, total_k, 64, 1, shape.bn, true) ||
-        !encode_3d(&mv, v, head_dim, num_heads_kv, total_k, 64, 1, shape.bn, true))
+        !encode_3d(&mv, v, head_dim, num_heads_kv, total_k, 64, 1, shape.v_box_keys, true))
       return MVP_ERR_UNSUPPORTED;
     if (launch_prefill(head_dim, pp, mq, mk, mv, st) != cudaSuccess) return MVP_ERR_CUDA;
     ++launches;

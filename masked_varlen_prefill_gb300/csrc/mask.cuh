@@ -49,6 +49,15 @@ struct RowVis {
   }
 };
 
+// Bit i set iff key c0 + i (i < 32) lies in the closed interval [lo, hi].
+__device__ __forceinline__ uint32_t interval_bits(int lo, int hi, int c0) {
+  const int a = max(lo, c0), b = min(hi, c0 + 31);
+  if (a > b) return 0u;
+  const uint32_t width = static_cast<uint32_t>(b - a + 1);  // 1..32
+  const uint32_t ones = (width >= 32u) ? 0xffffffffu : ((1u << width) - 1u);
+  return ones << (a - c0);
+}
+
 __device__ __forceinline__ RowVis empty_row() {
   RowVis v;
   v.b_lo = 1; v.b_hi = 0; v.r_lo = 1; v.r_hi = 0;

@@ -36,6 +36,7 @@ struct MaskParams {
   int window_right;          // -1 = unbounded (non-causal only)
   int sink_mode;
   float scale_log2;          // scale * log2(e)
+  float scale;               // > 0
 };
 
 // ----------------------------------------------------------------- prefill
@@ -61,6 +62,7 @@ struct PrefillShape {
   int bn;        // keys per tile
   int dv_cta;    // value columns per CTA
   int dv_split;  // CTAs per (q tile, head group) along the value dimension
+  int v_box_keys;  // keys per V TMA box
 };
 PrefillShape prefill_tile_shape(int head_dim);
 

@@ -68,6 +68,8 @@ def test_argument_errors_return_before_any_launch(lib):
     assert _attn(lib, q=(1 << 20) + 8) == mvp.MVP_ERR_UNSUPPORTED  # not 16-byte aligned
     assert _attn(lib, total_k=0) == mvp.MVP_ERR_ARG
     assert _attn(lib, scale=float("nan")) == mvp.MVP_ERR_ARG
+    assert _attn(lib, scale=0.0) == mvp.MVP_ERR_ARG
+    assert _attn(lib, scale=-0.5) == mvp.MVP_ERR_ARG
     assert _attn(lib, ndec=2) == mvp.MVP_ERR_ARG  # more decode requests than requests
     assert _attn(lib, ndec=-2) == mvp.MVP_ERR_ARG
     assert _attn(lib, total_q=0) == mvp.MVP_OK  # nothing to do
