@@ -22,10 +22,11 @@ __device__ int g_device_error_word;
 constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
 int* g_err_ptr[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 thread_local int g_last_launches = 0;
 
-cudaError_t device_state(int** err_ptr) {
+cudaError_t device_state(int** err_ptr, int* num_sms = nullptr) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -45,7 +46,14 @@ cudaError_t device_state(int** err_ptr) {
     if (e != cudaSuccess) return e;
     g_err_ptr[dev] = static_cast<int*>(ptr);
   }
+  if (g_num_sms[dev] == 0) {
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    g_num_sms[dev] = n > 0 ? n : 1;
+  }
   *err_ptr = g_err_ptr[dev];
+  if (num_sms) *num_sms = g_num_sms[dev];
   return cudaSuccess;
 }
 
@@ -159,7 +167,8 @@ int mvp_attn_fwd_varlen(const void* q, const void* k, const void* v, void* out, 
   if (static_cast<long long>(total_q) * num_heads_q * head_dim >= (1LL << 40)) return MVP_ERR_UNSUPPORTED;
 
   int* err = nullptr;
-  if (device_state(&err) != cudaSuccess) return MVP_ERR_CUDA;
+  int num_sms = 1;
+  if (device_state(&err, &num_sms) != cudaSuccess) return MVP_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   MaskParams m;
@@ -201,7 +210,8 @@ int mvp_attn_fwd_varlen(const void* q, const void* k, const void* v, void* out, 
     pp.n_qtiles = (max_q_len + bmp - 1) / bmp;
     pp.skip_decode = 1;
     pp.req_offset = prefill_first;
-    if (static_cast<long long>(num_heads_kv) * pp.n_hgroups * shape.dv_split > 65535) return MVP_ERR_UNSUPPORTED;
+    pp.n_ctas = num_sms;
+
     CUtensorMap mq, mk, mv;
     if (!encode_3d(&mq, q, head_dim, num_heads_q, total_q, 64, gpack, bmp, true) ||
         !encode_3d(&mk, k, head_dim, num_heads_kv, total_k, 64, 1, shape.bn, true) ||

@@ -1,6 +1,6 @@
 // Masked varlen attention forward, prefill rows: tcgen05 + TMA, sm_103a.
 //
-// Computes, for a 128-row query tile, softmax(scale * Q K^T + mask) V with the
+// Computes, for 128-row query tiles, softmax(scale * Q K^T + mask) V with the
 // online (running max / running sum) formulation in base 2, as the Triton
 // kernel of vLLM PR #49815 does ("Key source snippets", the sinks branch of
 // _fwd_kernel: exp2 domain, sink * log2(e), null-logit init m = sink, l = 1, or
@@ -9,29 +9,34 @@
 // two closed key intervals per row (mask.cuh).
 //
 // GB300 design (not the pages' kernels):
-// * One CTA = one 128-row tile.  With GQA, G_pack query heads of one KV head
+// * Work item = one 128-row tile.  With GQA, G_pack query heads of one KV head
 //   share the tile: row r is (position r / G_pack, head h0 + r % G_pack), so a
 //   K/V tile read from L2 serves G_pack heads.  The Q tile is a single 3-D TMA
 //   box (64 dims, G_pack heads, 128 / G_pack positions), 128-byte swizzled.
+// * Persistent CTAs (one per SM) walk the items with a static stride, q tile
+//   fastest so that concurrent CTAs share K/V windows in L2.  Every role computes each item's geometry
+//   and key-tile plan itself (a warp reduction over the tile's 128 rows), and
+//   all barrier phases run on CTA-wide counters, so the producer and the MMA
+//   issuer move on to the next item's Q, K and QK while the softmax warps
+//   still finish the current item.
 // * Warp roles: warp 0 issues TMA loads, warp 1 allocates TMEM and issues
 //   tcgen05.mma from one thread, and SPLIT softmax warpgroups (warps 2..)
 //   own the rows: with BN = 128 two warpgroups split every row's 128 scores
-//   into halves of 64 (warps w and w+4 read the same TMEM lanes), exchange
-//   the row max through shared memory once per tile, and split the O
-//   correction and epilogue by columns.  One thread handles 64 scores, so
-//   the exp/sum work of a tile is spread over twice as many warps.
+//   into halves of 64 (warps w and w+4 read the same TMEM lanes), exchange the
+//   row max through shared memory once per tile, and split the O correction
+//   and epilogue by columns.
 // * TMEM (512 columns): S double buffer [0, BN) and [BN, 2 BN) in fp32; the
 //   bf16 probabilities P overwrite the first BN/2 columns of their S buffer and
 //   feed O += P V as the TMEM operand of tcgen05.mma; O at [2 BN, 2 BN + DV).
 // * MMA order per step j: S_j = Q K_j^T, then O += P_{j-1} V_{j-1}, so the
 //   tensor core computes the next scores while the softmax warps work on the
-//   current ones.
+//   current ones.  MMA descriptors are computed once; loads are released per
+//   tile (each extra tcgen05.commit or wait costs the single issuing thread).
 // * Key tiles are visited only inside [min hull, max hull] of the tile's rows;
 //   tiles fully inside every row's all-visible interval skip the mask.
 // * O is rescaled lazily: a row's reference max only moves when the new max
-//   exceeds it by more than 2^8 (probabilities then stay <= 256), so O is read
-//   and written back rarely.
-// * Every barrier wait is bounded (ptx.cuh).
+//   exceeds it by more than 2^8 (probabilities then stay <= 256).
+// * Every mbarrier wait is bounded (ptx.cuh).
 #include <cuda_bf16.h>
 
 #include "mask.cuh"
@@ -44,27 +49,24 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr unsigned kFullMask = 0xffffffffu;
 
-// KB: 64-dim K chunks released per barrier; VK: keys per V barrier chunk.
-template <int D_, int DV_, int BN_, int KST_, int VST_, int KB_ = 1, int VK_ = 32>
+template <int D_, int DV_, int BN_, int KST_, int VST_>
 struct Cfg {
   static constexpr int D = D_;
-  static constexpr int DV = DV_;        // value columns handled by one CTA
-  static constexpr int BN = BN_;
-  static constexpr int KST = KST_;
-  static constexpr int VST = VST_;
-  static constexpr int QCH = D / 64;            // 64-dim chunks of Q and K (one TMA box each)
-  static constexpr int KB = KB_;
-  static constexpr int KBC = QCH / KB;          // K barrier chunks per tile
-  static constexpr int VCH = DV / 64;           // 64-dim chunks of a V tile
-  static constexpr int VK = VK_;
-  static constexpr int VKC = BN / VK;           // V barrier chunks per tile
-  static constexpr int K_CHUNK_BYTES = BN * 128;
-  static constexpr int V_KEYCHUNK_BYTES = VK * DV * 2;
+  static constexpr int DV = DV_;        // value columns handled by one item
+  static constexpr int BN = BN_;        // keys per tile
+  static constexpr int KST = KST_;      // K tile stages
+  static constexpr int VST = VST_;      // V tile stages
+  static constexpr int QCH = D / 64;    // 64-dim chunks of Q and K (one TMA box each)
+  static constexpr int VCH = DV / 64;   // 64-dim chunks of a V tile
+  static constexpr int DV_SPLIT = D / DV;
   static constexpr int SPLIT = BN / 64;         // softmax warpgroups (column halves of a row)
   static constexpr int HC = BN / SPLIT;         // score columns per softmax thread (64)
   static constexpr int HDV = DV / SPLIT;        // O columns per softmax thread
-  static constexpr int THREADS = 64 + 128 * SPLIT;
+  static constexpr int CONSUMER_WARPS = 2 + 4 * SPLIT;  // producer, MMA, softmax warps
+  static constexpr int SCHED_WARP = CONSUMER_WARPS;      // computes item plans ahead
+  static constexpr int THREADS = 32 * (CONSUMER_WARPS + 1);
   static constexpr int Q_BYTES = kBM * D * 2;
   static constexpr int K_BYTES = BN * D * 2;
   static constexpr int V_BYTES = BN * DV * 2;
@@ -72,8 +74,8 @@ struct Cfg {
   static constexpr int K_OFF = Q_BYTES;
   static constexpr int V_OFF = K_OFF + KST * K_BYTES;
   static constexpr int TILE_BYTES = V_OFF + VST * V_BYTES;
-  static constexpr int RED_OFF = TILE_BYTES;                       // row-max / row-sum exchange
-  static constexpr int RED_BYTES = SPLIT > 1 ? 2 * SPLIT * kBM * 4 : 0;
+  static constexpr int RED_OFF = TILE_BYTES;  // pair exchange slots: [2 parity][SPLIT][128] float2
+  static constexpr int RED_BYTES = SPLIT > 1 ? 2 * SPLIT * kBM * 8 : 0;
   static constexpr int SMEM_BYTES = RED_OFF + RED_BYTES + 1024;  // + alignment slack
   static constexpr int S_COL = 0;
   static constexpr int O_COL = 2 * BN;
@@ -81,27 +83,145 @@ struct Cfg {
   static_assert(O_COL + DV <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM_BYTES <= 227 * 1024, "smem budget");
   static_assert(BN == 64 || BN == 128, "BN");
-  static_assert(HDV % 32 == 0, "O columns per thread");
   static_assert(DV % 64 == 0 && DV <= 256, "DV");
+  static_assert(HDV % 32 == 0, "O columns per thread");
   static_assert(KST >= 1 && KST <= 4 && VST >= 1 && VST <= 4, "stages");
-  static_assert(KST * KBC <= 16 && VST * VKC <= 16, "barrier arrays");
-  static_assert(QCH % KB == 0 && BN % VK == 0 && VK % 16 == 0, "chunking");
 };
 
+// One work item: a 128-row query tile of one request, one KV head group and
+// (for D = 512) one half of the value dimension, with its key-tile plan.
+struct Item {
+  int b, pos0, q0, q_len, k0, k_len, ctx, h0, hkv, dv0;
+  bool valid;
+};
+
+struct Plan {
+  int kb_lo, n_tiles, int_lo, int_hi;
+};
+
+struct PlanEntry {
+  Item it;
+  Plan pl;
+  int last;  // 1: no more items for this CTA
+};
+
+constexpr int kPlanRing = 4;
+
 struct __align__(8) Barriers {
+  uint64_t plan_full[kPlanRing];
+  uint64_t plan_empty[kPlanRing];
+  PlanEntry plans[kPlanRing];
   uint64_t q_full;
-  uint64_t k_full[16];   // [stage][64-dim chunk]
-  uint64_t k_empty[16];
-  uint64_t v_full[16];   // [stage][32-key chunk]
-  uint64_t v_empty[16];
+  uint64_t q_empty;
+  uint64_t k_full[4];
+  uint64_t k_empty[4];
+  uint64_t v_full[4];
+  uint64_t v_empty[4];
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t o_done[2];
   uint64_t final_mma;
+  uint64_t xchg[4][2];  // softmax column-half pairs (per TMEM lane quarter), by parity
   uint32_t tmem_base;
   int abort_flag;
-  int red[4];  // min hull lo, max hull hi, max core lo, min core hi
 };
+
+// Items are numbered q tile fastest (latest tile first), then head group,
+// then request: the CTAs running at the same time then work on neighbouring
+// tiles of a few (request, KV head) pairs, whose K/V windows overlap and stay
+// in L2, and every CTA's strided sequence mixes heavy and light tiles.
+template <class C>
+__device__ __forceinline__ Item item_geometry(int item, const PrefillParams& p) {
+  const int nz = p.hkv * p.n_hgroups * C::DV_SPLIT;
+  const int x = item % p.n_qtiles;  // 0 = latest q tile (heaviest under causal masks)
+  const int rest = item / p.n_qtiles;
+  const int z = rest % nz;
+  Item it;
+  it.b = rest / nz + p.req_offset;
+  it.dv0 = (z % C::DV_SPLIT) * C::DV;
+  const int hz = z / C::DV_SPLIT;
+  it.hkv = hz / p.n_hgroups;
+  it.h0 = it.hkv * (p.hq / p.hkv) + (hz % p.n_hgroups) * p.gpack;
+  it.q0 = __ldg(p.m.cu_q + it.b);
+  it.q_len = __ldg(p.m.cu_q + it.b + 1) - it.q0;
+  it.k0 = __ldg(p.m.cu_k + it.b);
+  it.k_len = __ldg(p.m.cu_k + it.b + 1) - it.k0;
+  it.ctx = p.m.ctx_lens ? __ldg(p.m.ctx_lens + it.b) : (it.k_len - it.q_len);
+  it.pos0 = (p.n_qtiles - 1 - x) * (kBM / p.gpack);
+  it.valid = it.pos0 < it.q_len && !(p.skip_decode && it.q_len == 1);
+  return it;
+}
+
+// Key-tile plan of an item (warp-collective): the tiles between the smallest
+// and largest visible key of any row, and the tiles inside every row's
+// all-visible interval (no mask needed there).
+template <class C>
+__device__ __forceinline__ Plan plan_tiles(const Item& it, const PrefillParams& p, bool use_table, int lane) {
+  int hl_min = INT_MAX, hh_max = INT_MIN, cl_max = INT_MIN, ch_min = INT_MAX;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int row = lane + 32 * k;
+    const int qi = it.pos0 + row / p.gpack;
+    if (qi < it.q_len) {
+      const RowVis v = row_visibility(p.m, it.ctx + qi, it.k_len, use_table ? (it.q0 + qi) : -1);
+      int hl, hh, cl, ch;
+      v.hull(hl, hh);
+      v.core(cl, ch);
+      if (hl <= hh) {
+        hl_min = min(hl_min, hl);
+        hh_max = max(hh_max, hh);
+      }
+      cl_max = max(cl_max, cl);  // an empty core (INT_MAX, INT_MIN) removes the interior
+      ch_min = min(ch_min, ch);
+    }
+  }
+  hl_min = __reduce_min_sync(kFullMask, hl_min);
+  hh_max = __reduce_max_sync(kFullMask, hh_max);
+  cl_max = __reduce_max_sync(kFullMask, cl_max);
+  ch_min = __reduce_min_sync(kFullMask, ch_min);
+  Plan pl{0, 0, 1, 0};
+  if (hl_min <= hh_max) {
+    pl.kb_lo = hl_min / C::BN;
+    pl.n_tiles = hh_max / C::BN - pl.kb_lo + 1;
+    if (cl_max <= ch_min) {
+      pl.int_lo = (cl_max + C::BN - 1) / C::BN;
+      pl.int_hi = (ch_min + 1) / C::BN - 1;
+    }
+  }
+  return pl;
+}
+
+// Warp-collective: take plan entry n from the ring (written by the scheduler
+// warp) and release its slot.
+__device__ __forceinline__ bool consume_plan(Barriers& sb, int n, int lane, PlanEntry& e, int* err) {
+  const int slot = n % kPlanRing;
+  const bool ok = mbar_wait(&sb.plan_full[slot], (n / kPlanRing) & 1, &sb.abort_flag, err, kDevTimeoutOther);
+  e = sb.plans[slot];
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&sb.plan_empty[slot]);
+  return ok;
+}
+
+// The two column halves of a row (warps w and w+4) swap one float2 through
+// shared memory.  Exchange k uses slot and barrier k & 1 (the partner cannot
+// overwrite slot k & 1 before this thread has passed exchange k + 1).  The
+// wait is bounded, so a failed partner cannot hang the pair.
+__device__ __forceinline__ bool pair_exchange(float2* slots, uint64_t* xb, int& k, int half, int row, float2 mine,
+                                              float2& theirs, volatile int* abort_flag, int* err) {
+  float2* slot = slots + (k & 1) * (2 * kBM);
+  slot[half * kBM + row] = mine;
+  mbar_arrive(&xb[k & 1]);
+  const bool ok = mbar_wait(&xb[k & 1], (k >> 1) & 1, abort_flag, err, kDevTimeoutSoftmax);
+  theirs = slot[(1 - half) * kBM + row];
+  ++k;
+  return ok;
+}
+
+__device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t* r) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(r[0]), "r"(r[1]),
+               "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
 
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1)
@@ -113,32 +233,19 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-
-  // ---------------------------------------------------------------- tile
-  const int qt = p.n_qtiles - 1 - static_cast<int>(blockIdx.x);  // heavy (late) tiles first
-  const int b = blockIdx.y + p.req_offset;
-  const int dv_split = (C::DV < C::D) ? (C::D / C::DV) : 1;
-  const int zz = blockIdx.z;
-  const int dv0 = (zz % dv_split) * C::DV;
-  const int hz = zz / dv_split;
-  const int hkv = hz / p.n_hgroups;
-  const int h0 = hkv * (p.hq / p.hkv) + (hz % p.n_hgroups) * p.gpack;
-
-  const int q0 = __ldg(p.m.cu_q + b);
-  const int q_len = __ldg(p.m.cu_q + b + 1) - q0;
-  const int k0 = __ldg(p.m.cu_k + b);
-  const int k_len = __ldg(p.m.cu_k + b + 1) - k0;
-  const int bmp = kBM / p.gpack;  // positions per tile
-  const int pos0 = qt * bmp;
-  if (pos0 >= q_len) return;                  // uniform over the CTA
-  if (p.skip_decode && q_len == 1) return;    // handled by the decode kernel
-  const int ctx = p.m.ctx_lens ? __ldg(p.m.ctx_lens + b) : (k_len - q_len);
   const bool use_table = table_active(p.m);
+  const int n_items = p.n_qtiles * (p.num_reqs - p.req_offset) * p.hkv * p.n_hgroups * C::DV_SPLIT;
+  constexpr int BN = C::BN;
 
   // ---------------------------------------------------------------- setup
   if (threadIdx.x == 0) {
+    for (int i = 0; i < kPlanRing; ++i) {
+      mbar_init(&sb.plan_full[i], 1);
+      mbar_init(&sb.plan_empty[i], C::CONSUMER_WARPS);
+    }
     mbar_init(&sb.q_full, 1);
-    for (int i = 0; i < 16; ++i) {
+    mbar_init(&sb.q_empty, 1);
+    for (int i = 0; i < 4; ++i) {
       mbar_init(&sb.k_full[i], 1);
       mbar_init(&sb.k_empty[i], 1);
       mbar_init(&sb.v_full[i], 1);
@@ -150,11 +257,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       mbar_init(&sb.o_done[i], 1);
     }
     mbar_init(&sb.final_mma, 1);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&sb.xchg[i][0], 64);
+      mbar_init(&sb.xchg[i][1], 64);
+    }
     sb.abort_flag = 0;
-    sb.red[0] = INT_MAX;
-    sb.red[1] = INT_MIN;
-    sb.red[2] = INT_MIN;
-    sb.red[3] = INT_MAX;
     mbar_fence_init();
   }
   if (warp == 1) {
@@ -170,380 +277,441 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   uint8_t* sK = smem + C::K_OFF;
   uint8_t* sV = smem + C::V_OFF;
 
-  // Q load does not depend on the key range: start it right away.
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&map_q);
-    tma_prefetch_desc(&map_k);
-    tma_prefetch_desc(&map_v);
-    mbar_arrive_expect_tx(&sb.q_full, C::Q_BYTES);
-    for (int c = 0; c < C::QCH; ++c)
-      tma_load_3d(sQ + c * (kBM * 128), &map_q, &sb.q_full, c * 64, h0, q0 + pos0);
-  }
-
-  // Row geometry (softmax warps): interval reduction over the tile's rows.
-  const bool is_softmax = warp >= 2;
-  const int quarter = warp & 3;
-  const int half = is_softmax ? (warp - 2) / 4 : 0;  // which column half of the row
-  const int row = quarter * 32 + lane;
-  const int rpos = row / p.gpack;
-  const int head = h0 + (row % p.gpack);
-  const int qi = pos0 + rpos;
-  const bool row_valid = is_softmax && qi < q_len;
-  const int qpos = ctx + qi;
-  RowVis vis = empty_row();
-  if (row_valid) {
-    vis = row_visibility(p.m, qpos, k_len, use_table ? (q0 + qi) : -1);
-  }
-  if (row_valid && half == 0) {
-    int hl, hh, cl, ch;
-    vis.hull(hl, hh);
-    vis.core(cl, ch);
-    if (hl <= hh) {
-      atomicMin(&sb.red[0], hl);
-      atomicMax(&sb.red[1], hh);
-    }
-    atomicMax(&sb.red[2], cl);   // empty core (INT_MAX, INT_MIN) kills the interior
-    atomicMin(&sb.red[3], ch);
-  }
-  __syncthreads();
-
-  const int BN = C::BN;
-  int kb_lo = 0, n_tiles = 0, int_lo = 1, int_hi = 0;
-  if (sb.red[0] <= sb.red[1]) {
-    kb_lo = sb.red[0] / BN;
-    const int kb_hi = sb.red[1] / BN;
-    n_tiles = kb_hi - kb_lo + 1;
-    if (sb.red[2] <= sb.red[3]) {
-      int_lo = (sb.red[2] + BN - 1) / BN;
-      int_hi = (sb.red[3] + 1) / BN - 1;
-    }
-  }
-  const bool key0_mode = p.m.sink_mode == 1 && p.m.sinks != nullptr;
-
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // Loads follow the MMA consumption order: K_0, then per step j K_{j+1}
-    // and V_j.  K is released per 64-dim chunk (as the QK MMAs of that chunk
-    // finish) and V per 32-key chunk (as the PV MMAs over those keys finish),
-    // so the next tile streams in while the current one is still in use.
+    // Per item: Q, then K_0, then per step j K_{j+1} and V_j (the MMA
+    // consumption order); stage counters run across items.
     if (lane == 0) {
-      bool ok = true;
-      int kc = 0, vc = 0;  // tiles issued
-      int k_armed[16], v_armed[16];  // times each full barrier was armed
+      tma_prefetch_desc(&map_q);
+      tma_prefetch_desc(&map_k);
+      tma_prefetch_desc(&map_v);
+    }
+    bool ok = true;
+    int qn = 0, kc = 0, vc = 0;  // Q / K / V tiles issued
+    int k_armed[4] = {0, 0, 0, 0}, v_armed[4] = {0, 0, 0, 0};
+    for (int n = 0; ok; ++n) {
+      PlanEntry e;
+      ok = consume_plan(sb, n, lane, e, p.err);
+      if (!ok || e.last) break;
+      const Item& it = e.it;
+      const Plan& pl = e.pl;
+      if (pl.n_tiles == 0) continue;
+      if (lane == 0) {
+        if (qn > 0 && !mbar_wait(&sb.q_empty, (qn - 1) & 1, &sb.abort_flag, p.err, kDevTimeoutMma)) ok = false;
+        if (ok) {
+          mbar_arrive_expect_tx(&sb.q_full, C::Q_BYTES);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) k_armed[i] = v_armed[i] = 0;
-      auto load_k = [&](int j) -> bool {
-        const int s = kc % C::KST;
-        const int krow = k0 + (kb_lo + j) * BN;
-        uint8_t* dst = sK + s * C::K_BYTES;
-#pragma unroll
-        for (int g = 0; g < C::KBC; ++g) {
-          uint64_t* full = &sb.k_full[s * C::KBC + g];
-          if (kc >= C::KST &&
-              !mbar_wait(&sb.k_empty[s * C::KBC + g], ((kc / C::KST) - 1) & 1, &sb.abort_flag, p.err,
-                         kDevTimeoutLoad))
-            return false;
-          mbar_arrive_expect_tx(full, C::KB * C::K_CHUNK_BYTES);
-#pragma unroll
-          for (int cc = 0; cc < C::KB; ++cc) {
-            const int c = g * C::KB + cc;
-            tma_load_3d(dst + c * C::K_CHUNK_BYTES, &map_k, full, c * 64, hkv, krow);
-          }
-          ++k_armed[s * C::KBC + g];
+          for (int c = 0; c < C::QCH; ++c)
+            tma_load_3d(sQ + c * (kBM * 128), &map_q, &sb.q_full, c * 64, it.h0, it.q0 + it.pos0);
+          ++qn;
         }
-        ++kc;
-        return true;
-      };
-      auto load_v = [&](int j) -> bool {
-        const int s = vc % C::VST;
-        const int krow = k0 + (kb_lo + j) * BN;
-        uint8_t* dst = sV + s * C::V_BYTES;
-#pragma unroll
-        for (int q = 0; q < C::VKC; ++q) {
-          uint64_t* full = &sb.v_full[s * C::VKC + q];
-          if (vc >= C::VST &&
-              !mbar_wait(&sb.v_empty[s * C::VKC + q], ((vc / C::VST) - 1) & 1, &sb.abort_flag, p.err,
-                         kDevTimeoutLoad))
+        auto load_k = [&](int j) -> bool {
+          const int s = kc % C::KST;
+          if (kc >= C::KST &&
+              !mbar_wait(&sb.k_empty[s], ((kc / C::KST) - 1) & 1, &sb.abort_flag, p.err, kDevTimeoutLoad))
             return false;
-          mbar_arrive_expect_tx(full, C::V_KEYCHUNK_BYTES);
+          mbar_arrive_expect_tx(&sb.k_full[s], C::K_BYTES);
+          const int krow = it.k0 + (pl.kb_lo + j) * BN;
+#pragma unroll
+          for (int c = 0; c < C::QCH; ++c)
+            tma_load_3d(sK + s * C::K_BYTES + c * (BN * 128), &map_k, &sb.k_full[s], c * 64, it.hkv, krow);
+          ++k_armed[s];
+          ++kc;
+          return true;
+        };
+        auto load_v = [&](int j) -> bool {
+          const int s = vc % C::VST;
+          if (vc >= C::VST &&
+              !mbar_wait(&sb.v_empty[s], ((vc / C::VST) - 1) & 1, &sb.abort_flag, p.err, kDevTimeoutLoad))
+            return false;
+          mbar_arrive_expect_tx(&sb.v_full[s], C::V_BYTES);
+          const int krow = it.k0 + (pl.kb_lo + j) * BN;
 #pragma unroll
           for (int c = 0; c < C::VCH; ++c)
-            tma_load_3d(dst + c * (BN * 128) + q * C::VK * 128, &map_v, full, dv0 + c * 64, hkv, krow + q * C::VK);
-          ++v_armed[s * C::VKC + q];
+            tma_load_3d(sV + s * C::V_BYTES + c * (BN * 128), &map_v, &sb.v_full[s], it.dv0 + c * 64, it.hkv,
+                        krow);
+          ++v_armed[s];
+          ++vc;
+          return true;
+        };
+        if (ok) ok = load_k(0);
+        for (int j = 0; ok && j < pl.n_tiles; ++j) {
+          if (j + 1 < pl.n_tiles) ok = load_k(j + 1);
+          if (ok) ok = load_v(j);
         }
-        ++vc;
-        return true;
-      };
-      if (n_tiles > 0) ok = load_k(0);
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        if (j + 1 < n_tiles) ok = load_k(j + 1);
-        if (ok) ok = load_v(j);
       }
-      // Drain: never leave the CTA with a TMA write still in flight.  Each
-      // full barrier's last armed phase is waited for; these waits ignore the
-      // CTA abort flag (issued copies always complete, and they must before
-      // the CTA exits).
+      ok = __shfl_sync(kFullMask, ok, 0);
+    }
+    // Drain: never leave the CTA with a TMA write still in flight.  Each
+    // full barrier's last armed phase is waited for, ignoring the CTA abort
+    // flag (issued copies always complete, and must before the CTA exits).
+    if (lane == 0) {
       if (!ok) sb.abort_flag = 1;
       volatile int own_flag = 0;
-      mbar_wait(&sb.q_full, 0, &own_flag, nullptr, 0);
-      for (int i = 0; i < 16; ++i) {
+      if (qn > 0) mbar_wait(&sb.q_full, (qn - 1) & 1, &own_flag, nullptr, 0);
+      for (int i = 0; i < 4; ++i) {
         if (k_armed[i] > 0) mbar_wait(&sb.k_full[i], (k_armed[i] - 1) & 1, &own_flag, nullptr, 0);
         if (v_armed[i] > 0) mbar_wait(&sb.v_full[i], (v_armed[i] - 1) & 1, &own_flag, nullptr, 0);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // One thread issues every tcgen05.mma.  Descriptors are computed once;
-    // inside the unrolled loops each MMA only adds a compile-time offset, so
-    // the issue loop stays shorter than the tensor core's work.
-    if (lane == 0) {
-      constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, C::BN, false, false);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, C::DV, false, true);
-      const uint64_t dq = smem_desc_sw128(smem_u32(sQ), 16, 1024);
-      const uint64_t dk0 = smem_desc_sw128(smem_u32(sK), 16, 1024);
-      const uint64_t dv0 = smem_desc_sw128(smem_u32(sV), BN * 128, 1024);
-      bool ok = n_tiles > 0 ? mbar_wait(&sb.q_full, 0, &sb.abort_flag, p.err, kDevTimeoutLoad) : true;
-      for (int j = 0; ok && j <= n_tiles; ++j) {
-        if (j < n_tiles) {
-          const int s = j % C::KST;
-          const uint32_t d = tmem + C::S_COL + (j & 1) * BN;
-          const uint64_t dk = dk0 + static_cast<uint64_t>((s * C::K_BYTES) >> 4);
-#pragma unroll
-          for (int g = 0; g < C::KBC; ++g) {
-            // smem written by TMA and published by the mbarrier needs no
-            // tcgen05 fence; only TMEM hand-offs between threads do.
-            if (!mbar_wait(&sb.k_full[s * C::KBC + g], (j / C::KST) & 1, &sb.abort_flag, p.err, kDevTimeoutLoad)) {
+    // One thread issues every tcgen05.mma; descriptors are computed once and
+    // each MMA only adds a compile-time offset.  Tile t is the CTA-wide tile
+    // index: S buffer t & 1, K stage t % KST, V stage t % VST.
+    constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, C::BN, false, false);
+    constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, C::DV, false, true);
+    const uint64_t dq = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+    const uint64_t dk0 = smem_desc_sw128(smem_u32(sK), 16, 1024);
+    const uint64_t dv0 = smem_desc_sw128(smem_u32(sV), BN * 128, 1024);
+    bool ok = true;
+    int T = 0, qn = 0;
+    for (int n = 0; ok; ++n) {
+      PlanEntry e;
+      ok = consume_plan(sb, n, lane, e, p.err);
+      if (!ok || e.last) break;
+      const Plan& pl = e.pl;
+      if (pl.n_tiles == 0) continue;
+      if (lane == 0) {
+        ok = mbar_wait(&sb.q_full, qn & 1, &sb.abort_flag, p.err, kDevTimeoutLoad);
+        ++qn;
+        for (int j = 0; ok && j <= pl.n_tiles; ++j) {
+          if (j < pl.n_tiles) {
+            const int t = T + j;
+            const int s = t % C::KST;
+            if (!mbar_wait(&sb.k_full[s], (t / C::KST) & 1, &sb.abort_flag, p.err, kDevTimeoutLoad)) {
               ok = false;
               break;
             }
+            const uint32_t d = tmem + C::S_COL + (t & 1) * BN;
+            const uint64_t dk = dk0 + static_cast<uint64_t>((s * C::K_BYTES) >> 4);
 #pragma unroll
-            for (int cc = 0; cc < C::KB; ++cc) {
-              const int c = g * C::KB + cc;
+            for (int c = 0; c < C::QCH; ++c) {
 #pragma unroll
               for (int k16 = 0; k16 < 4; ++k16) {
                 const uint64_t a = dq + static_cast<uint64_t>((c * (kBM * 128) + k16 * 32) >> 4);
-                const uint64_t b = dk + static_cast<uint64_t>((c * C::K_CHUNK_BYTES + k16 * 32) >> 4);
+                const uint64_t b = dk + static_cast<uint64_t>((c * (BN * 128) + k16 * 32) >> 4);
                 mma_bf16_ss(d, a, b, idesc_qk, (c | k16) != 0 ? 1u : 0u);
               }
             }
-            mma_commit(&sb.k_empty[s * C::KBC + g]);
+            mma_commit(&sb.k_empty[s]);
+            if (j == pl.n_tiles - 1) mma_commit(&sb.q_empty);  // Q free for the next item
+            mma_commit(&sb.s_full[t & 1]);
           }
-          if (!ok) break;
-          mma_commit(&sb.s_full[j & 1]);
-        }
-        if (j >= 1) {
-          const int i = j - 1;
-          if (!mbar_wait(&sb.p_full[i & 1], (i >> 1) & 1, &sb.abort_flag, p.err, kDevTimeoutSoftmax)) { ok = false; break; }
-          tc_fence_after();
-          const int s = i % C::VST;
-          const uint32_t pcol = tmem + C::S_COL + (i & 1) * BN;
-          const uint64_t dv = dv0 + static_cast<uint64_t>((s * C::V_BYTES) >> 4);
-          const uint32_t first = (i > 0) ? 1u : 0u;
-#pragma unroll
-          for (int q = 0; q < C::VKC; ++q) {
-            if (!mbar_wait(&sb.v_full[s * C::VKC + q], (i / C::VST) & 1, &sb.abort_flag, p.err, kDevTimeoutLoad)) {
+          if (j >= 1) {
+            const int t = T + j - 1;
+            if (!mbar_wait(&sb.p_full[t & 1], (t >> 1) & 1, &sb.abort_flag, p.err, kDevTimeoutSoftmax)) {
               ok = false;
               break;
             }
-#pragma unroll
-            for (int h = 0; h < C::VK / 16; ++h) {
-              const int kk = q * (C::VK / 16) + h;  // 16-key step
-              const uint64_t b = dv + static_cast<uint64_t>((kk * 16 * 128) >> 4);
-              mma_bf16_ts(tmem + C::O_COL, pcol + kk * 8, b, idesc_pv, (q == 0 && h == 0) ? first : 1u);
+            tc_fence_after();  // P was written to TMEM by the softmax threads
+            const int s = t % C::VST;
+            if (!mbar_wait(&sb.v_full[s], (t / C::VST) & 1, &sb.abort_flag, p.err, kDevTimeoutLoad)) {
+              ok = false;
+              break;
             }
-            mma_commit(&sb.v_empty[s * C::VKC + q]);
+            const uint32_t pcol = tmem + C::S_COL + (t & 1) * BN;
+            const uint64_t dv = dv0 + static_cast<uint64_t>((s * C::V_BYTES) >> 4);
+            const uint32_t first = (j > 1) ? 1u : 0u;  // the item's first PV overwrites O
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk) {
+              const uint64_t b = dv + static_cast<uint64_t>((kk * 16 * 128) >> 4);
+              mma_bf16_ts(tmem + C::O_COL, pcol + kk * 8, b, idesc_pv, kk == 0 ? first : 1u);
+            }
+            mma_commit(&sb.v_empty[s]);
+            mma_commit(&sb.o_done[t & 1]);
           }
-          if (!ok) break;
-          mma_commit(&sb.o_done[i & 1]);
         }
+        T += pl.n_tiles;
       }
+      ok = __shfl_sync(kFullMask, ok, 0);
+    }
+    if (lane == 0) {
       if (!ok) sb.abort_flag = 1;
       // All issued MMAs must finish before TMEM is released.
       mma_commit(&sb.final_mma);
       volatile int own_flag = 0;
       mbar_wait(&sb.final_mma, 0, &own_flag, p.err, kDevTimeoutMma);
     }
-  } else {
+  } else if (warp < C::SCHED_WARP) {
     // ------------------------------------------------------------ softmax rows
     constexpr int HC = C::HC;
+    const int quarter = warp & 3;
+    const int half = (warp - 2) / 4;  // which column half of the row
+    const int row = quarter * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const float sc = p.m.scale_log2;  // > 0 (checked on the host)
-    float sink_l2 = 0.f, sink_raw = 0.f;
-    if (p.m.sink_mode != 0 && p.m.sinks != nullptr) {
-      const float sk = __ldg(p.m.sinks + head);
-      sink_l2 = sk * 1.4426950408889634f;  // log2 units
-      sink_raw = sk / p.m.scale;            // units of the raw q.k score
-    }
+    const bool key0_mode = p.m.sink_mode == 1 && p.m.sinks != nullptr;
     const bool null_mode = p.m.sink_mode == 2 && p.m.sinks != nullptr;
-    float m_ref = null_mode ? sink_l2 : -INFINITY;
-    // Partial row sums of this thread's columns: the bf16-rounded
-    // probabilities (they normalise O, which the PV MMA builds from them) and
-    // the unrounded ones (they give the LSE).  The null-logit term counts once.
-    float l_sum = (null_mode && half == 0) ? 1.f : 0.f;
-    float l_lse = l_sum;
-    float* red = reinterpret_cast<float*>(smem + C::RED_OFF);  // [2 parity][SPLIT][128]
+    float2* xslots = reinterpret_cast<float2*>(smem + C::RED_OFF);
+    uint64_t* xb = sb.xchg[quarter];
+    int xk = 0;  // exchanges done by this thread
+    const bool out_v8 = (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0;
     bool ok = true;
+    int T = 0, n = 0;
+    // This thread's row of an item: geometry, visible intervals and sink.
+    struct RowCtx {
+      int head, qi;
+      bool valid;
+      RowVis vis;
+      float sink;
+    };
+    auto row_ctx = [&](const PlanEntry& e) {
+      RowCtx r;
+      r.head = e.it.h0 + (row % p.gpack);
+      r.qi = e.it.pos0 + row / p.gpack;
+      r.valid = !e.last && r.qi < e.it.q_len;
+      r.vis = r.valid ? row_visibility(p.m, e.it.ctx + r.qi, e.it.k_len, use_table ? (e.it.q0 + r.qi) : -1)
+                      : empty_row();
+      r.sink = (!e.last && p.m.sink_mode != 0 && p.m.sinks != nullptr) ? __ldg(p.m.sinks + r.head) : 0.f;
+      return r;
+    };
+    PlanEntry cur;
+    ok = consume_plan(sb, n++, lane, cur, p.err);
+    RowCtx rc = row_ctx(cur);
+    while (ok && !cur.last) {
+      const Item& it = cur.it;
+      const Plan& pl = cur.pl;
+      const int head = rc.head;
+      const int qi = rc.qi;
+      const bool row_valid = rc.valid;
+      const RowVis vis = rc.vis;
+      const float sink_l2 = rc.sink * 1.4426950408889634f;  // log2 units
+      const float sink_raw = rc.sink / p.m.scale;            // units of the raw q.k score
+      float m_ref = null_mode ? sink_l2 : -INFINITY;
+      // Partial row sums of this thread's columns: the bf16-rounded
+      // probabilities (they normalise O, which the PV MMA builds from them)
+      // and the unrounded ones (they give the LSE).  The null logit counts once.
+      float l_sum = (null_mode && half == 0) ? 1.f : 0.f;
+      float l_lse = l_sum;
 
-    for (int j = 0; j < n_tiles; ++j) {
-      const int kb = kb_lo + j;
-      const uint32_t scol = tmem + lane_base + C::S_COL + (j & 1) * BN;
-      if (!mbar_wait(&sb.s_full[j & 1], (j >> 1) & 1, &sb.abort_flag, p.err, kDevTimeoutMma)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t s[HC];
+      for (int j = 0; j < pl.n_tiles; ++j) {
+        const int t = T + j;
+        const int kb = pl.kb_lo + j;
+        const uint32_t scol = tmem + lane_base + C::S_COL + (t & 1) * BN;
+        if (!mbar_wait(&sb.s_full[t & 1], (t >> 1) & 1, &sb.abort_flag, p.err, kDevTimeoutMma)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t s[HC];
 #pragma unroll
-      for (int c = 0; c < HC / 32; ++c)
-        tmem_ld_32x32b_x32(scol + half * HC + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[c * 32]));
+        for (int c = 0; c < HC / 32; ++c)
+          tmem_ld_32x32b_x32(scol + half * HC + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[c * 32]));
 #pragma unroll
-      for (int c = 0; c < HC / 32; ++c) tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(&s[c * 32]));
+        for (int c = 0; c < HC / 32; ++c) tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(&s[c * 32]));
 
-      // Mask: one bit per key of this thread's 64 columns.  Scores stay in raw
-      // q.k units; the scale folds into the exponent's FFMA (scale > 0).
-      const bool masked = !(kb >= int_lo && kb <= int_hi) || (key0_mode && kb == 0);
-      if (masked) {
-        const int c0 = kb * BN + half * HC;  // first key of these columns
-        if (key0_mode && c0 == 0 && vis.visible(0)) s[0] = __float_as_uint(__uint_as_float(s[0]) + sink_raw);
+        // Mask: one bit per key of this thread's columns.  Scores stay in raw
+        // q.k units; the scale folds into the exponent's FFMA (scale > 0).
+        const bool masked = !(kb >= pl.int_lo && kb <= pl.int_hi) || (key0_mode && kb == 0);
+        if (masked) {
+          const int c0 = kb * BN + half * HC;  // first key of these columns
+          if (key0_mode && c0 == 0 && vis.visible(0)) s[0] = __float_as_uint(__uint_as_float(s[0]) + sink_raw);
 #pragma unroll
-        for (int w = 0; w < HC / 32; ++w) {
-          const uint32_t bits = interval_bits(vis.b_lo, vis.b_hi, c0 + 32 * w) |
-                                interval_bits(vis.r_lo, vis.r_hi, c0 + 32 * w);
+          for (int w = 0; w < HC / 32; ++w) {
+            const uint32_t bits = interval_bits(vis.b_lo, vis.b_hi, c0 + 32 * w) |
+                                  interval_bits(vis.r_lo, vis.r_hi, c0 + 32 * w);
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            s[32 * w + i] = ((bits >> i) & 1u) ? s[32 * w + i] : __float_as_uint(-INFINITY);
+            for (int i = 0; i < 32; ++i)
+              s[32 * w + i] = ((bits >> i) & 1u) ? s[32 * w + i] : __float_as_uint(-INFINITY);
+          }
+        }
+        float mx8[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(__uint_as_float(s[k]), __uint_as_float(s[k + 8]));
+#pragma unroll
+        for (int i = 16; i < HC; i += 16)
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mx8[k] = fmax3(mx8[k], __uint_as_float(s[i + k]), __uint_as_float(s[i + 8 + k]));
+        float mx_raw = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
+        if constexpr (C::SPLIT > 1) {
+          // the two halves of a row meet once per tile
+          float2 other;
+          if (!pair_exchange(xslots, xb, xk, half, row, make_float2(mx_raw, 0.f), other, &sb.abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          mx_raw = fmaxf(mx_raw, other.x);
+        }
+        const float mx = mx_raw * sc;
+        // lazy reference max
+        float alpha = 1.f;
+        const bool need = (mx > m_ref + kRescaleThreshold) || (m_ref == -INFINITY && mx > -INFINITY);
+        if (need) {
+          alpha = ex2_approx(m_ref - mx);  // 0 when m_ref == -inf
+          l_sum *= alpha;
+          l_lse *= alpha;
+          m_ref = mx;
+        }
+        const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+        const uint64_t sc2 = f2_pack(sc, sc);
+        const uint64_t nm2 = f2_pack(-m_use, -m_use);
+        uint64_t acc_r[4], acc_e[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc_r[k] = acc_e[k] = 0ull;
+#pragma unroll
+        for (int i = 0; i < HC / 2; ++i) {
+          float t0, t1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])), sc2, nm2), t0, t1);
+          const float e0 = ex2_approx(t0);
+          const float e1 = ex2_approx(t1);
+          const uint32_t pk = pack_bf16x2(e0, e1);
+          acc_r[i & 3] = f2_add(acc_r[i & 3], f2_pack(__uint_as_float(pk << 16), __uint_as_float(pk & 0xffff0000u)));
+          acc_e[i & 3] = f2_add(acc_e[i & 3], f2_pack(e0, e1));
+          s[i] = pk;
+        }
+        {
+          float a0, a1, b0, b1;
+          f2_unpack(f2_add(f2_add(acc_r[0], acc_r[1]), f2_add(acc_r[2], acc_r[3])), a0, a1);
+          f2_unpack(f2_add(f2_add(acc_e[0], acc_e[1]), f2_add(acc_e[2], acc_e[3])), b0, b1);
+          l_sum += a0 + a1;
+          l_lse += b0 + b1;
+        }
+        // P (bf16 pairs) over this half's scores.  Both halves have their
+        // scores in registers (the exchange above), so neither overwrites
+        // columns the other still has to read.
+#pragma unroll
+        for (int c = 0; c < HC / 64; ++c)
+          tmem_st_32x32b_x32(scol + half * (HC / 2) + c * 32, *reinterpret_cast<const uint32_t(*)[32]>(&s[c * 32]));
+
+        // O correction for rows whose reference moved (warp-uniform branch:
+        // tcgen05.ld/st are warp-collective); each half corrects its columns.
+        if (j > 0 && __any_sync(kFullMask, need)) {
+          const int tp = t - 1;  // the previous tile's PV must have landed in O
+          if (!mbar_wait(&sb.o_done[tp & 1], (tp >> 1) & 1, &sb.abort_flag, p.err, kDevTimeoutMma)) ok = false;
+          if (ok) {
+            tc_fence_after();
+            const uint32_t ocol = tmem + lane_base + C::O_COL + half * C::HDV;
+#pragma unroll 1
+            for (int c = 0; c < C::HDV / 32; ++c) {
+              uint32_t o[32];
+              tmem_ld_32x32b_x32(ocol + c * 32, o);
+              tmem_ld_wait(o);
+#pragma unroll
+              for (int u = 0; u < 32; ++u) o[u] = __float_as_uint(__uint_as_float(o[u]) * alpha);
+              tmem_st_32x32b_x32(ocol + c * 32, o);
+            }
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&sb.p_full[t & 1]);
+        if (!ok) break;
+      }
+
+      // ---------------------------------------------------------- epilogue
+      // Take the next item's plan and start its row lookups (the range-table
+      // load) before this item's epilogue, which hides their latency.
+      PlanEntry nxt;
+      if (ok) ok = consume_plan(sb, n++, lane, nxt, p.err);
+      if (!ok) nxt.last = 1;
+      const RowCtx nrc = row_ctx(nxt);
+      if constexpr (C::SPLIT > 1) {
+        // combine the halves' partial sums
+        float2 other;
+        if (ok && pair_exchange(xslots, xb, xk, half, row, make_float2(l_sum, l_lse), other, &sb.abort_flag, p.err)) {
+          l_sum += other.x;
+          l_lse += other.y;
+        } else {
+          ok = false;
         }
       }
-      float mx8[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(__uint_as_float(s[k]), __uint_as_float(s[k + 8]));
-#pragma unroll
-      for (int i = 16; i < HC; i += 16)
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mx8[k] = fmax3(mx8[k], __uint_as_float(s[i + k]), __uint_as_float(s[i + 8 + k]));
-      float mx_raw = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
-      if constexpr (C::SPLIT > 1) {
-        // the two halves of a row meet once per tile (double-buffered by parity)
-        float* slot = red + (j & 1) * (C::SPLIT * kBM);
-        slot[half * kBM + row] = mx_raw;
-        named_barrier(1 + quarter, 64);
-        mx_raw = fmaxf(mx_raw, slot[(1 - half) * kBM + row]);
+      bool have_o = ok && pl.n_tiles > 0;
+      if (have_o) {
+        const int tl = T + pl.n_tiles - 1;  // the item's last PV
+        have_o = mbar_wait(&sb.o_done[tl & 1], (tl >> 1) & 1, &sb.abort_flag, p.err, kDevTimeoutMma);
+        tc_fence_after();
       }
-      const float mx = mx_raw * sc;
-      // lazy reference max
-      float alpha = 1.f;
-      const bool need = (mx > m_ref + kRescaleThreshold) || (m_ref == -INFINITY && mx > -INFINITY);
-      if (need) {
-        alpha = ex2_approx(m_ref - mx);  // 0 when m_ref == -inf
-        l_sum *= alpha;
-        l_lse *= alpha;
-        m_ref = mx;
-      }
-      const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-      const uint64_t sc2 = f2_pack(sc, sc);
-      const uint64_t nm2 = f2_pack(-m_use, -m_use);
-      uint64_t acc_r[4], acc_e[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) acc_r[k] = acc_e[k] = 0ull;
-#pragma unroll
-      for (int i = 0; i < HC / 2; ++i) {
-        float t0, t1;
-        f2_unpack(f2_fma(f2_pack(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])), sc2, nm2), t0, t1);
-        const float e0 = ex2_approx(t0);
-        const float e1 = ex2_approx(t1);
-        const uint32_t pk = pack_bf16x2(e0, e1);
-        acc_r[i & 3] = f2_add(acc_r[i & 3], f2_pack(__uint_as_float(pk << 16), __uint_as_float(pk & 0xffff0000u)));
-        acc_e[i & 3] = f2_add(acc_e[i & 3], f2_pack(e0, e1));
-        s[i] = pk;
-      }
-      {
-        float a0, a1, b0, b1;
-        f2_unpack(f2_add(f2_add(acc_r[0], acc_r[1]), f2_add(acc_r[2], acc_r[3])), a0, a1);
-        f2_unpack(f2_add(f2_add(acc_e[0], acc_e[1]), f2_add(acc_e[2], acc_e[3])), b0, b1);
-        l_sum += a0 + a1;
-        l_lse += b0 + b1;
-      }
-      // P (bf16 pairs) over this half's scores: HC/2 columns.  Both halves
-      // have their scores in registers (the exchange above), so neither can
-      // overwrite columns the other still has to read.
-#pragma unroll
-      for (int c = 0; c < HC / 64; ++c)
-        tmem_st_32x32b_x32(scol + half * (HC / 2) + c * 32, *reinterpret_cast<const uint32_t(*)[32]>(&s[c * 32]));
-
-      // O correction for rows whose reference moved (warp-uniform branch:
-      // tcgen05.ld/st are warp-collective); each half corrects its columns.
-      if (j > 0 && __any_sync(0xffffffffu, need)) {
-        const int i = j - 1;  // PV_{j-1} must have landed in O
-        if (!mbar_wait(&sb.o_done[i & 1], (i >> 1) & 1, &sb.abort_flag, p.err, kDevTimeoutMma)) { ok = false; }
-        if (ok) {
-          tc_fence_after();
-          const uint32_t ocol = tmem + lane_base + C::O_COL + half * C::HDV;
+      if (!have_o && pl.n_tiles > 0) ok = false;
+      // Normalise O and store this thread's row segment (TMEM loads two
+      // 32-column chunks per wait; 32-byte stores when the output allows).
+      const float inv_l = (l_sum > 0.f) ? 1.f / l_sum : 0.f;
+      __nv_bfloat16* orow = nullptr;
+      if (row_valid)
+        orow = reinterpret_cast<__nv_bfloat16*>(p.out) + (static_cast<size_t>(it.q0 + qi) * p.hq + head) * C::D +
+               it.dv0 + half * C::HDV;
+      const uint32_t ocol = tmem + lane_base + C::O_COL + half * C::HDV;
+      constexpr int EB = C::HDV >= 64 ? 2 : 1;  // 32-column chunks per TMEM wait
 #pragma unroll 1
-          for (int c = 0; c < C::HDV / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld_32x32b_x32(ocol + c * 32, o);
-            tmem_ld_wait(o);
+      for (int c = 0; c < C::HDV / (32 * EB); ++c) {
+        uint32_t o[EB][32];
+        if (have_o) {
 #pragma unroll
-            for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * alpha);
-            tmem_st_32x32b_x32(ocol + c * 32, o);
+          for (int u = 0; u < EB; ++u) tmem_ld_32x32b_x32(ocol + (c * EB + u) * 32, o[u]);
+#pragma unroll
+          for (int u = 0; u < EB; ++u) tmem_ld_wait(o[u]);
+        } else {
+#pragma unroll
+          for (int u = 0; u < EB; ++u)
+#pragma unroll
+            for (int v = 0; v < 32; ++v) o[u][v] = 0u;
+        }
+        if (row_valid) {
+#pragma unroll
+          for (int u = 0; u < EB; ++u) {
+            uint32_t packed[16];
+#pragma unroll
+            for (int v = 0; v < 16; ++v)
+              packed[v] =
+                  pack_bf16x2(__uint_as_float(o[u][2 * v]) * inv_l, __uint_as_float(o[u][2 * v + 1]) * inv_l);
+            __nv_bfloat16* dst = orow + (c * EB + u) * 32;
+            if (out_v8) {
+              st_global_v8(dst, packed);
+              st_global_v8(dst + 16, packed + 8);
+            } else {
+              uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+              for (int v = 0; v < 4; ++v)
+                d4[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+            }
           }
         }
       }
-      tmem_st_wait();
+      if (row_valid && half == 0 && p.lse != nullptr && it.dv0 == 0) {
+        const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+        const float lse = (l_lse > 0.f) ? (m_use + lg2_approx(l_lse)) * 0.6931471805599453f : -INFINITY;
+        p.lse[static_cast<size_t>(head) * p.total_q + it.q0 + qi] = lse;
+      }
+      // O may be overwritten by the next item's first PV only after these
+      // TMEM reads: the next p_full arrival of these threads orders them.
       tc_fence_before();
-      mbar_arrive(&sb.p_full[j & 1]);
-      if (!ok) break;
+      T += pl.n_tiles;
+      cur = nxt;
+      rc = nrc;
     }
-
-    // ---------------------------------------------------------- epilogue
-    if constexpr (C::SPLIT > 1) {
-      // Combine the halves' partial sums.  After the first barrier neither
-      // half still reads the last tile's max slot, so both parity slots are
-      // free: one carries l_sum, the other l_lse.
-      float* sa = red + (n_tiles & 1) * (C::SPLIT * kBM);
-      float* sb2 = red + ((n_tiles + 1) & 1) * (C::SPLIT * kBM);
-      named_barrier(1 + quarter, 64);
-      sa[half * kBM + row] = l_sum;
-      sb2[half * kBM + row] = l_lse;
-      named_barrier(1 + quarter, 64);
-      l_sum += sa[(1 - half) * kBM + row];
-      l_lse += sb2[(1 - half) * kBM + row];
-    }
-    bool have_o = ok && n_tiles > 0;
-    if (have_o) {
-      const int i = n_tiles - 1;
-      have_o = mbar_wait(&sb.o_done[i & 1], (i >> 1) & 1, &sb.abort_flag, p.err, kDevTimeoutMma);
-      tc_fence_after();
-    }
-    const float inv_l = (l_sum > 0.f) ? 1.f / l_sum : 0.f;
-    __nv_bfloat16* orow = nullptr;
-    if (row_valid)
-      orow = reinterpret_cast<__nv_bfloat16*>(p.out) + (static_cast<size_t>(q0 + qi) * p.hq + head) * C::D + dv0 +
-             half * C::HDV;
-    const uint32_t ocol = tmem + lane_base + C::O_COL + half * C::HDV;
-#pragma unroll 1
-    for (int c = 0; c < C::HDV / 32; ++c) {
-      uint32_t o[32];
-      if (have_o) {
-        tmem_ld_32x32b_x32(ocol + c * 32, o);
-        tmem_ld_wait(o);
-      } else {
-#pragma unroll
-        for (int t = 0; t < 32; ++t) o[t] = 0u;
+  } else {
+    // ------------------------------------------------------------ scheduler
+    // Walks this CTA's items (static stride), computes each valid item's
+    // geometry and key-tile plan, and publishes them through the plan ring,
+    // up to kPlanRing items ahead of the slowest consumer warp.
+    int n = 0;
+    bool ok = true;
+    auto publish = [&](const PlanEntry& e) -> bool {
+      const int slot = n % kPlanRing;
+      bool good = true;
+      if (lane == 0 && n >= kPlanRing)
+        good = mbar_wait(&sb.plan_empty[slot], ((n / kPlanRing) - 1) & 1, &sb.abort_flag, p.err, kDevTimeoutOther);
+      good = __shfl_sync(kFullMask, good, 0);
+      if (good && lane == 0) {
+        sb.plans[slot] = e;
+        mbar_arrive(&sb.plan_full[slot]);  // release: the entry is visible to the waiting consumers
       }
-      if (row_valid) {
-        uint32_t packed[16];
-#pragma unroll
-        for (int t = 0; t < 16; ++t)
-          packed[t] = pack_bf16x2(__uint_as_float(o[2 * t]) * inv_l, __uint_as_float(o[2 * t + 1]) * inv_l);
-        uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-        for (int t = 0; t < 4; ++t)
-          dst[t] = make_uint4(packed[4 * t], packed[4 * t + 1], packed[4 * t + 2], packed[4 * t + 3]);
-      }
+      ++n;
+      return good;
+    };
+    for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+      PlanEntry e;
+      e.it = item_geometry<C>(item, p);
+      if (!e.it.valid) continue;
+      e.pl = plan_tiles<C>(e.it, p, use_table, lane);
+      e.last = 0;
+      ok = publish(e);
     }
-    if (row_valid && half == 0 && p.lse != nullptr && dv0 == 0) {
-      const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-      const float lse = (l_lse > 0.f) ? (m_use + lg2_approx(l_lse)) * 0.6931471805599453f : -INFINITY;
-      p.lse[static_cast<size_t>(head) * p.total_q + q0 + qi] = lse;
+    if (ok) {
+      PlanEntry e{};
+      e.last = 1;
+      publish(e);
     }
   }
 
@@ -553,13 +721,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
-// Whole-tile load barriers: every extra tcgen05.commit / mbarrier wait costs
-// issue slots of the single MMA thread, and finer release granularity was
-// measured slower on GB300.
-using Cfg64 = Cfg<64, 64, 128, 4, 4, 1, 128>;
-using Cfg128 = Cfg<128, 128, 128, 2, 2, 2, 128>;
-using Cfg256 = Cfg<256, 256, 128, 1, 1, 4, 128>;
-using Cfg512 = Cfg<512, 256, 64, 1, 1, 8, 64>;
+using Cfg64 = Cfg<64, 64, 128, 4, 4>;
+using Cfg128 = Cfg<128, 128, 128, 2, 2>;
+using Cfg256 = Cfg<256, 256, 128, 1, 1>;
+using Cfg512 = Cfg<512, 256, 64, 1, 1>;
 
 template <class C>
 cudaError_t launch_cfg(const PrefillParams& p, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
@@ -567,8 +732,11 @@ cudaError_t launch_cfg(const PrefillParams& p, const CUtensorMap& mq, const CUte
   auto kern = attn_prefill_kernel<C>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  const int dv_split = C::D / C::DV;
-  dim3 grid(p.n_qtiles, p.num_reqs - p.req_offset, p.hkv * p.n_hgroups * dv_split);
+  const long long n_items =
+      static_cast<long long>(p.n_qtiles) * (p.num_reqs - p.req_offset) * p.hkv * p.n_hgroups * C::DV_SPLIT;
+  if (n_items <= 0) return cudaSuccess;
+  if (n_items > INT_MAX) return cudaErrorInvalidValue;
+  const int grid = static_cast<int>(n_items < p.n_ctas ? n_items : p.n_ctas);
   kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
@@ -577,10 +745,10 @@ cudaError_t launch_cfg(const PrefillParams& p, const CUtensorMap& mq, const CUte
 
 PrefillShape prefill_tile_shape(int head_dim) {
   switch (head_dim) {
-    case 64: return {Cfg64::BN, Cfg64::DV, 1, Cfg64::VK};
-    case 128: return {Cfg128::BN, Cfg128::DV, 1, Cfg128::VK};
-    case 256: return {Cfg256::BN, Cfg256::DV, 1, Cfg256::VK};
-    case 512: return {Cfg512::BN, Cfg512::DV, Cfg512::D / Cfg512::DV, Cfg512::VK};
+    case 64: return {Cfg64::BN, Cfg64::DV, Cfg64::DV_SPLIT, Cfg64::BN};
+    case 128: return {Cfg128::BN, Cfg128::DV, Cfg128::DV_SPLIT, Cfg128::BN};
+    case 256: return {Cfg256::BN, Cfg256::DV, Cfg256::DV_SPLIT, Cfg256::BN};
+    case 512: return {Cfg512::BN, Cfg512::DV, Cfg512::DV_SPLIT, Cfg512::BN};
     default: return {0, 0, 0, 0};
   }
 }

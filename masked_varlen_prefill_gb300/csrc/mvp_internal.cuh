@@ -53,7 +53,8 @@ struct PrefillParams {
   int n_hgroups;      // (hq / hkv) / gpack
   int n_qtiles;       // ceil(max_q_len / (128 / gpack))
   int skip_decode;    // requests with q_len == 1 are left to the decode kernel
-  int req_offset;     // first request of the grid (grid.y covers the rest)
+  int req_offset;     // first request covered (items walk [req_offset, num_reqs))
+  int n_ctas;         // persistent CTAs to launch (SM count)
 };
 
 // head_dim in {64, 128, 256, 512}.  Tensor maps are encoded by the caller
