@@ -279,68 +279,89 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // Per item: Q, then K_0, then per step j K_{j+1} and V_j (the MMA
-    // consumption order); stage counters run across items.
+    // Loads follow the order in which the MMA issuer frees the buffers: per
+    // item Q and K_0, then per step j K_{j+1} and V_j.  The next item's Q and
+    // K_0 go out before the current item's last V tile: they wait only for
+    // the last QK, which the tensor core finishes before the PV that frees
+    // that V stage.  Stage counters run across items.
     if (lane == 0) {
       tma_prefetch_desc(&map_q);
       tma_prefetch_desc(&map_k);
       tma_prefetch_desc(&map_v);
     }
     bool ok = true;
-    int qn = 0, kc = 0, vc = 0;  // Q / K / V tiles issued
+    int n = 0, qn = 0, kc = 0, vc = 0;  // plans taken, Q / K / V tiles issued
     int k_armed[4] = {0, 0, 0, 0}, v_armed[4] = {0, 0, 0, 0};
-    for (int n = 0; ok; ++n) {
-      PlanEntry e;
-      ok = consume_plan(sb, n, lane, e, p.err);
-      if (!ok || e.last) break;
-      const Item& it = e.it;
-      const Plan& pl = e.pl;
-      if (pl.n_tiles == 0) continue;
-      if (lane == 0) {
-        if (qn > 0 && !mbar_wait(&sb.q_empty, (qn - 1) & 1, &sb.abort_flag, p.err, kDevTimeoutMma)) ok = false;
-        if (ok) {
-          mbar_arrive_expect_tx(&sb.q_full, C::Q_BYTES);
-#pragma unroll
-          for (int c = 0; c < C::QCH; ++c)
-            tma_load_3d(sQ + c * (kBM * 128), &map_q, &sb.q_full, c * 64, it.h0, it.q0 + it.pos0);
-          ++qn;
+    // Next item that has key tiles (warp-collective); false at the end.
+    auto next_item = [&](PlanEntry& e) -> bool {
+      for (;;) {
+        if (!consume_plan(sb, n++, lane, e, p.err)) {
+          ok = false;
+          return false;
         }
-        auto load_k = [&](int j) -> bool {
-          const int s = kc % C::KST;
-          if (kc >= C::KST &&
-              !mbar_wait(&sb.k_empty[s], ((kc / C::KST) - 1) & 1, &sb.abort_flag, p.err, kDevTimeoutLoad))
-            return false;
-          mbar_arrive_expect_tx(&sb.k_full[s], C::K_BYTES);
-          const int krow = it.k0 + (pl.kb_lo + j) * BN;
+        if (e.last) return false;
+        if (e.pl.n_tiles > 0) return true;
+      }
+    };
+    auto load_q = [&](const PlanEntry& e) -> bool {
+      if (qn > 0 && !mbar_wait(&sb.q_empty, (qn - 1) & 1, &sb.abort_flag, p.err, kDevTimeoutMma)) return false;
+      mbar_arrive_expect_tx(&sb.q_full, C::Q_BYTES);
 #pragma unroll
-          for (int c = 0; c < C::QCH; ++c)
-            tma_load_3d(sK + s * C::K_BYTES + c * (BN * 128), &map_k, &sb.k_full[s], c * 64, it.hkv, krow);
-          ++k_armed[s];
-          ++kc;
-          return true;
-        };
-        auto load_v = [&](int j) -> bool {
-          const int s = vc % C::VST;
-          if (vc >= C::VST &&
-              !mbar_wait(&sb.v_empty[s], ((vc / C::VST) - 1) & 1, &sb.abort_flag, p.err, kDevTimeoutLoad))
-            return false;
-          mbar_arrive_expect_tx(&sb.v_full[s], C::V_BYTES);
-          const int krow = it.k0 + (pl.kb_lo + j) * BN;
+      for (int c = 0; c < C::QCH; ++c)
+        tma_load_3d(sQ + c * (kBM * 128), &map_q, &sb.q_full, c * 64, e.it.h0, e.it.q0 + e.it.pos0);
+      ++qn;
+      return true;
+    };
+    auto load_k = [&](const PlanEntry& e, int j) -> bool {
+      const int s = kc % C::KST;
+      if (kc >= C::KST &&
+          !mbar_wait(&sb.k_empty[s], ((kc / C::KST) - 1) & 1, &sb.abort_flag, p.err, kDevTimeoutLoad))
+        return false;
+      mbar_arrive_expect_tx(&sb.k_full[s], C::K_BYTES);
+      const int krow = e.it.k0 + (e.pl.kb_lo + j) * BN;
 #pragma unroll
-          for (int c = 0; c < C::VCH; ++c)
-            tma_load_3d(sV + s * C::V_BYTES + c * (BN * 128), &map_v, &sb.v_full[s], it.dv0 + c * 64, it.hkv,
-                        krow);
-          ++v_armed[s];
-          ++vc;
-          return true;
-        };
-        if (ok) ok = load_k(0);
-        for (int j = 0; ok && j < pl.n_tiles; ++j) {
-          if (j + 1 < pl.n_tiles) ok = load_k(j + 1);
-          if (ok) ok = load_v(j);
+      for (int c = 0; c < C::QCH; ++c)
+        tma_load_3d(sK + s * C::K_BYTES + c * (BN * 128), &map_k, &sb.k_full[s], c * 64, e.it.hkv, krow);
+      ++k_armed[s];
+      ++kc;
+      return true;
+    };
+    auto load_v = [&](const PlanEntry& e, int j) -> bool {
+      const int s = vc % C::VST;
+      if (vc >= C::VST &&
+          !mbar_wait(&sb.v_empty[s], ((vc / C::VST) - 1) & 1, &sb.abort_flag, p.err, kDevTimeoutLoad))
+        return false;
+      mbar_arrive_expect_tx(&sb.v_full[s], C::V_BYTES);
+      const int krow = e.it.k0 + (e.pl.kb_lo + j) * BN;
+#pragma unroll
+      for (int c = 0; c < C::VCH; ++c)
+        tma_load_3d(sV + s * C::V_BYTES + c * (BN * 128), &map_v, &sb.v_full[s], e.it.dv0 + c * 64, e.it.hkv,
+                    krow);
+      ++v_armed[s];
+      ++vc;
+      return true;
+    };
+    PlanEntry cur;
+    bool have = next_item(cur);
+    if (have && lane == 0) ok = load_q(cur) && load_k(cur, 0);
+    ok = __shfl_sync(kFullMask, ok, 0);
+    while (ok && have) {
+      const int nt = cur.pl.n_tiles;
+      if (lane == 0)
+        for (int j = 0; ok && j + 1 < nt; ++j) {
+          ok = load_k(cur, j + 1);
+          if (ok) ok = load_v(cur, j);
         }
+      ok = __shfl_sync(kFullMask, ok, 0);
+      PlanEntry nxt;
+      const bool have_next = ok && next_item(nxt);
+      if (lane == 0 && ok) {
+        if (have_next) ok = load_q(nxt) && load_k(nxt, 0);
+        if (ok) ok = load_v(cur, nt - 1);
       }
       ok = __shfl_sync(kFullMask, ok, 0);
+      cur = nxt;
+      have = have_next;
     }
     // Drain: never leave the CTA with a TMA write still in flight.  Each
     // full barrier's last armed phase is waited for, ignoring the CTA abort
