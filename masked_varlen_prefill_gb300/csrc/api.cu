@@ -207,14 +207,15 @@ int mvp_attn_fwd_varlen(const void* q, const void* k, const void* v, void* out, 
     pp.hkv = num_heads_kv;
     pp.gpack = gpack;
     pp.n_hgroups = group / gpack;
-    pp.n_qtiles = (max_q_len + bmp - 1) / bmp;
+    const int item_pos = bmp * shape.ncta;  // query positions per work item
+    pp.n_qtiles = (max_q_len + item_pos - 1) / item_pos;
     pp.skip_decode = 1;
     pp.req_offset = prefill_first;
     pp.n_ctas = num_sms;
 
     CUtensorMap mq, mk, mv;
     if (!encode_3d(&mq, q, head_dim, num_heads_q, total_q, 64, gpack, bmp, true) ||
-        !encode_3d(&mk, k, head_dim, num_heads_kv, total_k, 64, 1, shape.bn, true) ||
+        !encode_3d(&mk, k, head_dim, num_heads_kv, total_k, 64, 1, shape.k_box_keys, true) ||
         !encode_3d(&mv, v, head_dim, num_heads_kv, total_k, 64, 1, shape.v_box_keys, true))
       return MVP_ERR_UNSUPPORTED;
     if (launch_prefill(head_dim, pp, mq, mk, mv, st) != cudaSuccess) return MVP_ERR_CUDA;

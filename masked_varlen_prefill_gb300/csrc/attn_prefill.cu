@@ -9,10 +9,16 @@
 // two closed key intervals per row (mask.cuh).
 //
 // GB300 design (not the pages' kernels):
-// * Work item = one 128-row tile.  With GQA, G_pack query heads of one KV head
-//   share the tile: row r is (position r / G_pack, head h0 + r % G_pack), so a
-//   K/V tile read from L2 serves G_pack heads.  The Q tile is a single 3-D TMA
-//   box (64 dims, G_pack heads, 128 / G_pack positions), 128-byte swizzled.
+// * Work item = NCTA 128-row tiles.  With GQA, G_pack query heads of one KV
+//   head share a tile: row r is (position r / G_pack, head h0 + r % G_pack), so
+//   a K/V tile read from L2 serves G_pack heads.  The Q tile is a single 3-D
+//   TMA box (64 dims, G_pack heads, 128 / G_pack positions), 128-byte swizzled.
+// * D = 128 and 256 run as CTA pairs (a 2-CTA cluster, tcgen05 .cta_group::2):
+//   each MMA is M = 256 (each CTA's 128 rows, scores and O in its own TMEM),
+//   each CTA loads only half of every K tile (its keys) and half of every V
+//   tile (its value columns), and rank 0 issues the MMAs for both.  A tile
+//   costs each SM half the L2 -> shared-memory bytes and half the shared
+//   memory, which buys two K and two V stages at D = 256.
 // * Persistent CTAs (one per SM) walk the items with a static stride, q tile
 //   fastest so that concurrent CTAs share K/V windows in L2.  Every role computes each item's geometry
 //   and key-tile plan itself (a warp reduction over the tile's 128 rows), and
@@ -51,15 +57,19 @@ constexpr int kBM = 128;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr unsigned kFullMask = 0xffffffffu;
 
-template <int D_, int DV_, int BN_, int KST_, int VST_>
+template <int D_, int DV_, int BN_, int KST_, int VST_, int NCTA_>
 struct Cfg {
   static constexpr int D = D_;
   static constexpr int DV = DV_;        // value columns handled by one item
   static constexpr int BN = BN_;        // keys per tile
   static constexpr int KST = KST_;      // K tile stages
   static constexpr int VST = VST_;      // V tile stages
+  static constexpr int NCTA = NCTA_;    // CTAs sharing each MMA (1, or 2 for a CTA pair)
+  static constexpr int KROWS = BN / NCTA;   // keys of a K tile loaded by one CTA
+  static constexpr int DVC = DV / NCTA;     // value columns of a V tile loaded by one CTA
+  static constexpr int ITEM_ROWS = kBM * NCTA;
   static constexpr int QCH = D / 64;    // 64-dim chunks of Q and K (one TMA box each)
-  static constexpr int VCH = DV / 64;   // 64-dim chunks of a V tile
+  static constexpr int VCH = DVC / 64;  // 64-column chunks of this CTA's part of a V tile
   static constexpr int DV_SPLIT = D / DV;
   static constexpr int SPLIT = BN / 64;         // softmax warpgroups (column halves of a row)
   static constexpr int HC = BN / SPLIT;         // score columns per softmax thread (64)
@@ -68,8 +78,8 @@ struct Cfg {
   static constexpr int SCHED_WARP = CONSUMER_WARPS;      // computes item plans ahead
   static constexpr int THREADS = 32 * (CONSUMER_WARPS + 1);
   static constexpr int Q_BYTES = kBM * D * 2;
-  static constexpr int K_BYTES = BN * D * 2;
-  static constexpr int V_BYTES = BN * DV * 2;
+  static constexpr int K_BYTES = KROWS * D * 2;  // per CTA
+  static constexpr int V_BYTES = BN * DVC * 2;    // per CTA
   static constexpr int Q_OFF = 0;
   static constexpr int K_OFF = Q_BYTES;
   static constexpr int V_OFF = K_OFF + KST * K_BYTES;
@@ -83,13 +93,22 @@ struct Cfg {
   static_assert(O_COL + DV <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM_BYTES <= 227 * 1024, "smem budget");
   static_assert(BN == 64 || BN == 128, "BN");
-  static_assert(DV % 64 == 0 && DV <= 256, "DV");
+  static_assert(DV % 64 == 0 && DV <= 256 && DVC % 64 == 0, "DV");
+  static_assert(NCTA == 1 || NCTA == 2, "NCTA");
   static_assert(HDV % 32 == 0, "O columns per thread");
   static_assert(KST >= 1 && KST <= 4 && VST >= 1 && VST <= 4, "stages");
+  // With two K and two V stages, "K stage of tile t free" is exactly "S_t
+  // computed" (s_full[t & 1]) and "V stage of tile t free" is "O += P_t V_t
+  // done" (o_done[t & 1]); the Q buffer is free once the item's last S is.
+  // The single MMA-issuing thread then commits twice per tile instead of
+  // four or five times (its issue rate bounds the tensor pipe).
+  static constexpr bool MERGED_RELEASE = KST == 2 && VST == 2;
 };
 
-// One work item: a 128-row query tile of one request, one KV head group and
-// (for D = 512) one half of the value dimension, with its key-tile plan.
+// One work item: NCTA 128-row query tiles of one request and one KV head
+// group ((for D = 512) one half of the value dimension), with its key-tile
+// plan.  pos0 is the item's first query position; CTA rank r of a pair owns
+// positions pos0 + r * 128 / G_pack onwards.
 struct Item {
   int b, pos0, q0, q_len, k0, k_len, ctx, h0, hkv, dv0;
   bool valid;
@@ -147,19 +166,20 @@ __device__ __forceinline__ Item item_geometry(int item, const PrefillParams& p) 
   it.k0 = __ldg(p.m.cu_k + it.b);
   it.k_len = __ldg(p.m.cu_k + it.b + 1) - it.k0;
   it.ctx = p.m.ctx_lens ? __ldg(p.m.ctx_lens + it.b) : (it.k_len - it.q_len);
-  it.pos0 = (p.n_qtiles - 1 - x) * (kBM / p.gpack);
+  it.pos0 = (p.n_qtiles - 1 - x) * (C::ITEM_ROWS / p.gpack);
   it.valid = it.pos0 < it.q_len && !(p.skip_decode && it.q_len == 1);
   return it;
 }
 
-// Key-tile plan of an item (warp-collective): the tiles between the smallest
+// Key-tile plan of an item (warp-collective, over all NCTA * 128 rows, so
+// both CTAs of a pair walk the same tiles): the tiles between the smallest
 // and largest visible key of any row, and the tiles inside every row's
 // all-visible interval (no mask needed there).
 template <class C>
 __device__ __forceinline__ Plan plan_tiles(const Item& it, const PrefillParams& p, bool use_table, int lane) {
   int hl_min = INT_MAX, hh_max = INT_MIN, cl_max = INT_MIN, ch_min = INT_MAX;
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
+  for (int k = 0; k < 4 * C::NCTA; ++k) {
     const int row = lane + 32 * k;
     const int qi = it.pos0 + row / p.gpack;
     if (qi < it.q_len) {
@@ -223,6 +243,13 @@ __device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t* r) {
                : "memory");
 }
 
+// With NCTA == 2, TMA copies of both CTAs complete on rank 0's barrier.
+template <class C>
+__device__ __forceinline__ void tma_load(void* dst, const CUtensorMap* map, uint64_t* full, int x, int y, int z) {
+  if constexpr (C::NCTA == 2) tma_load_3d_pair(dst, map, mapa_shared(smem_u32(full), 0), x, y, z);
+  else tma_load_3d(dst, map, full, x, y, z);
+}
+
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1)
     attn_prefill_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
@@ -236,12 +263,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   const bool use_table = table_active(p.m);
   const int n_items = p.n_qtiles * (p.num_reqs - p.req_offset) * p.hkv * p.n_hgroups * C::DV_SPLIT;
   constexpr int BN = C::BN;
+  const int rank = C::NCTA == 2 ? static_cast<int>(cluster_rank()) : 0;
+  const bool leader = rank == 0;  // issues the MMAs and owns the "full" barriers
 
   // ---------------------------------------------------------------- setup
   if (threadIdx.x == 0) {
     for (int i = 0; i < kPlanRing; ++i) {
       mbar_init(&sb.plan_full[i], 1);
-      mbar_init(&sb.plan_empty[i], C::CONSUMER_WARPS);
+      mbar_init(&sb.plan_empty[i], C::CONSUMER_WARPS - (leader ? 0 : 1));  // a pair's rank 1 issues no MMAs
     }
     mbar_init(&sb.q_full, 1);
     mbar_init(&sb.q_empty, 1);
@@ -253,7 +282,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sb.s_full[i], 1);
-      mbar_init(&sb.p_full[i], 128 * C::SPLIT);
+      mbar_init(&sb.p_full[i], 4 * C::SPLIT * C::NCTA);  // one arrival per softmax warp
       mbar_init(&sb.o_done[i], 1);
     }
     mbar_init(&sb.final_mma, 1);
@@ -265,11 +294,17 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     mbar_fence_init();
   }
   if (warp == 1) {
-    tmem_alloc(&sb.tmem_base, C::TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (C::NCTA == 2) {
+      tmem_alloc_pair(&sb.tmem_base, C::TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(&sb.tmem_base, C::TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (C::NCTA == 2) cluster_sync_all();  // the peer's barriers are initialised
   tc_fence_after();
   const uint32_t tmem = sb.tmem_base;
 
@@ -303,40 +338,90 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (e.pl.n_tiles > 0) return true;
       }
     };
+    const int pos_off = rank * (kBM / p.gpack);  // this CTA's first position within an item
+    // L2 warming: Q tiles and first K / V tiles come from DRAM the first time
+    // they are read, with a latency several times a tile's MMA time.  The
+    // next item's Q and first kPrefetchAhead K / V tiles are prefetched while
+    // the current item runs, and every load prefetches the tile kPrefetchAhead
+    // steps further.  Each CTA of a pair warms its own half.
+    constexpr int kPrefetchAhead = 2;
+    auto prefetch_k = [&](const PlanEntry& e, int j) {
+      const int krow = e.it.k0 + (e.pl.kb_lo + j) * BN + rank * C::KROWS;
+#pragma unroll
+      for (int c = 0; c < C::QCH; ++c) tma_prefetch_l2_3d(&map_k, c * 64, e.it.hkv, krow);
+    };
+    auto prefetch_v = [&](const PlanEntry& e, int j) {
+      const int krow = e.it.k0 + (e.pl.kb_lo + j) * BN;
+#pragma unroll
+      for (int c = 0; c < C::VCH; ++c) tma_prefetch_l2_3d(&map_v, e.it.dv0 + rank * C::DVC + c * 64, e.it.hkv, krow);
+    };
+    // Plan n (the next one to consume) if the scheduler has published it;
+    // never waits.  The slot cannot be reused before this warp consumes it.
+    auto prefetch_next_item = [&]() {
+      const int slot = n % kPlanRing;
+      if (!mbar_try_wait(&sb.plan_full[slot], (n / kPlanRing) & 1)) return;
+      const PlanEntry e = sb.plans[slot];
+      if (e.last || e.pl.n_tiles == 0) return;
+#pragma unroll
+      for (int c = 0; c < C::QCH; ++c) tma_prefetch_l2_3d(&map_q, c * 64, e.it.h0, e.it.q0 + e.it.pos0 + pos_off);
+      for (int j = 0; j < kPrefetchAhead && j < e.pl.n_tiles; ++j) {
+        prefetch_k(e, j);
+        prefetch_v(e, j);
+      }
+    };
     auto load_q = [&](const PlanEntry& e) -> bool {
-      if (qn > 0 && !mbar_wait(&sb.q_empty, (qn - 1) & 1, &sb.abort_flag, p.err, kDevTimeoutMma)) return false;
-      mbar_arrive_expect_tx(&sb.q_full, C::Q_BYTES);
+      if (qn > 0) {
+        bool free;
+        if constexpr (C::MERGED_RELEASE) {
+          const int tl = kc - 1;  // the previous item's last tile
+          free = mbar_wait(&sb.s_full[tl & 1], (tl >> 1) & 1, &sb.abort_flag, p.err, kDevTimeoutMma);
+        } else {
+          free = mbar_wait(&sb.q_empty, (qn - 1) & 1, &sb.abort_flag, p.err, kDevTimeoutMma);
+        }
+        if (!free) return false;
+      }
+      if (leader) mbar_arrive_expect_tx(&sb.q_full, C::NCTA * C::Q_BYTES);
 #pragma unroll
       for (int c = 0; c < C::QCH; ++c)
-        tma_load_3d(sQ + c * (kBM * 128), &map_q, &sb.q_full, c * 64, e.it.h0, e.it.q0 + e.it.pos0);
+        tma_load<C>(sQ + c * (kBM * 128), &map_q, &sb.q_full, c * 64, e.it.h0, e.it.q0 + e.it.pos0 + pos_off);
       ++qn;
       return true;
     };
     auto load_k = [&](const PlanEntry& e, int j) -> bool {
       const int s = kc % C::KST;
-      if (kc >= C::KST &&
-          !mbar_wait(&sb.k_empty[s], ((kc / C::KST) - 1) & 1, &sb.abort_flag, p.err, kDevTimeoutLoad))
-        return false;
-      mbar_arrive_expect_tx(&sb.k_full[s], C::K_BYTES);
-      const int krow = e.it.k0 + (e.pl.kb_lo + j) * BN;
+      if (kc >= C::KST) {
+        const int tp = kc - C::KST;  // the tile that used this stage before
+        const bool free = C::MERGED_RELEASE
+                              ? mbar_wait(&sb.s_full[tp & 1], (tp >> 1) & 1, &sb.abort_flag, p.err, kDevTimeoutLoad)
+                              : mbar_wait(&sb.k_empty[s], (tp / C::KST) & 1, &sb.abort_flag, p.err, kDevTimeoutLoad);
+        if (!free) return false;
+      }
+      if (leader) mbar_arrive_expect_tx(&sb.k_full[s], C::NCTA * C::K_BYTES);
+      const int krow = e.it.k0 + (e.pl.kb_lo + j) * BN + rank * C::KROWS;
 #pragma unroll
       for (int c = 0; c < C::QCH; ++c)
-        tma_load_3d(sK + s * C::K_BYTES + c * (BN * 128), &map_k, &sb.k_full[s], c * 64, e.it.hkv, krow);
+        tma_load<C>(sK + s * C::K_BYTES + c * (C::KROWS * 128), &map_k, &sb.k_full[s], c * 64, e.it.hkv, krow);
+      if (j + kPrefetchAhead < e.pl.n_tiles) prefetch_k(e, j + kPrefetchAhead);
       ++k_armed[s];
       ++kc;
       return true;
     };
     auto load_v = [&](const PlanEntry& e, int j) -> bool {
       const int s = vc % C::VST;
-      if (vc >= C::VST &&
-          !mbar_wait(&sb.v_empty[s], ((vc / C::VST) - 1) & 1, &sb.abort_flag, p.err, kDevTimeoutLoad))
-        return false;
-      mbar_arrive_expect_tx(&sb.v_full[s], C::V_BYTES);
+      if (vc >= C::VST) {
+        const int tp = vc - C::VST;
+        const bool free = C::MERGED_RELEASE
+                              ? mbar_wait(&sb.o_done[tp & 1], (tp >> 1) & 1, &sb.abort_flag, p.err, kDevTimeoutLoad)
+                              : mbar_wait(&sb.v_empty[s], (tp / C::VST) & 1, &sb.abort_flag, p.err, kDevTimeoutLoad);
+        if (!free) return false;
+      }
+      if (leader) mbar_arrive_expect_tx(&sb.v_full[s], C::NCTA * C::V_BYTES);
       const int krow = e.it.k0 + (e.pl.kb_lo + j) * BN;
 #pragma unroll
       for (int c = 0; c < C::VCH; ++c)
-        tma_load_3d(sV + s * C::V_BYTES + c * (BN * 128), &map_v, &sb.v_full[s], e.it.dv0 + c * 64, e.it.hkv,
-                    krow);
+        tma_load<C>(sV + s * C::V_BYTES + c * (BN * 128), &map_v, &sb.v_full[s], e.it.dv0 + rank * C::DVC + c * 64,
+                    e.it.hkv, krow);
+      if (j + kPrefetchAhead < e.pl.n_tiles) prefetch_v(e, j + kPrefetchAhead);
       ++v_armed[s];
       ++vc;
       return true;
@@ -347,6 +432,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     ok = __shfl_sync(kFullMask, ok, 0);
     while (ok && have) {
       const int nt = cur.pl.n_tiles;
+      if (lane == 0) prefetch_next_item();
       if (lane == 0)
         for (int j = 0; ok && j + 1 < nt; ++j) {
           ok = load_k(cur, j + 1);
@@ -366,7 +452,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     // Drain: never leave the CTA with a TMA write still in flight.  Each
     // full barrier's last armed phase is waited for, ignoring the CTA abort
     // flag (issued copies always complete, and must before the CTA exits).
-    if (lane == 0) {
+    // A pair's full barriers live in rank 0 and count both CTAs' copies;
+    // rank 1 stays until rank 0 has drained (the final cluster barrier).
+    if (lane == 0 && !leader && !ok) sb.abort_flag = 1;
+    if (lane == 0 && leader) {
       if (!ok) sb.abort_flag = 1;
       volatile int own_flag = 0;
       if (qn > 0) mbar_wait(&sb.q_full, (qn - 1) & 1, &own_flag, nullptr, 0);
@@ -375,13 +464,16 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (v_armed[i] > 0) mbar_wait(&sb.v_full[i], (v_armed[i] - 1) & 1, &own_flag, nullptr, 0);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 && leader) {
     // ------------------------------------------------------------ MMA issuer
-    // One thread issues every tcgen05.mma; descriptors are computed once and
-    // each MMA only adds a compile-time offset.  Tile t is the CTA-wide tile
-    // index: S buffer t & 1, K stage t % KST, V stage t % VST.
-    constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, C::BN, false, false);
-    constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, C::DV, false, true);
+    // The whole warp runs this loop (converged, warp-uniform values); each
+    // tcgen05.mma and commit is issued by one elected lane.  Descriptors are
+    // computed once and each MMA only adds a compile-time offset.  Tile t is
+    // the CTA-wide tile index: S buffer t & 1, K stage t % KST, V stage
+    // t % VST.  In a pair, the same descriptors and TMEM addresses name the
+    // operands in both CTAs.
+    constexpr uint32_t idesc_qk = idesc_bf16_f32(C::ITEM_ROWS, C::BN, false, false);
+    constexpr uint32_t idesc_pv = idesc_bf16_f32(C::ITEM_ROWS, C::DV, false, true);
     const uint64_t dq = smem_desc_sw128(smem_u32(sQ), 16, 1024);
     const uint64_t dk0 = smem_desc_sw128(smem_u32(sK), 16, 1024);
     const uint64_t dv0 = smem_desc_sw128(smem_u32(sV), BN * 128, 1024);
@@ -393,67 +485,67 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       if (!ok || e.last) break;
       const Plan& pl = e.pl;
       if (pl.n_tiles == 0) continue;
-      if (lane == 0) {
-        ok = mbar_wait(&sb.q_full, qn & 1, &sb.abort_flag, p.err, kDevTimeoutLoad);
-        ++qn;
-        for (int j = 0; ok && j <= pl.n_tiles; ++j) {
-          if (j < pl.n_tiles) {
-            const int t = T + j;
-            const int s = t % C::KST;
-            if (!mbar_wait(&sb.k_full[s], (t / C::KST) & 1, &sb.abort_flag, p.err, kDevTimeoutLoad)) {
-              ok = false;
-              break;
-            }
-            const uint32_t d = tmem + C::S_COL + (t & 1) * BN;
-            const uint64_t dk = dk0 + static_cast<uint64_t>((s * C::K_BYTES) >> 4);
-#pragma unroll
-            for (int c = 0; c < C::QCH; ++c) {
-#pragma unroll
-              for (int k16 = 0; k16 < 4; ++k16) {
-                const uint64_t a = dq + static_cast<uint64_t>((c * (kBM * 128) + k16 * 32) >> 4);
-                const uint64_t b = dk + static_cast<uint64_t>((c * (BN * 128) + k16 * 32) >> 4);
-                mma_bf16_ss(d, a, b, idesc_qk, (c | k16) != 0 ? 1u : 0u);
-              }
-            }
-            mma_commit(&sb.k_empty[s]);
-            if (j == pl.n_tiles - 1) mma_commit(&sb.q_empty);  // Q free for the next item
-            mma_commit(&sb.s_full[t & 1]);
+      ok = mbar_wait_spin(&sb.q_full, qn & 1, &sb.abort_flag, p.err, kDevTimeoutLoad);
+      ++qn;
+      for (int j = 0; ok && j <= pl.n_tiles; ++j) {
+        if (j < pl.n_tiles) {
+          const int t = T + j;
+          const int s = t % C::KST;
+          if (!mbar_wait_spin(&sb.k_full[s], (t / C::KST) & 1, &sb.abort_flag, p.err, kDevTimeoutLoad)) {
+            ok = false;
+            break;
           }
-          if (j >= 1) {
-            const int t = T + j - 1;
-            if (!mbar_wait(&sb.p_full[t & 1], (t >> 1) & 1, &sb.abort_flag, p.err, kDevTimeoutSoftmax)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();  // P was written to TMEM by the softmax threads
-            const int s = t % C::VST;
-            if (!mbar_wait(&sb.v_full[s], (t / C::VST) & 1, &sb.abort_flag, p.err, kDevTimeoutLoad)) {
-              ok = false;
-              break;
-            }
-            const uint32_t pcol = tmem + C::S_COL + (t & 1) * BN;
-            const uint64_t dv = dv0 + static_cast<uint64_t>((s * C::V_BYTES) >> 4);
-            const uint32_t first = (j > 1) ? 1u : 0u;  // the item's first PV overwrites O
+          const uint32_t d = tmem + C::S_COL + (t & 1) * BN;
+          const uint64_t dk = dk0 + static_cast<uint64_t>((s * C::K_BYTES) >> 4);
 #pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk) {
-              const uint64_t b = dv + static_cast<uint64_t>((kk * 16 * 128) >> 4);
-              mma_bf16_ts(tmem + C::O_COL, pcol + kk * 8, b, idesc_pv, kk == 0 ? first : 1u);
+          for (int c = 0; c < C::QCH; ++c) {
+#pragma unroll
+            for (int k16 = 0; k16 < 4; ++k16) {
+              const uint64_t a = dq + static_cast<uint64_t>((c * (kBM * 128) + k16 * 32) >> 4);
+              const uint64_t b = dk + static_cast<uint64_t>((c * (C::KROWS * 128) + k16 * 32) >> 4);
+              mma_ss_elect<C::NCTA>(d, a, b, idesc_qk, (c | k16) != 0 ? 1u : 0u);
             }
-            mma_commit(&sb.v_empty[s]);
-            mma_commit(&sb.o_done[t & 1]);
           }
+          if constexpr (!C::MERGED_RELEASE) {
+            mma_commit_elect<C::NCTA>(&sb.k_empty[s]);
+            if (j == pl.n_tiles - 1) mma_commit_elect<C::NCTA>(&sb.q_empty);  // Q free for the next item
+          }
+          mma_commit_elect<C::NCTA>(&sb.s_full[t & 1]);
         }
-        T += pl.n_tiles;
+        if (j >= 1) {
+          const int t = T + j - 1;
+          if (!mbar_wait_spin(&sb.p_full[t & 1], (t >> 1) & 1, &sb.abort_flag, p.err, kDevTimeoutSoftmax)) {
+            ok = false;
+            break;
+          }
+          const int s = t % C::VST;
+          if (!mbar_wait_spin(&sb.v_full[s], (t / C::VST) & 1, &sb.abort_flag, p.err, kDevTimeoutLoad)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();  // P was written to TMEM by the softmax threads
+          const uint32_t pcol = tmem + C::S_COL + (t & 1) * BN;
+          const uint64_t dv = dv0 + static_cast<uint64_t>((s * C::V_BYTES) >> 4);
+          const uint32_t first = (j > 1) ? 1u : 0u;  // the item's first PV overwrites O
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            const uint64_t b = dv + static_cast<uint64_t>((kk * 16 * 128) >> 4);
+            mma_ts_elect<C::NCTA>(tmem + C::O_COL, pcol + kk * 8, b, idesc_pv, kk == 0 ? first : 1u);
+          }
+          if constexpr (!C::MERGED_RELEASE) mma_commit_elect<C::NCTA>(&sb.v_empty[s]);
+          mma_commit_elect<C::NCTA>(&sb.o_done[t & 1]);
+        }
       }
-      ok = __shfl_sync(kFullMask, ok, 0);
+      T += pl.n_tiles;
     }
-    if (lane == 0) {
-      if (!ok) sb.abort_flag = 1;
-      // All issued MMAs must finish before TMEM is released.
-      mma_commit(&sb.final_mma);
-      volatile int own_flag = 0;
-      mbar_wait(&sb.final_mma, 0, &own_flag, p.err, kDevTimeoutMma);
-    }
+    if (!ok && lane == 0) sb.abort_flag = 1;
+    // All issued MMAs must finish before TMEM is released (and, in a pair,
+    // before the peer's shared memory and TMEM go away).
+    mma_commit_elect<C::NCTA>(&sb.final_mma);
+    volatile int own_flag = 0;
+    mbar_wait(&sb.final_mma, 0, &own_flag, p.err, kDevTimeoutMma);
+  } else if (warp == 1) {
+    // A pair's rank 1: its TMEM is allocated by this warp; rank 0 issues the MMAs.
   } else if (warp < C::SCHED_WARP) {
     // ------------------------------------------------------------ softmax rows
     constexpr int HC = C::HC;
@@ -477,10 +569,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       RowVis vis;
       float sink;
     };
+    const int pos_off = rank * (kBM / p.gpack);  // this CTA's first position within an item
+    // p_full lives in rank 0: one arrival per warp (released at cluster scope in a pair)
+    const uint32_t p_full_addr0 = C::NCTA == 2 ? mapa_shared(smem_u32(&sb.p_full[0]), 0) : 0u;
     auto row_ctx = [&](const PlanEntry& e) {
       RowCtx r;
       r.head = e.it.h0 + (row % p.gpack);
-      r.qi = e.it.pos0 + row / p.gpack;
+      r.qi = e.it.pos0 + pos_off + row / p.gpack;
       r.valid = !e.last && r.qi < e.it.q_len;
       r.vis = r.valid ? row_visibility(p.m, e.it.ctx + r.qi, e.it.k_len, use_table ? (e.it.q0 + r.qi) : -1)
                       : empty_row();
@@ -617,7 +712,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&sb.p_full[t & 1]);
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (C::NCTA == 2) mbar_arrive_cluster(p_full_addr0 + (t & 1) * 8);
+          else mbar_arrive(&sb.p_full[t & 1]);
+        }
         if (!ok) break;
       }
 
@@ -721,7 +820,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       ++n;
       return good;
     };
-    for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+    const int n_groups = gridDim.x / C::NCTA;  // clusters (single CTAs when NCTA == 1)
+    for (int item = blockIdx.x / C::NCTA; ok && item < n_items; item += n_groups) {
       PlanEntry e;
       e.it = item_geometry<C>(item, p);
       if (!e.it.valid) continue;
@@ -738,14 +838,18 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (C::NCTA == 2) cluster_sync_all();  // rank 0's MMAs and drain are complete
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+  if (warp == 1) {
+    if constexpr (C::NCTA == 2) tmem_dealloc_pair(tmem, C::TMEM_COLS);
+    else tmem_dealloc(tmem, C::TMEM_COLS);
+  }
 }
 
-using Cfg64 = Cfg<64, 64, 128, 4, 4>;
-using Cfg128 = Cfg<128, 128, 128, 2, 2>;
-using Cfg256 = Cfg<256, 256, 128, 1, 1>;
-using Cfg512 = Cfg<512, 256, 64, 1, 1>;
+using Cfg64 = Cfg<64, 64, 128, 4, 4, 1>;
+using Cfg128 = Cfg<128, 128, 128, 4, 4, 2>;
+using Cfg256 = Cfg<256, 256, 128, 2, 2, 2>;
+using Cfg512 = Cfg<512, 256, 64, 1, 1, 1>;
 
 template <class C>
 cudaError_t launch_cfg(const PrefillParams& p, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
@@ -757,8 +861,39 @@ cudaError_t launch_cfg(const PrefillParams& p, const CUtensorMap& mq, const CUte
       static_cast<long long>(p.n_qtiles) * (p.num_reqs - p.req_offset) * p.hkv * p.n_hgroups * C::DV_SPLIT;
   if (n_items <= 0) return cudaSuccess;
   if (n_items > INT_MAX) return cudaErrorInvalidValue;
-  const int grid = static_cast<int>(n_items < p.n_ctas ? n_items : p.n_ctas);
-  kern<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(mq, mk, mv, p);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C::NCTA;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // Persistent groups: as many CTAs (pairs) as can be resident at once (the
+  // pair count is queried once per device; clusters must fit within a GPC).
+  int groups = p.n_ctas / C::NCTA;
+  if constexpr (C::NCTA > 1) {
+    static int active_pairs[64] = {};
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (active_pairs[dev] == 0) {
+      cfg.gridDim = dim3(groups * C::NCTA);
+      int active = 0;
+      e = cudaOccupancyMaxActiveClusters(&active, kern, &cfg);
+      if (e != cudaSuccess) return e;
+      active_pairs[dev] = active > 0 ? active : groups;
+    }
+    if (active_pairs[dev] < groups) groups = active_pairs[dev];
+  }
+  if (n_items < groups) groups = static_cast<int>(n_items);
+  cfg.gridDim = dim3(groups * C::NCTA);
+  e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -766,11 +901,11 @@ cudaError_t launch_cfg(const PrefillParams& p, const CUtensorMap& mq, const CUte
 
 PrefillShape prefill_tile_shape(int head_dim) {
   switch (head_dim) {
-    case 64: return {Cfg64::BN, Cfg64::DV, Cfg64::DV_SPLIT, Cfg64::BN};
-    case 128: return {Cfg128::BN, Cfg128::DV, Cfg128::DV_SPLIT, Cfg128::BN};
-    case 256: return {Cfg256::BN, Cfg256::DV, Cfg256::DV_SPLIT, Cfg256::BN};
-    case 512: return {Cfg512::BN, Cfg512::DV, Cfg512::DV_SPLIT, Cfg512::BN};
-    default: return {0, 0, 0, 0};
+    case 64: return {Cfg64::BN, Cfg64::DV, Cfg64::DV_SPLIT, Cfg64::BN, Cfg64::KROWS, Cfg64::NCTA};
+    case 128: return {Cfg128::BN, Cfg128::DV, Cfg128::DV_SPLIT, Cfg128::BN, Cfg128::KROWS, Cfg128::NCTA};
+    case 256: return {Cfg256::BN, Cfg256::DV, Cfg256::DV_SPLIT, Cfg256::BN, Cfg256::KROWS, Cfg256::NCTA};
+    case 512: return {Cfg512::BN, Cfg512::DV, Cfg512::DV_SPLIT, Cfg512::BN, Cfg512::KROWS, Cfg512::NCTA};
+    default: return {0, 0, 0, 0, 0, 0};
   }
 }
 

@@ -51,7 +51,7 @@ struct PrefillParams {
   int hkv;
   int gpack;          // q heads packed into one 128-row tile (power of two)
   int n_hgroups;      // (hq / hkv) / gpack
-  int n_qtiles;       // ceil(max_q_len / (128 / gpack))
+  int n_qtiles;       // items per (request, head group): ceil(max_q_len / (ncta * 128 / gpack))
   int skip_decode;    // requests with q_len == 1 are left to the decode kernel
   int req_offset;     // first request covered (items walk [req_offset, num_reqs))
   int n_ctas;         // persistent CTAs to launch (SM count)
@@ -64,6 +64,8 @@ struct PrefillShape {
   int dv_cta;    // value columns per CTA
   int dv_split;  // CTAs per (q tile, head group) along the value dimension
   int v_box_keys;  // keys per V TMA box
+  int k_box_keys;  // keys per K TMA box (a CTA pair's CTA loads half a tile)
+  int ncta;        // CTAs sharing each MMA: 1, or 2 (a cluster pair)
 };
 PrefillShape prefill_tile_shape(int head_dim);
 
