@@ -73,10 +73,27 @@ struct Cfg {
   static constexpr int DV_SPLIT = D / DV;
   static constexpr int SPLIT = BN / 64;         // softmax warpgroups (column halves of a row)
   static constexpr int HC = BN / SPLIT;         // score columns per softmax thread (64)
-  static constexpr int HDV = DV / SPLIT;        // O columns per softmax thread
-  static constexpr int CONSUMER_WARPS = 2 + 4 * SPLIT;  // producer, MMA, softmax warps
-  static constexpr int SCHED_WARP = CONSUMER_WARPS;      // computes item plans ahead
-  static constexpr int THREADS = 32 * (CONSUMER_WARPS + 1);
+  static constexpr int HDV = DV / SPLIT;        // O columns per softmax thread (rescale)
+  // Warp layout: warpgroup 0 = TMA producer (warp 0), MMA issuer (1), plan
+  // scheduler (2), one idle warp; SPLIT softmax warpgroups; one epilogue
+  // warpgroup that reads O out of TMEM and stores the output rows.
+  static constexpr int PRODUCER_WARP = 0;
+  static constexpr int MMA_WARP = 1;
+  static constexpr int SCHED_WARP = 2;
+  static constexpr int SOFTMAX_BEGIN = 4;
+  static constexpr int SOFTMAX_END = SOFTMAX_BEGIN + 4 * SPLIT;
+  static constexpr int EPI_BEGIN = SOFTMAX_END;
+  static constexpr int WARPS = EPI_BEGIN + 4;
+  static constexpr int THREADS = 32 * WARPS;
+  static constexpr int CONSUMER_WARPS = 2 + 4 * SPLIT + 4;  // warps that read the plan ring
+  // Register split for 512 threads (128 each at launch): the softmax warps
+  // get 168, the epilogue and warpgroup 0 88 each (sum 4 x 128).
+  static constexpr bool REG_SPLIT = SPLIT == 2;
+  static constexpr int REGS_CTRL = 88;
+  static constexpr int REGS_SOFTMAX = 168;
+  static constexpr int REGS_EPI = 88;
+  static_assert(!REG_SPLIT || (THREADS == 512 && REGS_CTRL + 2 * REGS_SOFTMAX + REGS_EPI <= 4 * 128),
+                "register split");
   static constexpr int Q_BYTES = kBM * D * 2;
   static constexpr int K_BYTES = KROWS * D * 2;  // per CTA
   static constexpr int V_BYTES = BN * DVC * 2;    // per CTA
@@ -86,7 +103,11 @@ struct Cfg {
   static constexpr int TILE_BYTES = V_OFF + VST * V_BYTES;
   static constexpr int RED_OFF = TILE_BYTES;  // pair exchange slots: [2 parity][SPLIT][128] float2
   static constexpr int RED_BYTES = SPLIT > 1 ? 2 * SPLIT * kBM * 8 : 0;
-  static constexpr int SMEM_BYTES = RED_OFF + RED_BYTES + 1024;  // + alignment slack
+  // Hand-off slots softmax -> epilogue: (1 / l, LSE) per row and item.  Two
+  // when they fit (the D = 512 tiles leave room for one).
+  static constexpr int ROW_OFF = RED_OFF + RED_BYTES;
+  static constexpr int EPI_SLOTS = (ROW_OFF + 2 * kBM * 8 + 1024 + 1024 <= 227 * 1024) ? 2 : 1;
+  static constexpr int SMEM_BYTES = ROW_OFF + EPI_SLOTS * kBM * 8 + 1024;  // + alignment slack
   static constexpr int S_COL = 0;
   static constexpr int O_COL = 2 * BN;
   static constexpr int TMEM_COLS = 512;
@@ -140,6 +161,9 @@ struct __align__(8) Barriers {
   uint64_t p_full[2];
   uint64_t o_done[2];
   uint64_t final_mma;
+  uint64_t epi_full[2];   // an item's (1 / l, LSE) rows are written (half-0 softmax warps)
+  uint64_t epi_empty[2];  // ... and read (epilogue warps)
+  uint64_t o_free;        // O of the previous item is out of TMEM (rank 0; arrivals from both CTAs)
   uint64_t xchg[4][2];  // softmax column-half pairs (per TMEM lane quarter), by parity
   uint32_t tmem_base;
   int abort_flag;
@@ -286,6 +310,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       mbar_init(&sb.o_done[i], 1);
     }
     mbar_init(&sb.final_mma, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sb.epi_full[i], 4);
+      mbar_init(&sb.epi_empty[i], 4);
+    }
+    mbar_init(&sb.o_free, 4 * C::NCTA);
     for (int i = 0; i < 4; ++i) {
       mbar_init(&sb.xchg[i][0], 64);
       mbar_init(&sb.xchg[i][1], 64);
@@ -312,245 +341,291 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   uint8_t* sK = smem + C::K_OFF;
   uint8_t* sV = smem + C::V_OFF;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    // Loads follow the order in which the MMA issuer frees the buffers: per
-    // item Q and K_0, then per step j K_{j+1} and V_j.  The next item's Q and
-    // K_0 go out before the current item's last V tile: they wait only for
-    // the last QK, which the tensor core finishes before the PV that frees
-    // that V stage.  Stage counters run across items.
-    if (lane == 0) {
-      tma_prefetch_desc(&map_q);
-      tma_prefetch_desc(&map_k);
-      tma_prefetch_desc(&map_v);
-    }
-    bool ok = true;
-    int n = 0, qn = 0, kc = 0, vc = 0;  // plans taken, Q / K / V tiles issued
-    int k_armed[4] = {0, 0, 0, 0}, v_armed[4] = {0, 0, 0, 0};
-    // Next item that has key tiles (warp-collective); false at the end.
-    auto next_item = [&](PlanEntry& e) -> bool {
-      for (;;) {
-        if (!consume_plan(sb, n++, lane, e, p.err)) {
-          ok = false;
-          return false;
-        }
-        if (e.last) return false;
-        if (e.pl.n_tiles > 0) return true;
+
+  if (warp < C::SOFTMAX_BEGIN) {
+    if constexpr (C::REG_SPLIT) regs_decrease<C::REGS_CTRL>();
+    if (warp == 0) {
+      // ------------------------------------------------------------ producer
+      // Loads follow the order in which the MMA issuer frees the buffers: per
+      // item Q and K_0, then per step j K_{j+1} and V_j.  The next item's Q and
+      // K_0 go out before the current item's last V tile: they wait only for
+      // the last QK, which the tensor core finishes before the PV that frees
+      // that V stage.  Stage counters run across items.
+      if (lane == 0) {
+        tma_prefetch_desc(&map_q);
+        tma_prefetch_desc(&map_k);
+        tma_prefetch_desc(&map_v);
       }
-    };
-    const int pos_off = rank * (kBM / p.gpack);  // this CTA's first position within an item
-    // L2 warming: Q tiles and first K / V tiles come from DRAM the first time
-    // they are read, with a latency several times a tile's MMA time.  The
-    // next item's Q and first kPrefetchAhead K / V tiles are prefetched while
-    // the current item runs, and every load prefetches the tile kPrefetchAhead
-    // steps further.  Each CTA of a pair warms its own half.
-    constexpr int kPrefetchAhead = 2;
-    auto prefetch_k = [&](const PlanEntry& e, int j) {
-      const int krow = e.it.k0 + (e.pl.kb_lo + j) * BN + rank * C::KROWS;
-#pragma unroll
-      for (int c = 0; c < C::QCH; ++c) tma_prefetch_l2_3d(&map_k, c * 64, e.it.hkv, krow);
-    };
-    auto prefetch_v = [&](const PlanEntry& e, int j) {
-      const int krow = e.it.k0 + (e.pl.kb_lo + j) * BN;
-#pragma unroll
-      for (int c = 0; c < C::VCH; ++c) tma_prefetch_l2_3d(&map_v, e.it.dv0 + rank * C::DVC + c * 64, e.it.hkv, krow);
-    };
-    // Plan n (the next one to consume) if the scheduler has published it;
-    // never waits.  The slot cannot be reused before this warp consumes it.
-    auto prefetch_next_item = [&]() {
-      const int slot = n % kPlanRing;
-      if (!mbar_try_wait(&sb.plan_full[slot], (n / kPlanRing) & 1)) return;
-      const PlanEntry e = sb.plans[slot];
-      if (e.last || e.pl.n_tiles == 0) return;
-#pragma unroll
-      for (int c = 0; c < C::QCH; ++c) tma_prefetch_l2_3d(&map_q, c * 64, e.it.h0, e.it.q0 + e.it.pos0 + pos_off);
-      for (int j = 0; j < kPrefetchAhead && j < e.pl.n_tiles; ++j) {
-        prefetch_k(e, j);
-        prefetch_v(e, j);
-      }
-    };
-    auto load_q = [&](const PlanEntry& e) -> bool {
-      if (qn > 0) {
-        bool free;
-        if constexpr (C::MERGED_RELEASE) {
-          const int tl = kc - 1;  // the previous item's last tile
-          free = mbar_wait(&sb.s_full[tl & 1], (tl >> 1) & 1, &sb.abort_flag, p.err, kDevTimeoutMma);
-        } else {
-          free = mbar_wait(&sb.q_empty, (qn - 1) & 1, &sb.abort_flag, p.err, kDevTimeoutMma);
-        }
-        if (!free) return false;
-      }
-      if (leader) mbar_arrive_expect_tx(&sb.q_full, C::NCTA * C::Q_BYTES);
-#pragma unroll
-      for (int c = 0; c < C::QCH; ++c)
-        tma_load<C>(sQ + c * (kBM * 128), &map_q, &sb.q_full, c * 64, e.it.h0, e.it.q0 + e.it.pos0 + pos_off);
-      ++qn;
-      return true;
-    };
-    auto load_k = [&](const PlanEntry& e, int j) -> bool {
-      const int s = kc % C::KST;
-      if (kc >= C::KST) {
-        const int tp = kc - C::KST;  // the tile that used this stage before
-        const bool free = C::MERGED_RELEASE
-                              ? mbar_wait(&sb.s_full[tp & 1], (tp >> 1) & 1, &sb.abort_flag, p.err, kDevTimeoutLoad)
-                              : mbar_wait(&sb.k_empty[s], (tp / C::KST) & 1, &sb.abort_flag, p.err, kDevTimeoutLoad);
-        if (!free) return false;
-      }
-      if (leader) mbar_arrive_expect_tx(&sb.k_full[s], C::NCTA * C::K_BYTES);
-      const int krow = e.it.k0 + (e.pl.kb_lo + j) * BN + rank * C::KROWS;
-#pragma unroll
-      for (int c = 0; c < C::QCH; ++c)
-        tma_load<C>(sK + s * C::K_BYTES + c * (C::KROWS * 128), &map_k, &sb.k_full[s], c * 64, e.it.hkv, krow);
-      if (j + kPrefetchAhead < e.pl.n_tiles) prefetch_k(e, j + kPrefetchAhead);
-      ++k_armed[s];
-      ++kc;
-      return true;
-    };
-    auto load_v = [&](const PlanEntry& e, int j) -> bool {
-      const int s = vc % C::VST;
-      if (vc >= C::VST) {
-        const int tp = vc - C::VST;
-        const bool free = C::MERGED_RELEASE
-                              ? mbar_wait(&sb.o_done[tp & 1], (tp >> 1) & 1, &sb.abort_flag, p.err, kDevTimeoutLoad)
-                              : mbar_wait(&sb.v_empty[s], (tp / C::VST) & 1, &sb.abort_flag, p.err, kDevTimeoutLoad);
-        if (!free) return false;
-      }
-      if (leader) mbar_arrive_expect_tx(&sb.v_full[s], C::NCTA * C::V_BYTES);
-      const int krow = e.it.k0 + (e.pl.kb_lo + j) * BN;
-#pragma unroll
-      for (int c = 0; c < C::VCH; ++c)
-        tma_load<C>(sV + s * C::V_BYTES + c * (BN * 128), &map_v, &sb.v_full[s], e.it.dv0 + rank * C::DVC + c * 64,
-                    e.it.hkv, krow);
-      if (j + kPrefetchAhead < e.pl.n_tiles) prefetch_v(e, j + kPrefetchAhead);
-      ++v_armed[s];
-      ++vc;
-      return true;
-    };
-    PlanEntry cur;
-    bool have = next_item(cur);
-    if (have && lane == 0) ok = load_q(cur) && load_k(cur, 0);
-    ok = __shfl_sync(kFullMask, ok, 0);
-    while (ok && have) {
-      const int nt = cur.pl.n_tiles;
-      if (lane == 0) prefetch_next_item();
-      if (lane == 0)
-        for (int j = 0; ok && j + 1 < nt; ++j) {
-          ok = load_k(cur, j + 1);
-          if (ok) ok = load_v(cur, j);
-        }
-      ok = __shfl_sync(kFullMask, ok, 0);
-      PlanEntry nxt;
-      const bool have_next = ok && next_item(nxt);
-      if (lane == 0 && ok) {
-        if (have_next) ok = load_q(nxt) && load_k(nxt, 0);
-        if (ok) ok = load_v(cur, nt - 1);
-      }
-      ok = __shfl_sync(kFullMask, ok, 0);
-      cur = nxt;
-      have = have_next;
-    }
-    // Drain: never leave the CTA with a TMA write still in flight.  Each
-    // full barrier's last armed phase is waited for, ignoring the CTA abort
-    // flag (issued copies always complete, and must before the CTA exits).
-    // A pair's full barriers live in rank 0 and count both CTAs' copies;
-    // rank 1 stays until rank 0 has drained (the final cluster barrier).
-    if (lane == 0 && !leader && !ok) sb.abort_flag = 1;
-    if (lane == 0 && leader) {
-      if (!ok) sb.abort_flag = 1;
-      volatile int own_flag = 0;
-      if (qn > 0) mbar_wait(&sb.q_full, (qn - 1) & 1, &own_flag, nullptr, 0);
-      for (int i = 0; i < 4; ++i) {
-        if (k_armed[i] > 0) mbar_wait(&sb.k_full[i], (k_armed[i] - 1) & 1, &own_flag, nullptr, 0);
-        if (v_armed[i] > 0) mbar_wait(&sb.v_full[i], (v_armed[i] - 1) & 1, &own_flag, nullptr, 0);
-      }
-    }
-  } else if (warp == 1 && leader) {
-    // ------------------------------------------------------------ MMA issuer
-    // The whole warp runs this loop (converged, warp-uniform values); each
-    // tcgen05.mma and commit is issued by one elected lane.  Descriptors are
-    // computed once and each MMA only adds a compile-time offset.  Tile t is
-    // the CTA-wide tile index: S buffer t & 1, K stage t % KST, V stage
-    // t % VST.  In a pair, the same descriptors and TMEM addresses name the
-    // operands in both CTAs.
-    constexpr uint32_t idesc_qk = idesc_bf16_f32(C::ITEM_ROWS, C::BN, false, false);
-    constexpr uint32_t idesc_pv = idesc_bf16_f32(C::ITEM_ROWS, C::DV, false, true);
-    const uint64_t dq = smem_desc_sw128(smem_u32(sQ), 16, 1024);
-    const uint64_t dk0 = smem_desc_sw128(smem_u32(sK), 16, 1024);
-    const uint64_t dv0 = smem_desc_sw128(smem_u32(sV), BN * 128, 1024);
-    bool ok = true;
-    int T = 0, qn = 0;
-    for (int n = 0; ok; ++n) {
-      PlanEntry e;
-      ok = consume_plan(sb, n, lane, e, p.err);
-      if (!ok || e.last) break;
-      const Plan& pl = e.pl;
-      if (pl.n_tiles == 0) continue;
-      ok = mbar_wait_spin(&sb.q_full, qn & 1, &sb.abort_flag, p.err, kDevTimeoutLoad);
-      ++qn;
-      for (int j = 0; ok && j <= pl.n_tiles; ++j) {
-        if (j < pl.n_tiles) {
-          const int t = T + j;
-          const int s = t % C::KST;
-          if (!mbar_wait_spin(&sb.k_full[s], (t / C::KST) & 1, &sb.abort_flag, p.err, kDevTimeoutLoad)) {
+      bool ok = true;
+      int n = 0, qn = 0, kc = 0, vc = 0;  // plans taken, Q / K / V tiles issued
+      int k_armed[4] = {0, 0, 0, 0}, v_armed[4] = {0, 0, 0, 0};
+      // Next item that has key tiles (warp-collective); false at the end.
+      auto next_item = [&](PlanEntry& e) -> bool {
+        for (;;) {
+          if (!consume_plan(sb, n++, lane, e, p.err)) {
             ok = false;
-            break;
+            return false;
           }
-          const uint32_t d = tmem + C::S_COL + (t & 1) * BN;
-          const uint64_t dk = dk0 + static_cast<uint64_t>((s * C::K_BYTES) >> 4);
-#pragma unroll
-          for (int c = 0; c < C::QCH; ++c) {
-#pragma unroll
-            for (int k16 = 0; k16 < 4; ++k16) {
-              const uint64_t a = dq + static_cast<uint64_t>((c * (kBM * 128) + k16 * 32) >> 4);
-              const uint64_t b = dk + static_cast<uint64_t>((c * (C::KROWS * 128) + k16 * 32) >> 4);
-              mma_ss_elect<C::NCTA>(d, a, b, idesc_qk, (c | k16) != 0 ? 1u : 0u);
+          if (e.last) return false;
+          if (e.pl.n_tiles > 0) return true;
+        }
+      };
+      const int pos_off = rank * (kBM / p.gpack);  // this CTA's first position within an item
+      // L2 warming: Q tiles and first K / V tiles come from DRAM the first time
+      // they are read, with a latency several times a tile's MMA time.  The
+      // next item's Q and first kPrefetchAhead K / V tiles are prefetched while
+      // the current item runs, and every load prefetches the tile kPrefetchAhead
+      // steps further.  Each CTA of a pair warms its own half.
+      constexpr int kPrefetchAhead = 2;
+      auto prefetch_k = [&](const PlanEntry& e, int j) {
+        const int krow = e.it.k0 + (e.pl.kb_lo + j) * BN + rank * C::KROWS;
+  #pragma unroll
+        for (int c = 0; c < C::QCH; ++c) tma_prefetch_l2_3d(&map_k, c * 64, e.it.hkv, krow);
+      };
+      auto prefetch_v = [&](const PlanEntry& e, int j) {
+        const int krow = e.it.k0 + (e.pl.kb_lo + j) * BN;
+  #pragma unroll
+        for (int c = 0; c < C::VCH; ++c) tma_prefetch_l2_3d(&map_v, e.it.dv0 + rank * C::DVC + c * 64, e.it.hkv, krow);
+      };
+      // Plan n (the next one to consume) if the scheduler has published it;
+      // never waits.  The slot cannot be reused before this warp consumes it.
+      auto prefetch_next_item = [&]() {
+        const int slot = n % kPlanRing;
+        if (!mbar_try_wait(&sb.plan_full[slot], (n / kPlanRing) & 1)) return;
+        const PlanEntry e = sb.plans[slot];
+        if (e.last || e.pl.n_tiles == 0) return;
+  #pragma unroll
+        for (int c = 0; c < C::QCH; ++c) tma_prefetch_l2_3d(&map_q, c * 64, e.it.h0, e.it.q0 + e.it.pos0 + pos_off);
+        for (int j = 0; j < kPrefetchAhead && j < e.pl.n_tiles; ++j) {
+          prefetch_k(e, j);
+          prefetch_v(e, j);
+        }
+      };
+      auto load_q = [&](const PlanEntry& e) -> bool {
+        if (qn > 0) {
+          bool free;
+          if constexpr (C::MERGED_RELEASE) {
+            const int tl = kc - 1;  // the previous item's last tile
+            free = mbar_wait(&sb.s_full[tl & 1], (tl >> 1) & 1, &sb.abort_flag, p.err, kDevTimeoutMma);
+          } else {
+            free = mbar_wait(&sb.q_empty, (qn - 1) & 1, &sb.abort_flag, p.err, kDevTimeoutMma);
+          }
+          if (!free) return false;
+        }
+        if (leader) mbar_arrive_expect_tx(&sb.q_full, C::NCTA * C::Q_BYTES);
+  #pragma unroll
+        for (int c = 0; c < C::QCH; ++c)
+          tma_load<C>(sQ + c * (kBM * 128), &map_q, &sb.q_full, c * 64, e.it.h0, e.it.q0 + e.it.pos0 + pos_off);
+        ++qn;
+        return true;
+      };
+      auto load_k = [&](const PlanEntry& e, int j) -> bool {
+        const int s = kc % C::KST;
+        if (kc >= C::KST) {
+          const int tp = kc - C::KST;  // the tile that used this stage before
+          const bool free = C::MERGED_RELEASE
+                                ? mbar_wait(&sb.s_full[tp & 1], (tp >> 1) & 1, &sb.abort_flag, p.err, kDevTimeoutLoad)
+                                : mbar_wait(&sb.k_empty[s], (tp / C::KST) & 1, &sb.abort_flag, p.err, kDevTimeoutLoad);
+          if (!free) return false;
+        }
+        if (leader) mbar_arrive_expect_tx(&sb.k_full[s], C::NCTA * C::K_BYTES);
+        const int krow = e.it.k0 + (e.pl.kb_lo + j) * BN + rank * C::KROWS;
+  #pragma unroll
+        for (int c = 0; c < C::QCH; ++c)
+          tma_load<C>(sK + s * C::K_BYTES + c * (C::KROWS * 128), &map_k, &sb.k_full[s], c * 64, e.it.hkv, krow);
+        if (j + kPrefetchAhead < e.pl.n_tiles) prefetch_k(e, j + kPrefetchAhead);
+        ++k_armed[s];
+        ++kc;
+        return true;
+      };
+      auto load_v = [&](const PlanEntry& e, int j) -> bool {
+        const int s = vc % C::VST;
+        if (vc >= C::VST) {
+          const int tp = vc - C::VST;
+          const bool free = C::MERGED_RELEASE
+                                ? mbar_wait(&sb.o_done[tp & 1], (tp >> 1) & 1, &sb.abort_flag, p.err, kDevTimeoutLoad)
+                                : mbar_wait(&sb.v_empty[s], (tp / C::VST) & 1, &sb.abort_flag, p.err, kDevTimeoutLoad);
+          if (!free) return false;
+        }
+        if (leader) mbar_arrive_expect_tx(&sb.v_full[s], C::NCTA * C::V_BYTES);
+        const int krow = e.it.k0 + (e.pl.kb_lo + j) * BN;
+  #pragma unroll
+        for (int c = 0; c < C::VCH; ++c)
+          tma_load<C>(sV + s * C::V_BYTES + c * (BN * 128), &map_v, &sb.v_full[s], e.it.dv0 + rank * C::DVC + c * 64,
+                      e.it.hkv, krow);
+        if (j + kPrefetchAhead < e.pl.n_tiles) prefetch_v(e, j + kPrefetchAhead);
+        ++v_armed[s];
+        ++vc;
+        return true;
+      };
+      PlanEntry cur;
+      bool have = next_item(cur);
+      if (have && lane == 0) ok = load_q(cur) && load_k(cur, 0);
+      ok = __shfl_sync(kFullMask, ok, 0);
+      while (ok && have) {
+        const int nt = cur.pl.n_tiles;
+        if (lane == 0) prefetch_next_item();
+        if (lane == 0)
+          for (int j = 0; ok && j + 1 < nt; ++j) {
+            ok = load_k(cur, j + 1);
+            if (ok) ok = load_v(cur, j);
+          }
+        ok = __shfl_sync(kFullMask, ok, 0);
+        PlanEntry nxt;
+        const bool have_next = ok && next_item(nxt);
+        if (lane == 0 && ok) {
+          if (have_next) ok = load_q(nxt) && load_k(nxt, 0);
+          if (ok) ok = load_v(cur, nt - 1);
+        }
+        ok = __shfl_sync(kFullMask, ok, 0);
+        cur = nxt;
+        have = have_next;
+      }
+      // Drain: never leave the CTA with a TMA write still in flight.  Each
+      // full barrier's last armed phase is waited for, ignoring the CTA abort
+      // flag (issued copies always complete, and must before the CTA exits).
+      // A pair's full barriers live in rank 0 and count both CTAs' copies;
+      // rank 1 stays until rank 0 has drained (the final cluster barrier).
+      if (lane == 0 && !leader && !ok) sb.abort_flag = 1;
+      if (lane == 0 && leader) {
+        if (!ok) sb.abort_flag = 1;
+        volatile int own_flag = 0;
+        if (qn > 0) mbar_wait(&sb.q_full, (qn - 1) & 1, &own_flag, nullptr, 0);
+        for (int i = 0; i < 4; ++i) {
+          if (k_armed[i] > 0) mbar_wait(&sb.k_full[i], (k_armed[i] - 1) & 1, &own_flag, nullptr, 0);
+          if (v_armed[i] > 0) mbar_wait(&sb.v_full[i], (v_armed[i] - 1) & 1, &own_flag, nullptr, 0);
+        }
+      }
+    } else if (warp == 1 && leader) {
+      // ------------------------------------------------------------ MMA issuer
+      // The whole warp runs this loop (converged, warp-uniform values); each
+      // tcgen05.mma and commit is issued by one elected lane.  Descriptors are
+      // computed once and each MMA only adds a compile-time offset.  Tile t is
+      // the CTA-wide tile index: S buffer t & 1, K stage t % KST, V stage
+      // t % VST.  In a pair, the same descriptors and TMEM addresses name the
+      // operands in both CTAs.
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(C::ITEM_ROWS, C::BN, false, false);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(C::ITEM_ROWS, C::DV, false, true);
+      const uint64_t dq = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t dk0 = smem_desc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t dv0 = smem_desc_sw128(smem_u32(sV), BN * 128, 1024);
+      bool ok = true;
+      int T = 0, qn = 0;
+      for (int n = 0; ok; ++n) {
+        PlanEntry e;
+        ok = consume_plan(sb, n, lane, e, p.err);
+        if (!ok || e.last) break;
+        const Plan& pl = e.pl;
+        if (pl.n_tiles == 0) continue;
+        ok = mbar_wait_spin(&sb.q_full, qn & 1, &sb.abort_flag, p.err, kDevTimeoutLoad);
+        ++qn;
+        for (int j = 0; ok && j <= pl.n_tiles; ++j) {
+          if (j < pl.n_tiles) {
+            const int t = T + j;
+            const int s = t % C::KST;
+            if (!mbar_wait_spin(&sb.k_full[s], (t / C::KST) & 1, &sb.abort_flag, p.err, kDevTimeoutLoad)) {
+              ok = false;
+              break;
             }
+            const uint32_t d = tmem + C::S_COL + (t & 1) * BN;
+            const uint64_t dk = dk0 + static_cast<uint64_t>((s * C::K_BYTES) >> 4);
+  #pragma unroll
+            for (int c = 0; c < C::QCH; ++c) {
+  #pragma unroll
+              for (int k16 = 0; k16 < 4; ++k16) {
+                const uint64_t a = dq + static_cast<uint64_t>((c * (kBM * 128) + k16 * 32) >> 4);
+                const uint64_t b = dk + static_cast<uint64_t>((c * (C::KROWS * 128) + k16 * 32) >> 4);
+                mma_ss_elect<C::NCTA>(d, a, b, idesc_qk, (c | k16) != 0 ? 1u : 0u);
+              }
+            }
+            if constexpr (!C::MERGED_RELEASE) {
+              mma_commit_elect<C::NCTA>(&sb.k_empty[s]);
+              if (j == pl.n_tiles - 1) mma_commit_elect<C::NCTA>(&sb.q_empty);  // Q free for the next item
+            }
+            mma_commit_elect<C::NCTA>(&sb.s_full[t & 1]);
           }
-          if constexpr (!C::MERGED_RELEASE) {
-            mma_commit_elect<C::NCTA>(&sb.k_empty[s]);
-            if (j == pl.n_tiles - 1) mma_commit_elect<C::NCTA>(&sb.q_empty);  // Q free for the next item
+          if (j >= 1) {
+            const int t = T + j - 1;
+            if (!mbar_wait_spin(&sb.p_full[t & 1], (t >> 1) & 1, &sb.abort_flag, p.err, kDevTimeoutSoftmax)) {
+              ok = false;
+              break;
+            }
+            // The item's first PV overwrites O: the epilogue warps must have
+            // read the previous item's O out of TMEM (both CTAs of a pair).
+            if (j == 1 && qn > 1 &&
+                !mbar_wait_spin(&sb.o_free, (qn - 2) & 1, &sb.abort_flag, p.err, kDevTimeoutSoftmax)) {
+              ok = false;
+              break;
+            }
+            const int s = t % C::VST;
+            if (!mbar_wait_spin(&sb.v_full[s], (t / C::VST) & 1, &sb.abort_flag, p.err, kDevTimeoutLoad)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();  // P (softmax warps) and the O read-out (epilogue warps) are ordered before
+            const uint32_t pcol = tmem + C::S_COL + (t & 1) * BN;
+            const uint64_t dv = dv0 + static_cast<uint64_t>((s * C::V_BYTES) >> 4);
+            const uint32_t first = (j > 1) ? 1u : 0u;  // the item's first PV overwrites O
+  #pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk) {
+              const uint64_t b = dv + static_cast<uint64_t>((kk * 16 * 128) >> 4);
+              mma_ts_elect<C::NCTA>(tmem + C::O_COL, pcol + kk * 8, b, idesc_pv, kk == 0 ? first : 1u);
+            }
+            if constexpr (!C::MERGED_RELEASE) mma_commit_elect<C::NCTA>(&sb.v_empty[s]);
+            mma_commit_elect<C::NCTA>(&sb.o_done[t & 1]);
           }
-          mma_commit_elect<C::NCTA>(&sb.s_full[t & 1]);
         }
-        if (j >= 1) {
-          const int t = T + j - 1;
-          if (!mbar_wait_spin(&sb.p_full[t & 1], (t >> 1) & 1, &sb.abort_flag, p.err, kDevTimeoutSoftmax)) {
-            ok = false;
-            break;
-          }
-          const int s = t % C::VST;
-          if (!mbar_wait_spin(&sb.v_full[s], (t / C::VST) & 1, &sb.abort_flag, p.err, kDevTimeoutLoad)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();  // P was written to TMEM by the softmax threads
-          const uint32_t pcol = tmem + C::S_COL + (t & 1) * BN;
-          const uint64_t dv = dv0 + static_cast<uint64_t>((s * C::V_BYTES) >> 4);
-          const uint32_t first = (j > 1) ? 1u : 0u;  // the item's first PV overwrites O
-#pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk) {
-            const uint64_t b = dv + static_cast<uint64_t>((kk * 16 * 128) >> 4);
-            mma_ts_elect<C::NCTA>(tmem + C::O_COL, pcol + kk * 8, b, idesc_pv, kk == 0 ? first : 1u);
-          }
-          if constexpr (!C::MERGED_RELEASE) mma_commit_elect<C::NCTA>(&sb.v_empty[s]);
-          mma_commit_elect<C::NCTA>(&sb.o_done[t & 1]);
-        }
+        T += pl.n_tiles;
       }
-      T += pl.n_tiles;
+      if (!ok && lane == 0) sb.abort_flag = 1;
+      // All issued MMAs must finish before TMEM is released (and, in a pair,
+      // before the peer's shared memory and TMEM go away).
+      mma_commit_elect<C::NCTA>(&sb.final_mma);
+      volatile int own_flag = 0;
+      mbar_wait(&sb.final_mma, 0, &own_flag, p.err, kDevTimeoutMma);
+    } else if (warp == 1) {
+      // A pair's rank 1: its TMEM is allocated by this warp; rank 0 issues the MMAs.
+    } else if (warp == C::SCHED_WARP) {
+      // ------------------------------------------------------------ scheduler
+      // Walks this CTA's items (static stride), computes each valid item's
+      // geometry and key-tile plan, and publishes them through the plan ring,
+      // up to kPlanRing items ahead of the slowest consumer warp.
+      int n = 0;
+      bool ok = true;
+      auto publish = [&](const PlanEntry& e) -> bool {
+        const int slot = n % kPlanRing;
+        bool good = true;
+        if (lane == 0 && n >= kPlanRing)
+          good = mbar_wait(&sb.plan_empty[slot], ((n / kPlanRing) - 1) & 1, &sb.abort_flag, p.err, kDevTimeoutOther);
+        good = __shfl_sync(kFullMask, good, 0);
+        if (good && lane == 0) {
+          sb.plans[slot] = e;
+          mbar_arrive(&sb.plan_full[slot]);  // release: the entry is visible to the waiting consumers
+        }
+        ++n;
+        return good;
+      };
+      const int n_groups = gridDim.x / C::NCTA;  // clusters (single CTAs when NCTA == 1)
+      for (int item = blockIdx.x / C::NCTA; ok && item < n_items; item += n_groups) {
+        PlanEntry e;
+        e.it = item_geometry<C>(item, p);
+        if (!e.it.valid) continue;
+        e.pl = plan_tiles<C>(e.it, p, use_table, lane);
+        e.last = 0;
+        ok = publish(e);
+      }
+      if (ok) {
+        PlanEntry e{};
+        e.last = 1;
+        publish(e);
+      }
     }
-    if (!ok && lane == 0) sb.abort_flag = 1;
-    // All issued MMAs must finish before TMEM is released (and, in a pair,
-    // before the peer's shared memory and TMEM go away).
-    mma_commit_elect<C::NCTA>(&sb.final_mma);
-    volatile int own_flag = 0;
-    mbar_wait(&sb.final_mma, 0, &own_flag, p.err, kDevTimeoutMma);
-  } else if (warp == 1) {
-    // A pair's rank 1: its TMEM is allocated by this warp; rank 0 issues the MMAs.
-  } else if (warp < C::SCHED_WARP) {
+  } else if (warp < C::SOFTMAX_END) {
     // ------------------------------------------------------------ softmax rows
+    if constexpr (C::REG_SPLIT) regs_increase<C::REGS_SOFTMAX>();
     constexpr int HC = C::HC;
     const int quarter = warp & 3;
-    const int half = (warp - 2) / 4;  // which column half of the row
+    const int half = (warp - C::SOFTMAX_BEGIN) / 4;  // which column half of the row
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const float sc = p.m.scale_log2;  // > 0 (checked on the host)
@@ -559,9 +634,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     float2* xslots = reinterpret_cast<float2*>(smem + C::RED_OFF);
     uint64_t* xb = sb.xchg[quarter];
     int xk = 0;  // exchanges done by this thread
-    const bool out_v8 = (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0;
+    float2* rowinfo = reinterpret_cast<float2*>(smem + C::ROW_OFF);
     bool ok = true;
-    int T = 0, n = 0;
+    int T = 0, n = 0, hk = 0;  // hk: items handed to the epilogue warps
     // This thread's row of an item: geometry, visible intervals and sink.
     struct RowCtx {
       int head, qi;
@@ -572,21 +647,41 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     const int pos_off = rank * (kBM / p.gpack);  // this CTA's first position within an item
     // p_full lives in rank 0: one arrival per warp (released at cluster scope in a pair)
     const uint32_t p_full_addr0 = C::NCTA == 2 ? mapa_shared(smem_u32(&sb.p_full[0]), 0) : 0u;
-    auto row_ctx = [&](const PlanEntry& e) {
+    // The row's global inputs (range-table entry, sink), loaded one item
+    // ahead so that their latency hides behind the current item's tiles.
+    struct RowLoads {
+      int2 tab;
+      float sink;
+    };
+    auto row_loads = [&](const PlanEntry& e) {
+      RowLoads l;
+      const int qi = e.it.pos0 + pos_off + row / p.gpack;
+      const bool valid = !e.last && qi < e.it.q_len;
+      l.tab = (valid && use_table) ? __ldg(reinterpret_cast<const int2*>(p.m.table) + e.it.q0 + qi) : make_int2(1, 0);
+      l.sink = (!e.last && p.m.sink_mode != 0 && p.m.sinks != nullptr) ? __ldg(p.m.sinks + e.it.h0 + (row % p.gpack))
+                                                                       : 0.f;
+      return l;
+    };
+    auto row_ctx = [&](const PlanEntry& e, const RowLoads& l) {
       RowCtx r;
       r.head = e.it.h0 + (row % p.gpack);
       r.qi = e.it.pos0 + pos_off + row / p.gpack;
       r.valid = !e.last && r.qi < e.it.q_len;
-      r.vis = r.valid ? row_visibility(p.m, e.it.ctx + r.qi, e.it.k_len, use_table ? (e.it.q0 + r.qi) : -1)
-                      : empty_row();
-      r.sink = (!e.last && p.m.sink_mode != 0 && p.m.sinks != nullptr) ? __ldg(p.m.sinks + r.head) : 0.f;
+      r.vis = r.valid ? row_visibility_from(p.m, e.it.ctx + r.qi, e.it.k_len, use_table, l.tab) : empty_row();
+      r.sink = l.sink;
       return r;
     };
     PlanEntry cur;
     ok = consume_plan(sb, n++, lane, cur, p.err);
-    RowCtx rc = row_ctx(cur);
+    RowCtx rc = row_ctx(cur, row_loads(cur));
     while (ok && !cur.last) {
       const Item& it = cur.it;
+      // Take the next item's plan now and start its row loads; they are
+      // used only after this item's tiles.
+      PlanEntry nxt;
+      if (ok) ok = consume_plan(sb, n++, lane, nxt, p.err);
+      if (!ok) nxt.last = 1;
+      const RowLoads nloads = row_loads(nxt);
       const Plan& pl = cur.pl;
       const int head = rc.head;
       const int qi = rc.qi;
@@ -720,13 +815,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (!ok) break;
       }
 
-      // ---------------------------------------------------------- epilogue
-      // Take the next item's plan and start its row lookups (the range-table
-      // load) before this item's epilogue, which hides their latency.
-      PlanEntry nxt;
-      if (ok) ok = consume_plan(sb, n++, lane, nxt, p.err);
-      if (!ok) nxt.last = 1;
-      const RowCtx nrc = row_ctx(nxt);
+      // ---------------------------------------------------------- end of item
+      const RowCtx nrc = row_ctx(nxt, nloads);
       if constexpr (C::SPLIT > 1) {
         // combine the halves' partial sums
         float2 other;
@@ -737,103 +827,110 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           ok = false;
         }
       }
-      bool have_o = ok && pl.n_tiles > 0;
-      if (have_o) {
-        const int tl = T + pl.n_tiles - 1;  // the item's last PV
-        have_o = mbar_wait(&sb.o_done[tl & 1], (tl >> 1) & 1, &sb.abort_flag, p.err, kDevTimeoutMma);
-        tc_fence_after();
-      }
-      if (!have_o && pl.n_tiles > 0) ok = false;
-      // Normalise O and store this thread's row segment (TMEM loads two
-      // 32-column chunks per wait; 32-byte stores when the output allows).
-      const float inv_l = (l_sum > 0.f) ? 1.f / l_sum : 0.f;
-      __nv_bfloat16* orow = nullptr;
-      if (row_valid)
-        orow = reinterpret_cast<__nv_bfloat16*>(p.out) + (static_cast<size_t>(it.q0 + qi) * p.hq + head) * C::D +
-               it.dv0 + half * C::HDV;
-      const uint32_t ocol = tmem + lane_base + C::O_COL + half * C::HDV;
-      constexpr int EB = C::HDV >= 64 ? 2 : 1;  // 32-column chunks per TMEM wait
-#pragma unroll 1
-      for (int c = 0; c < C::HDV / (32 * EB); ++c) {
-        uint32_t o[EB][32];
-        if (have_o) {
-#pragma unroll
-          for (int u = 0; u < EB; ++u) tmem_ld_32x32b_x32(ocol + (c * EB + u) * 32, o[u]);
-#pragma unroll
-          for (int u = 0; u < EB; ++u) tmem_ld_wait(o[u]);
-        } else {
-#pragma unroll
-          for (int u = 0; u < EB; ++u)
-#pragma unroll
-            for (int v = 0; v < 32; ++v) o[u][v] = 0u;
-        }
-        if (row_valid) {
-#pragma unroll
-          for (int u = 0; u < EB; ++u) {
-            uint32_t packed[16];
-#pragma unroll
-            for (int v = 0; v < 16; ++v)
-              packed[v] =
-                  pack_bf16x2(__uint_as_float(o[u][2 * v]) * inv_l, __uint_as_float(o[u][2 * v + 1]) * inv_l);
-            __nv_bfloat16* dst = orow + (c * EB + u) * 32;
-            if (out_v8) {
-              st_global_v8(dst, packed);
-              st_global_v8(dst + 16, packed + 8);
-            } else {
-              uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-              for (int v = 0; v < 4; ++v)
-                d4[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
-            }
-          }
-        }
-      }
-      if (row_valid && half == 0 && p.lse != nullptr && it.dv0 == 0) {
+      // Hand the row's normaliser and LSE to the epilogue warps, which read
+      // O out of TMEM once the item's last PV is done; these warps go on to
+      // the next item at once.
+      if (half == 0) {
+        const int slot = hk % C::EPI_SLOTS;
+        if (hk >= C::EPI_SLOTS &&
+            !mbar_wait(&sb.epi_empty[slot], ((hk / C::EPI_SLOTS) - 1) & 1, &sb.abort_flag, p.err, kDevTimeoutStore))
+          ok = false;
         const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+        const float inv_l = (l_sum > 0.f) ? 1.f / l_sum : 0.f;
         const float lse = (l_lse > 0.f) ? (m_use + lg2_approx(l_lse)) * 0.6931471805599453f : -INFINITY;
-        p.lse[static_cast<size_t>(head) * p.total_q + it.q0 + qi] = lse;
+        rowinfo[slot * kBM + row] = make_float2(inv_l, lse);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sb.epi_full[slot]);  // release: the row values are visible
       }
-      // O may be overwritten by the next item's first PV only after these
-      // TMEM reads: the next p_full arrival of these threads orders them.
-      tc_fence_before();
+      ++hk;
       T += pl.n_tiles;
       cur = nxt;
       rc = nrc;
     }
   } else {
-    // ------------------------------------------------------------ scheduler
-    // Walks this CTA's items (static stride), computes each valid item's
-    // geometry and key-tile plan, and publishes them through the plan ring,
-    // up to kPlanRing items ahead of the slowest consumer warp.
-    int n = 0;
+    // ------------------------------------------------------------ epilogue
+    if constexpr (C::REG_SPLIT) regs_decrease<C::REGS_EPI>();
+    // One thread per row (TMEM lane): waits for the row's (1 / l, LSE) from
+    // the softmax warps and for the item's last PV, reads O out of TMEM 32
+    // columns at a time, normalises, stores; after the last TMEM read it
+    // releases O for the next item's first PV (o_free).
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const int pos_off = rank * (kBM / p.gpack);
+    const bool out_v8 = (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0;
+    const float2* rowinfo = reinterpret_cast<const float2*>(smem + C::ROW_OFF);
+    const uint32_t o_free_addr0 = C::NCTA == 2 ? mapa_shared(smem_u32(&sb.o_free), 0) : 0u;
     bool ok = true;
-    auto publish = [&](const PlanEntry& e) -> bool {
-      const int slot = n % kPlanRing;
-      bool good = true;
-      if (lane == 0 && n >= kPlanRing)
-        good = mbar_wait(&sb.plan_empty[slot], ((n / kPlanRing) - 1) & 1, &sb.abort_flag, p.err, kDevTimeoutOther);
-      good = __shfl_sync(kFullMask, good, 0);
-      if (good && lane == 0) {
-        sb.plans[slot] = e;
-        mbar_arrive(&sb.plan_full[slot]);  // release: the entry is visible to the waiting consumers
-      }
-      ++n;
-      return good;
-    };
-    const int n_groups = gridDim.x / C::NCTA;  // clusters (single CTAs when NCTA == 1)
-    for (int item = blockIdx.x / C::NCTA; ok && item < n_items; item += n_groups) {
+    int T = 0, hk = 0;
+    for (int n = 0; ok; ++n) {
       PlanEntry e;
-      e.it = item_geometry<C>(item, p);
-      if (!e.it.valid) continue;
-      e.pl = plan_tiles<C>(e.it, p, use_table, lane);
-      e.last = 0;
-      ok = publish(e);
+      ok = consume_plan(sb, n, lane, e, p.err);
+      if (!ok || e.last) break;
+      const int head = e.it.h0 + (row % p.gpack);
+      const int qi = e.it.pos0 + pos_off + row / p.gpack;
+      const bool valid = qi < e.it.q_len;
+      const int slot = hk % C::EPI_SLOTS;
+      if (!mbar_wait(&sb.epi_full[slot], (hk / C::EPI_SLOTS) & 1, &sb.abort_flag, p.err, kDevTimeoutSoftmax)) {
+        ok = false;
+        break;
+      }
+      const float2 info = rowinfo[slot * kBM + row];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sb.epi_empty[slot]);
+      ++hk;
+      const bool has_tiles = e.pl.n_tiles > 0;
+      if (has_tiles) {
+        const int tl = T + e.pl.n_tiles - 1;  // the item's last PV
+        if (!mbar_wait(&sb.o_done[tl & 1], (tl >> 1) & 1, &sb.abort_flag, p.err, kDevTimeoutMma)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
+      __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.out) +
+                            (static_cast<size_t>(e.it.q0 + qi) * p.hq + head) * C::D + e.it.dv0;
+      const uint32_t ocol = tmem + lane_base + C::O_COL;
+#pragma unroll 1
+      for (int c = 0; c < C::DV / 32; ++c) {
+        uint32_t o[32];
+        if (has_tiles) {
+          tmem_ld_32x32b_x32(ocol + c * 32, o);
+          tmem_ld_wait(o);
+        } else {
+#pragma unroll
+          for (int v = 0; v < 32; ++v) o[v] = 0u;
+        }
+        if (has_tiles && c == C::DV / 32 - 1) {
+          // O is out of TMEM: the next item's first PV may overwrite it.
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            if constexpr (C::NCTA == 2) mbar_arrive_cluster(o_free_addr0);
+            else mbar_arrive(&sb.o_free);
+          }
+        }
+        if (valid) {
+          uint32_t w[16];
+#pragma unroll
+          for (int v = 0; v < 16; ++v)
+            w[v] = pack_bf16x2(__uint_as_float(o[2 * v]) * info.x, __uint_as_float(o[2 * v + 1]) * info.x);
+          __nv_bfloat16* dst = orow + c * 32;
+          if (out_v8) {
+            st_global_v8(dst, w);
+            st_global_v8(dst + 16, w + 8);
+          } else {
+            uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) d4[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+          }
+        }
+      }
+      if (valid && p.lse != nullptr && e.it.dv0 == 0)
+        p.lse[static_cast<size_t>(head) * p.total_q + e.it.q0 + qi] = info.y;
+      T += e.pl.n_tiles;
     }
-    if (ok) {
-      PlanEntry e{};
-      e.last = 1;
-      publish(e);
-    }
+    if (!ok && lane == 0) sb.abort_flag = 1;
   }
 
   tc_fence_before();

@@ -64,9 +64,17 @@ __device__ __forceinline__ RowVis empty_row() {
   return v;
 }
 
+// The same from an already loaded table entry (use_range false: range off).
+__device__ __forceinline__ RowVis row_visibility_from(const MaskParams& m, int p, int k_len, bool use_range, int2 e);
+
 // p: absolute query position; k_len: keys of the request; table_row: packed
 // row index of this query, or -1 when the range part is off.
 __device__ __forceinline__ RowVis row_visibility(const MaskParams& m, int p, int k_len, int table_row) {
+  const int2 e = table_row >= 0 ? __ldg(reinterpret_cast<const int2*>(m.table) + table_row) : make_int2(1, 0);
+  return row_visibility_from(m, p, k_len, table_row >= 0, e);
+}
+
+__device__ __forceinline__ RowVis row_visibility_from(const MaskParams& m, int p, int k_len, bool use_range, int2 e) {
   RowVis v;
   const long long wl = m.window_left, wr = m.window_right;
   long long lo = (wl >= 0) ? (long long)p - wl : 0;
@@ -79,8 +87,7 @@ __device__ __forceinline__ RowVis row_visibility(const MaskParams& m, int p, int
   v.b_hi = (int)hi;
   v.r_lo = 1;
   v.r_hi = 0;
-  if (table_row >= 0) {
-    const int2 e = __ldg(reinterpret_cast<const int2*>(m.table) + table_row);
+  if (use_range) {
     long long rl = e.x;
     if (wl >= 0 && (long long)p - wl > rl) rl = (long long)p - wl;
     if (rl < 0) rl = 0;

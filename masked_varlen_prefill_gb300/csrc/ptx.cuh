@@ -20,6 +20,7 @@ enum DeviceError : int {
   kDevTimeoutMma = 2,       // an MMA completion barrier never arrived
   kDevTimeoutSoftmax = 3,   // a softmax/correction hand-off never arrived
   kDevTimeoutOther = 4,
+  kDevTimeoutStore = 5,     // the epilogue warps never released a hand-off slot
 };
 
 // Wall-clock budget of one barrier wait.  Legitimate waits in these kernels
@@ -413,6 +414,19 @@ __device__ __forceinline__ void mma_commit_elect(uint64_t* bar) {
         "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
         "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
         : "memory");
+}
+
+// ------------------------------------------------------------------ registers
+// Warpgroup register re-allocation (all 128 threads of the warpgroup execute
+// the same instruction).  The per-thread totals of all warpgroups must not
+// exceed what the block was launched with.
+template <uint32_t N>
+__device__ __forceinline__ void regs_increase() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_decrease() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // ------------------------------------------------------------------ descriptors
