@@ -152,6 +152,41 @@ int mvp_attn_fwd_varlen(const void* q, const void* k, const void* v, void* out, 
                         void* stream);
 
 /*
+ * The same attention over a paged K/V cache (the block-table layout of
+ * vLLM's paged attention, which the FA4 pages run their masks on): the keys
+ * and values of request b are not packed rows but seq_lens_k[b] positions
+ * spread over fixed-size blocks of a shared cache.
+ *
+ * k_cache, v_cache  bf16 [num_blocks * block_size, num_heads_kv, head_dim]
+ *                 (that is, [num_blocks, block_size, Hkv, D] contiguous),
+ *                 16-byte aligned.
+ * block_table     int32 [num_reqs, max_blocks_per_seq]: key j of request b
+ *                 is row block_table[b][j / block_size] * block_size
+ *                 + j % block_size of the caches.  Only the entries of blocks
+ *                 holding the request's keys are read; ids outside
+ *                 [0, num_blocks) read zeros (TMA bounds), never out of the
+ *                 caches.
+ * seq_lens_k      int32 [num_reqs], keys per request (k_len); the request's
+ *                 queries end at its last key unless context_lens says
+ *                 otherwise.
+ * block_size      16, 32, 64, 128 or 256.
+ * max_blocks_per_seq * block_size must cover max_k_len.
+ * All other arguments, results and errors are those of mvp_attn_fwd_varlen
+ * (cu_seqlens_k is replaced by seq_lens_k + block_table); packed and paged
+ * calls on the same logical keys give bit-identical results.
+ * Errors: MVP_ERR_ARG also for a block size outside the list, a table too
+ * short for max_k_len, or NULL block_table / seq_lens_k.
+ */
+int mvp_attn_fwd_paged(const void* q, const void* k_cache, const void* v_cache, void* out, float* lse,
+                       const int32_t* cu_seqlens_q, const int32_t* seq_lens_k, const int32_t* block_table,
+                       int block_size, int max_blocks_per_seq, int num_blocks, const int32_t* context_lens,
+                       int num_reqs, int total_q, int max_q_len, int max_k_len, int num_decode_reqs,
+                       int num_heads_q, int num_heads_kv, int head_dim, const int32_t* range_table,
+                       const int32_t* range_covered, int causal, int window_left, int window_right,
+                       const float* sinks, int sink_mode, float scale, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
+/*
  * Allocation-free variant of mvp_attn_fwd_varlen.  The pages have no
  * counterpart of this call; it exists for callers that cannot allocate device
  * memory where they run attention (an engine whose free memory is already
@@ -192,7 +227,8 @@ int mvp_get_last_device_error(void* stream);
 const char* mvp_status_str(int status);
 
 /* Number of kernel launches the last successful mvp_attn_fwd_varlen /
- * mvp_fill_query_ranges call enqueued on this thread (for launch accounting). */
+ * mvp_attn_fwd_paged / mvp_fill_query_ranges call enqueued on this thread
+ * (for launch accounting). */
 int mvp_last_launch_count(void);
 
 #ifdef __cplusplus

@@ -20,6 +20,7 @@ from ._lib import (  # noqa: F401
     SINK_NULL_LOGIT,
     MvpError,
     attn_fwd_varlen,
+    attn_fwd_paged,
     attn_fwd_varlen_host,
     attn_fwd_varlen_static_ws,
     attn_workspace_size,

@@ -34,6 +34,8 @@ _SIGNATURES = {
     "mvp_attn_workspace_size": (_sz, [_i, _i, _i, _i]),
     "mvp_attn_fwd_varlen": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i,
                                  _vp, _vp, _i, _i, _i, _vp, _i, _f, _vp, _sz, _vp]),
+    "mvp_attn_fwd_paged": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _vp, _i, _i, _i, _i, _i, _i, _i,
+                                _i, _vp, _vp, _i, _i, _i, _vp, _i, _f, _vp, _sz, _vp]),
     "mvp_attn_fwd_varlen_static_ws": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
                                            _i, _i, _vp, _vp, _i, _i, _i, _vp, _i, _f, _vp]),
     "mvp_static_scratch_bytes": (_sz, []),
@@ -160,6 +162,51 @@ def attn_fwd_varlen(q, k, v, out, cu_seqlens_q, cu_seqlens_k, max_q_len, max_k_l
         _ptr(sinks), int(sink_mode), float(scale), _ptr(workspace), ws_bytes, _stream(stream, dev))
     if st != MVP_OK:
         raise MvpError("mvp_attn_fwd_varlen", st)
+
+
+def attn_fwd_paged(q, k_cache, v_cache, out, cu_seqlens_q, seq_lens_k, block_table, block_size, max_q_len,
+                   max_k_len, *, lse=None, context_lens=None, range_table=None, range_covered=None, causal=True,
+                   window_left=-1, window_right=-1, sinks=None, sink_mode=SINK_NONE, scale=None, workspace=None,
+                   num_decode_reqs=-1, stream=None):
+    """Masked varlen attention over a paged K/V cache (see
+    ``mvp_attn_fwd_paged``): k_cache/v_cache [num_blocks * block_size, Hkv,
+    D] (or [num_blocks, block_size, Hkv, D]) bf16, block_table int32 [B,
+    max_blocks_per_seq], seq_lens_k int32 [B]; the rest as ``attn_fwd_varlen``."""
+    lib = load_library()
+    dev = q.device
+    if k_cache.dim() == 4:
+        k_cache = k_cache.reshape(-1, k_cache.shape[2], k_cache.shape[3])
+        v_cache = v_cache.reshape(-1, v_cache.shape[2], v_cache.shape[3])
+    for n, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("out", out)):
+        _check_cuda(n, t, torch.bfloat16, dev)
+    for n, t in (("cu_seqlens_q", cu_seqlens_q), ("seq_lens_k", seq_lens_k), ("block_table", block_table),
+                 ("context_lens", context_lens), ("range_table", range_table), ("range_covered", range_covered)):
+        _check_cuda(n, t, torch.int32, dev)
+    _check_cuda("lse", lse, torch.float32, dev)
+    _check_cuda("sinks", sinks, torch.float32, dev)
+    if workspace is not None and (not workspace.is_cuda or not workspace.is_contiguous()):
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    if q.dim() != 3 or k_cache.dim() != 3 or v_cache.shape != k_cache.shape or out.shape != q.shape:
+        raise ValueError("q/out must be [total_q, Hq, D] and the caches [num_blocks * block_size, Hkv, D]")
+    if block_table is None or block_table.dim() != 2 or seq_lens_k is None:
+        raise ValueError("block_table must be [B, max_blocks_per_seq] and seq_lens_k [B]")
+    total_q, hq, d = q.shape
+    rows, hkv, dk = k_cache.shape
+    if dk != d:
+        raise ValueError("q and the caches differ in head_dim")
+    if rows % int(block_size) != 0:
+        raise ValueError("cache rows must be a multiple of block_size")
+    if scale is None:
+        scale = d ** -0.5
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.mvp_attn_fwd_paged(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(lse), _ptr(cu_seqlens_q), _ptr(seq_lens_k),
+        _ptr(block_table), int(block_size), block_table.shape[1], rows // int(block_size), _ptr(context_lens),
+        cu_seqlens_q.shape[0] - 1, total_q, int(max_q_len), int(max_k_len), int(num_decode_reqs), hq, hkv, d,
+        _ptr(range_table), _ptr(range_covered), int(bool(causal)), int(window_left), int(window_right),
+        _ptr(sinks), int(sink_mode), float(scale), _ptr(workspace), ws_bytes, _stream(stream, dev))
+    if st != MVP_OK:
+        raise MvpError("mvp_attn_fwd_paged", st)
 
 
 def attn_fwd_varlen_static_ws(q, k, v, out, cu_seqlens_q, cu_seqlens_k, max_q_len, max_k_len, *, lse=None,

@@ -140,15 +140,35 @@ size_t mvp_attn_workspace_size(int num_reqs, int num_heads_q, int head_dim, int 
   return static_cast<size_t>(num_reqs) * num_heads_q * splits * (head_dim + 2) * sizeof(float);
 }
 
-int mvp_attn_fwd_varlen(const void* q, const void* k, const void* v, void* out, float* lse,
-                        const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, const int32_t* context_lens,
-                        int num_reqs, int total_q, int total_k, int max_q_len, int max_k_len,
-                        int num_decode_reqs, int num_heads_q, int num_heads_kv, int head_dim, const int32_t* range_table, const int32_t* range_covered,
-                        int causal, int window_left, int window_right, const float* sinks, int sink_mode,
-                        float scale, void* workspace, size_t workspace_bytes, void* stream) {
-  g_last_launches = 0;
+}  // extern "C"
+
+namespace mvp {
+namespace {
+
+// Where the keys and values live: packed ([total_k, Hkv, D] with row offsets
+// cu_k) or paged ([num_blocks * block_size, Hkv, D] addressed through a
+// block table, keys per request in seq_k).
+struct KVArgs {
+  const void* k;
+  const void* v;
+  long long rows;  // rows of the K/V tensors
+  const int32_t* cu_k;
+  const int32_t* seq_k;
+  const int32_t* block_table;
+  int block_shift;
+  int max_blocks;
+};
+
+int attn_fwd_impl(const void* q, void* out, float* lse, const int32_t* cu_seqlens_q, const int32_t* context_lens,
+                  int num_reqs, int total_q, int max_q_len, int max_k_len, int num_decode_reqs, int num_heads_q,
+                  int num_heads_kv, int head_dim, const int32_t* range_table, const int32_t* range_covered,
+                  int causal, int window_left, int window_right, const float* sinks, int sink_mode, float scale,
+                  void* workspace, size_t workspace_bytes, void* stream, const KVArgs& kv) {
+  const void* k = kv.k;
+  const void* v = kv.v;
+  const bool paged = kv.block_table != nullptr;
   // ------------------------------------------------------------ validation
-  if (num_reqs < 1 || num_reqs > 65535 || total_q < 0 || total_k < 0) return MVP_ERR_ARG;
+  if (num_reqs < 1 || num_reqs > 65535 || total_q < 0 || kv.rows < 0) return MVP_ERR_ARG;
   if (num_heads_q < 1 || num_heads_kv < 1 || num_heads_q % num_heads_kv != 0) return MVP_ERR_ARG;
   if (head_dim != 64 && head_dim != 128 && head_dim != 256 && head_dim != 512) return MVP_ERR_UNSUPPORTED;
   if (sink_mode < 0 || sink_mode > 2) return MVP_ERR_ARG;
@@ -158,14 +178,17 @@ int mvp_attn_fwd_varlen(const void* q, const void* k, const void* v, void* out, 
   if (num_decode_reqs < -1 || num_decode_reqs > num_reqs) return MVP_ERR_ARG;
   if (!(scale > 0.f) || scale > 3.0e38f) return MVP_ERR_ARG;  // NaN, <= 0, inf
   if (total_q == 0) return MVP_OK;
-  if (total_k < 1 || max_q_len < 1 || max_k_len < 1) return MVP_ERR_ARG;
+  if (kv.rows < 1 || kv.rows > INT_MAX || max_q_len < 1 || max_k_len < 1) return MVP_ERR_ARG;
   if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || cu_seqlens_q == nullptr ||
-      cu_seqlens_k == nullptr)
+      (paged ? kv.seq_k == nullptr : kv.cu_k == nullptr))
     return MVP_ERR_ARG;
+  const int total_k = static_cast<int>(kv.rows);
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return MVP_ERR_UNSUPPORTED;
   if (range_table != nullptr && (reinterpret_cast<uintptr_t>(range_table) & 7u) != 0) return MVP_ERR_UNSUPPORTED;
   if (static_cast<long long>(total_q) * num_heads_q * head_dim >= (1LL << 40)) return MVP_ERR_UNSUPPORTED;
 
+  // Paged: a TMA box never crosses a cache block.
+  auto box_rows = [&](int rows) { return paged ? (rows < (1 << kv.block_shift) ? rows : (1 << kv.block_shift)) : rows; };
   int* err = nullptr;
   int num_sms = 1;
   if (device_state(&err, &num_sms) != cudaSuccess) return MVP_ERR_CUDA;
@@ -173,7 +196,11 @@ int mvp_attn_fwd_varlen(const void* q, const void* k, const void* v, void* out, 
 
   MaskParams m;
   m.cu_q = cu_seqlens_q;
-  m.cu_k = cu_seqlens_k;
+  m.cu_k = paged ? nullptr : kv.cu_k;
+  m.seq_k = paged ? kv.seq_k : nullptr;
+  m.block_table = kv.block_table;
+  m.block_shift = paged ? kv.block_shift : 0;
+  m.max_blocks = paged ? kv.max_blocks : 0;
   m.ctx_lens = context_lens;
   m.table = range_table;
   m.covered = range_table ? range_covered : nullptr;
@@ -215,8 +242,8 @@ int mvp_attn_fwd_varlen(const void* q, const void* k, const void* v, void* out, 
 
     CUtensorMap mq, mk, mv;
     if (!encode_3d(&mq, q, head_dim, num_heads_q, total_q, 64, gpack, bmp, true) ||
-        !encode_3d(&mk, k, head_dim, num_heads_kv, total_k, 64, 1, shape.k_box_keys, true) ||
-        !encode_3d(&mv, v, head_dim, num_heads_kv, total_k, 64, 1, shape.v_box_keys, true))
+        !encode_3d(&mk, k, head_dim, num_heads_kv, total_k, 64, 1, box_rows(shape.k_box_keys), true) ||
+        !encode_3d(&mv, v, head_dim, num_heads_kv, total_k, 64, 1, box_rows(shape.v_box_keys), true))
       return MVP_ERR_UNSUPPORTED;
     if (launch_prefill(head_dim, pp, mq, mk, mv, st) != cudaSuccess) return MVP_ERR_CUDA;
     ++launches;
@@ -235,9 +262,12 @@ int mvp_attn_fwd_varlen(const void* q, const void* k, const void* v, void* out, 
     dp.hq = num_heads_q;
     dp.hkv = num_heads_kv;
     dp.group = group;
+    const int kt = decode_keys_per_tile(head_dim);
+    // Keys a decode row's CTA walks: its visible hull, started on a multiple
+    // of the tile size (the kernel aligns it down by up to kt - 1 keys).
     long long span = max_k_len;
     if (causal && window_left >= 0 && range_table == nullptr && context_lens == nullptr)
-      span = (window_left + 1LL < span) ? window_left + 1LL : span;
+      span = (window_left + static_cast<long long>(kt) < span) ? window_left + static_cast<long long>(kt) : span;
     int splits = static_cast<int>((span + kDecodeChunk - 1) / kDecodeChunk);
     if (splits > kMaxSplits) splits = kMaxSplits;
     const size_t per_split = static_cast<size_t>(decode_count) * num_heads_q * (head_dim + 2) * sizeof(float);
@@ -245,7 +275,6 @@ int mvp_attn_fwd_varlen(const void* q, const void* k, const void* v, void* out, 
     else if (static_cast<size_t>(splits) * per_split > workspace_bytes)
       splits = static_cast<int>(workspace_bytes / per_split);
     if (splits < 2) splits = 1;
-    const int kt = decode_keys_per_tile(head_dim);
     long long chunk = (span + splits - 1) / splits;
     chunk = ((chunk + kt - 1) / kt) * kt;
     if (chunk > INT_MAX) chunk = INT_MAX;
@@ -256,13 +285,54 @@ int mvp_attn_fwd_varlen(const void* q, const void* k, const void* v, void* out, 
     if (static_cast<long long>(num_heads_kv) * ((group + per_cta - 1) / per_cta) > 65535) return MVP_ERR_UNSUPPORTED;
     CUtensorMap mk, mv;
     const int box = decode_box_inner(head_dim);
-    if (!encode_3d(&mk, k, head_dim, num_heads_kv, total_k, box, 1, kt, false) ||
-        !encode_3d(&mv, v, head_dim, num_heads_kv, total_k, box, 1, kt, false))
+    if (!encode_3d(&mk, k, head_dim, num_heads_kv, total_k, box, 1, box_rows(kt), false) ||
+        !encode_3d(&mv, v, head_dim, num_heads_kv, total_k, box, 1, box_rows(kt), false))
       return MVP_ERR_UNSUPPORTED;
     if (launch_decode(head_dim, dp, mk, mv, st, &launches) != cudaSuccess) return MVP_ERR_CUDA;
   }
   g_last_launches = launches;
   return MVP_OK;
+}
+
+}  // namespace
+}  // namespace mvp
+
+extern "C" {
+
+int mvp_attn_fwd_varlen(const void* q, const void* k, const void* v, void* out, float* lse,
+                        const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, const int32_t* context_lens,
+                        int num_reqs, int total_q, int total_k, int max_q_len, int max_k_len, int num_decode_reqs,
+                        int num_heads_q, int num_heads_kv, int head_dim, const int32_t* range_table,
+                        const int32_t* range_covered, int causal, int window_left, int window_right,
+                        const float* sinks, int sink_mode, float scale, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+  g_last_launches = 0;
+  KVArgs kv{k, v, total_k, cu_seqlens_k, nullptr, nullptr, 0, 0};
+  return attn_fwd_impl(q, out, lse, cu_seqlens_q, context_lens, num_reqs, total_q, max_q_len, max_k_len,
+                       num_decode_reqs, num_heads_q, num_heads_kv, head_dim, range_table, range_covered, causal,
+                       window_left, window_right, sinks, sink_mode, scale, workspace, workspace_bytes, stream, kv);
+}
+
+int mvp_attn_fwd_paged(const void* q, const void* k_cache, const void* v_cache, void* out, float* lse,
+                       const int32_t* cu_seqlens_q, const int32_t* seq_lens_k, const int32_t* block_table,
+                       int block_size, int max_blocks_per_seq, int num_blocks, const int32_t* context_lens,
+                       int num_reqs, int total_q, int max_q_len, int max_k_len, int num_decode_reqs, int num_heads_q,
+                       int num_heads_kv, int head_dim, const int32_t* range_table, const int32_t* range_covered,
+                       int causal, int window_left, int window_right, const float* sinks, int sink_mode, float scale,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+  g_last_launches = 0;
+  int shift = 0;
+  while (shift < 30 && (1 << shift) < block_size) ++shift;
+  if (block_size < 16 || block_size > 256 || (1 << shift) != block_size) return MVP_ERR_ARG;
+  if (num_blocks < 1 || max_blocks_per_seq < 1 || block_table == nullptr || seq_lens_k == nullptr)
+    return MVP_ERR_ARG;
+  if (static_cast<long long>(max_blocks_per_seq) * block_size < max_k_len) return MVP_ERR_ARG;
+  if (static_cast<long long>(num_blocks) * block_size > INT_MAX) return MVP_ERR_UNSUPPORTED;
+  KVArgs kv{k_cache, v_cache, static_cast<long long>(num_blocks) * block_size, nullptr, seq_lens_k, block_table,
+            shift, max_blocks_per_seq};
+  return attn_fwd_impl(q, out, lse, cu_seqlens_q, context_lens, num_reqs, total_q, max_q_len, max_k_len,
+                       num_decode_reqs, num_heads_q, num_heads_kv, head_dim, range_table, range_covered, causal,
+                       window_left, window_right, sinks, sink_mode, scale, workspace, workspace_bytes, stream, kv);
 }
 
 int mvp_get_last_device_error(void* stream) {

@@ -85,7 +85,9 @@ __device__ __forceinline__ int row_off(int kk, int lane) {
   return box * (C::KT * C::BOX * 2) + kk * (C::BOX * 2) + (dim0 % C::BOX) * 2;
 }
 
-template <int D, int GP>
+// PAGED: K/V rows come through a block table (compile-time, so the packed
+// kernel carries none of the paged addressing).
+template <int D, int GP, bool PAGED>
 __global__ void __launch_bounds__(kThreads)
     attn_decode_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                        const DecodeParams p) {
@@ -110,12 +112,23 @@ __global__ void __launch_bounds__(kThreads)
   const int q0 = __ldg(p.m.cu_q + b);
   const int q_len = __ldg(p.m.cu_q + b + 1) - q0;
   if (q_len != 1) return;
-  const int k0 = __ldg(p.m.cu_k + b);
-  const int k_len = __ldg(p.m.cu_k + b + 1) - k0;
+  int k0, k_len;
+  if constexpr (PAGED) {
+    k0 = 0;
+    k_len = __ldg(p.m.seq_k + b);
+  } else {
+    k0 = __ldg(p.m.cu_k + b);
+    k_len = __ldg(p.m.cu_k + b + 1) - k0;
+  }
   const int pos = p.m.ctx_lens ? __ldg(p.m.ctx_lens + b) : (k_len - 1);
   const RowVis vis = row_visibility(p.m, pos, k_len, table_active(p.m) ? q0 : -1);
   int lo, hi;
   vis.hull(lo, hi);
+  // Tiles start on multiples of KT (the keys before the visible set are
+  // masked): a tile never straddles a cache block of a paged layout (block
+  // sizes and KT are powers of two), and packed and paged calls walk the
+  // same tiles.
+  if (lo <= hi) lo &= ~(C::KT - 1);
   const int c_lo = lo + sp * p.chunk;
   const int c_hi = (lo <= hi) ? min(hi, c_lo + p.chunk - 1) : -1;
   const int n_keys = (lo <= hi && c_lo <= c_hi) ? (c_hi - c_lo + 1) : 0;
@@ -147,6 +160,7 @@ __global__ void __launch_bounds__(kThreads)
     if (lane == 0 && n_tiles > 0) {
       tma_prefetch_desc(&map_k);
       tma_prefetch_desc(&map_v);
+      const int kbox = PAGED ? min(C::KT, 1 << p.m.block_shift) : C::KT;
       int issued = 0;
       bool ok = true;
       for (int t = 0; t < n_tiles; ++t) {
@@ -159,11 +173,14 @@ __global__ void __launch_bounds__(kThreads)
         mbar_arrive_expect_tx(&sb.full[s], 2 * C::TILE);
         uint8_t* ks = smem + s * 2 * C::TILE;
         uint8_t* vs = ks + C::TILE;
-        const int row = k0 + c_lo + t * C::KT;
+        // one box per run of keys inside one cache block (the whole tile when packed)
+        for (int r = 0; r < C::KT; r += kbox) {
+          const int row = PAGED ? kv_row(p.m, b, k0, k_len, c_lo + t * C::KT + r) : k0 + c_lo + t * C::KT + r;
 #pragma unroll
-        for (int x = 0; x < C::NBOX; ++x) {
-          tma_load_3d(ks + x * (C::KT * C::BOX * 2), &map_k, &sb.full[s], x * C::BOX, hkv, row);
-          tma_load_3d(vs + x * (C::KT * C::BOX * 2), &map_v, &sb.full[s], x * C::BOX, hkv, row);
+          for (int x = 0; x < C::NBOX; ++x) {
+            tma_load_3d(ks + x * (C::KT * C::BOX * 2) + r * (C::BOX * 2), &map_k, &sb.full[s], x * C::BOX, hkv, row);
+            tma_load_3d(vs + x * (C::KT * C::BOX * 2) + r * (C::BOX * 2), &map_v, &sb.full[s], x * C::BOX, hkv, row);
+          }
         }
         ++issued;
       }
@@ -395,7 +412,7 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams 
 
 template <int D, int GP>
 cudaError_t launch_dg(const DecodeParams& p, const CUtensorMap& mk, const CUtensorMap& mv, cudaStream_t stream) {
-  auto kern = attn_decode_kernel<D, GP>;
+  auto kern = p.m.block_table != nullptr ? attn_decode_kernel<D, GP, true> : attn_decode_kernel<D, GP, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DCfg<D>::SMEM);
   if (e != cudaSuccess) return e;
   const int n_sub = (p.group + GP - 1) / GP;

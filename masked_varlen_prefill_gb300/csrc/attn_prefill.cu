@@ -173,7 +173,7 @@ struct __align__(8) Barriers {
 // then request: the CTAs running at the same time then work on neighbouring
 // tiles of a few (request, KV head) pairs, whose K/V windows overlap and stay
 // in L2, and every CTA's strided sequence mixes heavy and light tiles.
-template <class C>
+template <class C, bool PAGED>
 __device__ __forceinline__ Item item_geometry(int item, const PrefillParams& p) {
   const int nz = p.hkv * p.n_hgroups * C::DV_SPLIT;
   const int x = item % p.n_qtiles;  // 0 = latest q tile (heaviest under causal masks)
@@ -187,8 +187,13 @@ __device__ __forceinline__ Item item_geometry(int item, const PrefillParams& p) 
   it.h0 = it.hkv * (p.hq / p.hkv) + (hz % p.n_hgroups) * p.gpack;
   it.q0 = __ldg(p.m.cu_q + it.b);
   it.q_len = __ldg(p.m.cu_q + it.b + 1) - it.q0;
-  it.k0 = __ldg(p.m.cu_k + it.b);
-  it.k_len = __ldg(p.m.cu_k + it.b + 1) - it.k0;
+  if constexpr (PAGED) {
+    it.k0 = 0;
+    it.k_len = __ldg(p.m.seq_k + it.b);
+  } else {
+    it.k0 = __ldg(p.m.cu_k + it.b);
+    it.k_len = __ldg(p.m.cu_k + it.b + 1) - it.k0;
+  }
   it.ctx = p.m.ctx_lens ? __ldg(p.m.ctx_lens + it.b) : (it.k_len - it.q_len);
   it.pos0 = (p.n_qtiles - 1 - x) * (C::ITEM_ROWS / p.gpack);
   it.valid = it.pos0 < it.q_len && !(p.skip_decode && it.q_len == 1);
@@ -274,7 +279,9 @@ __device__ __forceinline__ void tma_load(void* dst, const CUtensorMap* map, uint
   else tma_load_3d(dst, map, full, x, y, z);
 }
 
-template <class C>
+// PAGED: K/V rows come through a block table (compile-time, so the packed
+// kernel carries none of the paged addressing).
+template <class C, bool PAGED>
 __global__ void __launch_bounds__(C::THREADS, 1)
     attn_prefill_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                         const __grid_constant__ CUtensorMap map_v, const PrefillParams p) {
@@ -377,14 +384,19 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       // the current item runs, and every load prefetches the tile kPrefetchAhead
       // steps further.  Each CTA of a pair warms its own half.
       constexpr int kPrefetchAhead = 2;
+      // Paged K/V: loads go one block run at a time (box heights capped at the
+      // block size on the host), and the warming below is skipped.
+      constexpr bool paged = PAGED;
+      const int kbox = PAGED ? min(C::KROWS, 1 << p.m.block_shift) : C::KROWS;
+      const int vbox = PAGED ? min(BN, 1 << p.m.block_shift) : BN;
       auto prefetch_k = [&](const PlanEntry& e, int j) {
         const int krow = e.it.k0 + (e.pl.kb_lo + j) * BN + rank * C::KROWS;
-  #pragma unroll
+#pragma unroll
         for (int c = 0; c < C::QCH; ++c) tma_prefetch_l2_3d(&map_k, c * 64, e.it.hkv, krow);
       };
       auto prefetch_v = [&](const PlanEntry& e, int j) {
         const int krow = e.it.k0 + (e.pl.kb_lo + j) * BN;
-  #pragma unroll
+#pragma unroll
         for (int c = 0; c < C::VCH; ++c) tma_prefetch_l2_3d(&map_v, e.it.dv0 + rank * C::DVC + c * 64, e.it.hkv, krow);
       };
       // Plan n (the next one to consume) if the scheduler has published it;
@@ -394,9 +406,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (!mbar_try_wait(&sb.plan_full[slot], (n / kPlanRing) & 1)) return;
         const PlanEntry e = sb.plans[slot];
         if (e.last || e.pl.n_tiles == 0) return;
-  #pragma unroll
+#pragma unroll
         for (int c = 0; c < C::QCH; ++c) tma_prefetch_l2_3d(&map_q, c * 64, e.it.h0, e.it.q0 + e.it.pos0 + pos_off);
-        for (int j = 0; j < kPrefetchAhead && j < e.pl.n_tiles; ++j) {
+        for (int j = 0; !paged && j < kPrefetchAhead && j < e.pl.n_tiles; ++j) {
           prefetch_k(e, j);
           prefetch_v(e, j);
         }
@@ -413,7 +425,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           if (!free) return false;
         }
         if (leader) mbar_arrive_expect_tx(&sb.q_full, C::NCTA * C::Q_BYTES);
-  #pragma unroll
+#pragma unroll
         for (int c = 0; c < C::QCH; ++c)
           tma_load<C>(sQ + c * (kBM * 128), &map_q, &sb.q_full, c * 64, e.it.h0, e.it.q0 + e.it.pos0 + pos_off);
         ++qn;
@@ -429,11 +441,23 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           if (!free) return false;
         }
         if (leader) mbar_arrive_expect_tx(&sb.k_full[s], C::NCTA * C::K_BYTES);
-        const int krow = e.it.k0 + (e.pl.kb_lo + j) * BN + rank * C::KROWS;
-  #pragma unroll
-        for (int c = 0; c < C::QCH; ++c)
-          tma_load<C>(sK + s * C::K_BYTES + c * (C::KROWS * 128), &map_k, &sb.k_full[s], c * 64, e.it.hkv, krow);
-        if (j + kPrefetchAhead < e.pl.n_tiles) prefetch_k(e, j + kPrefetchAhead);
+        const int key0 = (e.pl.kb_lo + j) * BN + rank * C::KROWS;  // this CTA's first key of the tile
+        if constexpr (PAGED) {
+          // one box per run of K rows inside one cache block
+          for (int r = 0; r < C::KROWS; r += kbox) {
+            const int krow = kv_row(p.m, e.it.b, e.it.k0, e.it.k_len, key0 + r);
+#pragma unroll
+            for (int c = 0; c < C::QCH; ++c)
+              tma_load<C>(sK + s * C::K_BYTES + c * (C::KROWS * 128) + r * 128, &map_k, &sb.k_full[s], c * 64,
+                          e.it.hkv, krow);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < C::QCH; ++c)
+            tma_load<C>(sK + s * C::K_BYTES + c * (C::KROWS * 128), &map_k, &sb.k_full[s], c * 64, e.it.hkv,
+                        e.it.k0 + key0);
+        }
+        if (!paged && j + kPrefetchAhead < e.pl.n_tiles) prefetch_k(e, j + kPrefetchAhead);
         ++k_armed[s];
         ++kc;
         return true;
@@ -448,12 +472,22 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           if (!free) return false;
         }
         if (leader) mbar_arrive_expect_tx(&sb.v_full[s], C::NCTA * C::V_BYTES);
-        const int krow = e.it.k0 + (e.pl.kb_lo + j) * BN;
-  #pragma unroll
-        for (int c = 0; c < C::VCH; ++c)
-          tma_load<C>(sV + s * C::V_BYTES + c * (BN * 128), &map_v, &sb.v_full[s], e.it.dv0 + rank * C::DVC + c * 64,
-                      e.it.hkv, krow);
-        if (j + kPrefetchAhead < e.pl.n_tiles) prefetch_v(e, j + kPrefetchAhead);
+        const int key0 = (e.pl.kb_lo + j) * BN;
+        if constexpr (PAGED) {
+          for (int r = 0; r < BN; r += vbox) {
+            const int vrow = kv_row(p.m, e.it.b, e.it.k0, e.it.k_len, key0 + r);
+#pragma unroll
+            for (int c = 0; c < C::VCH; ++c)
+              tma_load<C>(sV + s * C::V_BYTES + c * (BN * 128) + r * 128, &map_v, &sb.v_full[s],
+                          e.it.dv0 + rank * C::DVC + c * 64, e.it.hkv, vrow);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < C::VCH; ++c)
+            tma_load<C>(sV + s * C::V_BYTES + c * (BN * 128), &map_v, &sb.v_full[s], e.it.dv0 + rank * C::DVC + c * 64,
+                        e.it.hkv, e.it.k0 + key0);
+        }
+        if (!paged && j + kPrefetchAhead < e.pl.n_tiles) prefetch_v(e, j + kPrefetchAhead);
         ++v_armed[s];
         ++vc;
         return true;
@@ -529,9 +563,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             }
             const uint32_t d = tmem + C::S_COL + (t & 1) * BN;
             const uint64_t dk = dk0 + static_cast<uint64_t>((s * C::K_BYTES) >> 4);
-  #pragma unroll
+#pragma unroll
             for (int c = 0; c < C::QCH; ++c) {
-  #pragma unroll
+#pragma unroll
               for (int k16 = 0; k16 < 4; ++k16) {
                 const uint64_t a = dq + static_cast<uint64_t>((c * (kBM * 128) + k16 * 32) >> 4);
                 const uint64_t b = dk + static_cast<uint64_t>((c * (C::KROWS * 128) + k16 * 32) >> 4);
@@ -566,7 +600,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             const uint32_t pcol = tmem + C::S_COL + (t & 1) * BN;
             const uint64_t dv = dv0 + static_cast<uint64_t>((s * C::V_BYTES) >> 4);
             const uint32_t first = (j > 1) ? 1u : 0u;  // the item's first PV overwrites O
-  #pragma unroll
+#pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk) {
               const uint64_t b = dv + static_cast<uint64_t>((kk * 16 * 128) >> 4);
               mma_ts_elect<C::NCTA>(tmem + C::O_COL, pcol + kk * 8, b, idesc_pv, kk == 0 ? first : 1u);
@@ -608,7 +642,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       const int n_groups = gridDim.x / C::NCTA;  // clusters (single CTAs when NCTA == 1)
       for (int item = blockIdx.x / C::NCTA; ok && item < n_items; item += n_groups) {
         PlanEntry e;
-        e.it = item_geometry<C>(item, p);
+        e.it = item_geometry<C, PAGED>(item, p);
         if (!e.it.valid) continue;
         e.pl = plan_tiles<C>(e.it, p, use_table, lane);
         e.last = 0;
@@ -951,7 +985,7 @@ using Cfg512 = Cfg<512, 256, 64, 1, 1, 1>;
 template <class C>
 cudaError_t launch_cfg(const PrefillParams& p, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                        cudaStream_t stream) {
-  auto kern = attn_prefill_kernel<C>;
+  auto kern = p.m.block_table != nullptr ? attn_prefill_kernel<C, true> : attn_prefill_kernel<C, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const long long n_items =

@@ -99,6 +99,20 @@ __device__ __forceinline__ RowVis row_visibility_from(const MaskParams& m, int p
   return v;
 }
 
+// Row of a paged K/V cache (vLLM-style block table, block size
+// 2^block_shift) that holds key l of request b: the block id of l's block
+// times the block size plus l's offset in it.  Keys at or past the request's
+// last block reuse its last block id (they are masked anyway), so the table
+// is only read inside the request's blocks.
+__device__ __forceinline__ int kv_row(const MaskParams& m, int b, int /*k0*/, int k_len, int l) {
+  const int last = k_len > 0 ? ((k_len - 1) >> m.block_shift) : 0;
+  const int blk = min(l >> m.block_shift, last);
+  const int id = __ldg(m.block_table + static_cast<size_t>(b) * m.max_blocks + blk);
+  // unsigned: a corrupt id wraps instead of overflowing; TMA bounds-checks the row
+  return static_cast<int>((static_cast<unsigned>(id) << m.block_shift) +
+                          static_cast<unsigned>(l & ((1 << m.block_shift) - 1)));
+}
+
 __device__ __forceinline__ bool table_active(const MaskParams& m) {
   if (m.table == nullptr) return false;
   if (m.covered == nullptr) return true;

@@ -26,7 +26,11 @@ cudaError_t launch_fill(const FillParams& p, cudaStream_t stream);
 // coordinates of the request).  Shared by the prefill and decode kernels.
 struct MaskParams {
   const int32_t* cu_q;
-  const int32_t* cu_k;
+  const int32_t* cu_k;       // packed K/V: [num_reqs + 1] row offsets (null when paged)
+  const int32_t* seq_k;      // paged K/V: keys per request [num_reqs] (null when packed)
+  const int32_t* block_table;  // paged K/V: [num_reqs, max_blocks] block ids (null when packed)
+  int block_shift;           // log2(block size) when paged
+  int max_blocks;            // row stride of block_table
   const int32_t* ctx_lens;   // or null
   const int32_t* table;      // [total_q, 2] or null
   const int32_t* covered;    // device scalar or null

@@ -199,6 +199,43 @@ WORKLOADS = ["tiny_window_sinks", "mm_prefix_sliding", "global_causal_d512",
              "chunked_prefill_ranges", "mixed_serving_a", "mixed_serving_b"]
 
 
+def to_paged(k, v, k_lens, block_size: int, seed: int = 0, spare_blocks: int = 3, table_fill: int = -1):
+    """Lay packed keys/values out in a paged cache (input generation only).
+
+    k, v: [total_k, Hkv, D] packed by request (k_lens[b] rows each).  Returns
+    (k_cache, v_cache, block_table, seq_lens): the caches are [num_blocks *
+    block_size, Hkv, D] (random bf16 in every unused slot), request b's keys
+    occupy ceil(k_lens[b] / block_size) blocks drawn in a seeded random order
+    from num_blocks = needed + spare_blocks, block_table is int32 [B,
+    max_blocks + 1] with unused entries set to ``table_fill``, seq_lens int32
+    [B].  Tensors live on k's device.
+    """
+    gen = np.random.default_rng(seed)
+    need = [(int(n) + block_size - 1) // block_size for n in k_lens]
+    num_blocks = sum(need) + spare_blocks
+    perm = gen.permutation(num_blocks)
+    max_blocks = max(max(need), 1) + 1
+    table = np.full((len(k_lens), max_blocks), table_fill, dtype=np.int32)
+    hkv, d = k.shape[1], k.shape[2]
+    tg = torch.Generator(device="cpu").manual_seed(seed)
+    k_cache = torch.randn(num_blocks * block_size, hkv, d, generator=tg).to(torch.bfloat16)
+    v_cache = torch.randn(num_blocks * block_size, hkv, d, generator=tg).to(torch.bfloat16)
+    kc, vc = k.cpu(), v.cpu()
+    used, row = 0, 0
+    for b, n in enumerate(k_lens):
+        for i in range(need[b]):
+            blk = int(perm[used])
+            used += 1
+            table[b, i] = blk
+            m = min(block_size, int(n) - i * block_size)
+            k_cache[blk * block_size: blk * block_size + m] = kc[row + i * block_size: row + i * block_size + m]
+            v_cache[blk * block_size: blk * block_size + m] = vc[row + i * block_size: row + i * block_size + m]
+        row += int(n)
+    dev = k.device
+    return (k_cache.to(dev), v_cache.to(dev), torch.from_numpy(table).to(dev),
+            torch.tensor([int(n) for n in k_lens], dtype=torch.int32, device=dev))
+
+
 def scaled_workload(name: str, seed: int = 100) -> Workload:
     """Small versions of the workloads: same head layout, D, mask kind and
     sink mode, sequence lengths cut so the float64 oracle finishes in seconds

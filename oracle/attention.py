@@ -161,5 +161,27 @@ def attention_forward(q, k, v, cu_seqlens_q, cu_seqlens_k, causal, window_left,
     return out, lse
 
 
+def gather_paged(k_cache, v_cache, block_table, seq_lens, block_size):
+    """Packed ``(k, v, cu_seqlens_k)`` from a paged cache (float64 oracle view).
+
+    The paged layout of vLLM's paged attention, which the FA4 pages run their
+    masks on: key ``j`` of request ``b`` is row
+    ``block_table[b][j // block_size] * block_size + j % block_size`` of
+    ``k_cache`` / ``v_cache`` (``[num_blocks * block_size, Hkv, D]``).  The
+    paged forward pass is the packed forward pass of these gathered keys.
+    """
+    kc = np.asarray(_as_f64(k_cache))
+    vc = np.asarray(_as_f64(v_cache))
+    bt = np.asarray(block_table)
+    rows = []
+    for b, n in enumerate(np.asarray(seq_lens).tolist()):
+        for j in range(int(n)):
+            rows.append(int(bt[b, j // block_size]) * block_size + j % block_size)
+    idx = np.asarray(rows, dtype=np.int64)
+    cu = np.zeros(len(seq_lens) + 1, dtype=np.int64)
+    cu[1:] = np.cumsum(np.asarray(seq_lens, dtype=np.int64))
+    return kc[idx], vc[idx], cu
+
+
 def default_scale(head_dim: int) -> float:
     return 1.0 / math.sqrt(head_dim)

@@ -75,6 +75,32 @@ def test_argument_errors_return_before_any_launch(lib):
     assert _attn(lib, total_q=0) == mvp.MVP_OK  # nothing to do
 
 
+def _paged(lib, **over):
+    args = dict(q=1 << 20, kc=1 << 20, vc=1 << 20, out=1 << 20, lse=None, cu_q=1 << 20, seq_k=1 << 20,
+                bt=1 << 20, bs=16, max_blocks=4, num_blocks=8, ctx=None, num_reqs=1, total_q=4, max_q=4, max_k=64,
+                ndec=-1, hq=4, hkv=2, d=128, table=None, covered=None, causal=1, wl=-1, wr=-1, sinks=None,
+                sink_mode=0, scale=0.1, ws=None, ws_bytes=0, stream=None)
+    args.update(over)
+    return lib.mvp_attn_fwd_paged(*[args[k] for k in (
+        "q", "kc", "vc", "out", "lse", "cu_q", "seq_k", "bt", "bs", "max_blocks", "num_blocks", "ctx", "num_reqs",
+        "total_q", "max_q", "max_k", "ndec", "hq", "hkv", "d", "table", "covered", "causal", "wl", "wr", "sinks",
+        "sink_mode", "scale", "ws", "ws_bytes", "stream")])
+
+
+def test_paged_argument_errors(lib):
+    # Host validation of the block layout, before any CUDA call.
+    assert _paged(lib, bs=8) == mvp.MVP_ERR_ARG  # below 16
+    assert _paged(lib, bs=48) == mvp.MVP_ERR_ARG  # not a power of two
+    assert _paged(lib, bs=512) == mvp.MVP_ERR_ARG  # above 256
+    assert _paged(lib, max_blocks=3) == mvp.MVP_ERR_ARG  # 3 x 16 < max_k_len 64
+    assert _paged(lib, bt=None) == mvp.MVP_ERR_ARG
+    assert _paged(lib, seq_k=None) == mvp.MVP_ERR_ARG
+    assert _paged(lib, num_blocks=0) == mvp.MVP_ERR_ARG
+    assert _paged(lib, kc=(1 << 20) + 8) == mvp.MVP_ERR_UNSUPPORTED  # not 16-byte aligned
+    assert _paged(lib, d=96) == mvp.MVP_ERR_UNSUPPORTED
+    assert _paged(lib, total_q=0) == mvp.MVP_OK  # nothing to do
+
+
 def test_fill_argument_errors(lib):
     f = lib.mvp_fill_query_ranges
     assert f(None, 1, 1, 1 << 20, 1 << 20, 10, 1 << 20, 4, None, None) == mvp.MVP_ERR_ARG  # ranges null

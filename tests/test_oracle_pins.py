@@ -109,3 +109,28 @@ def test_workload_recipes():
             assert 64 <= e - s + 1 <= 320
     w = workloads.workload("mixed_serving_b")
     assert w.q_lens.count(1) == 256 and w.num_reqs == 260 and w.window_left == 4095
+
+
+def test_paged_gather_hand_example_and_round_trip():
+    """The paged view: key j of request b is row table[b][j // bs] * bs + j % bs.
+    A hand-worked table pins the index arithmetic; a generator round trip
+    (random block order, garbage in unused entries) must give back the packed
+    keys exactly."""
+    bs = 2
+    k_cache = torch.arange(8 * bs, dtype=torch.float32).reshape(8 * bs, 1, 1)
+    table = np.array([[3, 0, -1], [5, 1, 6]], dtype=np.int32)
+    k, v, cu = attention.gather_paged(k_cache, k_cache, table, [3, 5], bs)
+    # request 0: keys 0,1 in block 3 (rows 6,7), key 2 in block 0 (row 0)
+    # request 1: keys 0,1 block 5 (rows 10,11), keys 2,3 block 1 (rows 2,3), key 4 block 6 (row 12)
+    assert k[:, 0, 0].tolist() == [6, 7, 0, 10, 11, 2, 3, 12]
+    assert cu.tolist() == [0, 3, 8]
+    gen = torch.Generator().manual_seed(3)
+    lens = [5, 37, 1, 64]
+    kp = torch.randn(sum(lens), 2, 8, generator=gen).to(torch.bfloat16)
+    vp = torch.randn(sum(lens), 2, 8, generator=gen).to(torch.bfloat16)
+    for block in (16, 32):
+        kc, vc, bt, sl = workloads.to_paged(kp, vp, lens, block, seed=block, table_fill=99999)
+        k2, v2, cu2 = attention.gather_paged(kc, vc, bt.numpy(), sl.numpy(), block)
+        assert np.array_equal(k2, kp.to(torch.float64).numpy())
+        assert np.array_equal(v2, vp.to(torch.float64).numpy())
+        assert cu2.tolist() == [0, 5, 42, 43, 107]
