@@ -394,6 +394,10 @@ def run_gpu(args, world, rank, local):
     if n_dec > 0:
         nbytes = mvp.attn_workspace_size(n_dec, w.num_heads_q, w.head_dim, max_k)
         ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev) if nbytes else None
+    paged = None
+    if args.paged:
+        kc, vc, bt, sl = workloads.to_paged(k, v, w.k_lens, args.paged, seed=w.seed)
+        paged = dict(k_cache=kc, v_cache=vc, block_table=bt, seq_lens_k=sl)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     kw = dict(causal=w.causal, window_left=w.window_left, window_right=w.window_right, sinks=sinks,
@@ -408,7 +412,13 @@ def run_gpu(args, world, rank, local):
     def attn(lo=0, hi=None):
         """Attention over requests [lo, hi) of the batch (default: all)."""
         hi = w.num_reqs if hi is None else hi
-        if lo == 0 and hi == w.num_reqs:
+        if paged is not None:
+            nd = max(0, min(n_dec, hi) - lo)
+            mvp.attn_fwd_paged(q, paged["k_cache"], paged["v_cache"], out, cu_q[lo:hi + 1],
+                               paged["seq_lens_k"][lo:hi], paged["block_table"][lo:hi], args.paged,
+                               max(w.q_lens[lo:hi]), max(w.k_lens[lo:hi]), range_table=table,
+                               range_covered=covered, num_decode_reqs=nd, **kw)
+        elif lo == 0 and hi == w.num_reqs:
             mvp.attn_fwd_varlen(q, k, v, out, cu_q, cu_k, max_q, max_k, range_table=table,
                                 range_covered=covered, num_decode_reqs=n_dec, **kw)
         else:
@@ -507,7 +517,8 @@ def run_gpu(args, world, rank, local):
         achieved = pre_flops / pre_s / 1e12
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_t, "unit": "TFLOP/s",
                     "frac": achieved / peak_t,
-                    "traffic": load_traffic(os.path.join(kernel_dir, "attn_prefill.cu")),
+                    "traffic": (None if paged is not None
+                                else load_traffic(os.path.join(kernel_dir, "attn_prefill.cu"))),
                     "kernel": f"attn_prefill_kernel (D={w.head_dim})",
                     "peak_source": f"bf16_tflops (burst) of {peak_src}", "kernel_ms_per_launch": 1e3 * pre_s}
     else:
@@ -520,7 +531,9 @@ def run_gpu(args, world, rank, local):
     # ------------------------------------------------------------- e2e (host buffers)
     e2e = None
     if not args.no_e2e:
-        dev_in = [q, k, v, cu_q, cu_k] + ([seq_lens, ranges] if ranges is not None else []) + \
+        kv_in = [k, v, cu_k] if paged is None else [paged["k_cache"], paged["v_cache"], paged["block_table"],
+                                                     paged["seq_lens_k"]]
+        dev_in = [q, cu_q] + kv_in + ([seq_lens, ranges] if ranges is not None else []) + \
                  ([sinks] if sinks is not None else [])
         host_in = [t.cpu().pin_memory() for t in dev_in]
         host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
@@ -566,6 +579,8 @@ def run_gpu(args, world, rank, local):
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                 "config": {"workload": desc, "global_batch": w.num_reqs * world, "seq_len": max_q,
+                           "kv_layout": (f"paged, {args.paged}-token blocks in a seeded random order"
+                                         if args.paged else "packed"),
                            "l2": "flushed between steps (256 MiB write, outside the events)",
                            "parallelism": "replicas" if world > 1 else "single GPU"},
                 "pct_tensor_peak": 100.0 * value / peak_t, "tokens_per_s": tokens_per_s,
@@ -592,6 +607,9 @@ def main(argv=None):
     ap.add_argument("--cpu-rows-per-req", type=int, default=768)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--paged", type=int, default=0, metavar="BLOCK",
+                    help="run the workload on a paged K/V cache with this block size (blocks in a seeded random "
+                         "order; mvp_attn_fwd_paged) instead of packed K/V")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

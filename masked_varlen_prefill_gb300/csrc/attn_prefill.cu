@@ -87,7 +87,7 @@ struct Cfg {
   static constexpr int THREADS = 32 * WARPS;
   static constexpr int CONSUMER_WARPS = 2 + 4 * SPLIT + 4;  // warps that read the plan ring
   // Register split for 512 threads (128 each at launch): the softmax warps
-  // get 168, the epilogue and warpgroup 0 88 each (sum 4 x 128).
+  // get 168, warpgroup 0 and the epilogue 88 each (sum 4 x 128).
   static constexpr bool REG_SPLIT = SPLIT == 2;
   static constexpr int REGS_CTRL = 88;
   static constexpr int REGS_SOFTMAX = 168;
@@ -107,7 +107,15 @@ struct Cfg {
   // when they fit (the D = 512 tiles leave room for one).
   static constexpr int ROW_OFF = RED_OFF + RED_BYTES;
   static constexpr int EPI_SLOTS = (ROW_OFF + 2 * kBM * 8 + 1024 + 1024 <= 227 * 1024) ? 2 : 1;
-  static constexpr int SMEM_BYTES = ROW_OFF + EPI_SLOTS * kBM * 8 + 1024;  // + alignment slack
+  // Paged K/V: the producer warp caches the block ids of its current and next
+  // item here (two buffers of IDS_CAP ids): up to 2048 each, what fits (none
+  // at D = 512).
+  static constexpr int IDS_OFF = ROW_OFF + EPI_SLOTS * kBM * 8;
+  static constexpr int ids_cap(int cap) {
+    return cap < 64 ? 0 : (IDS_OFF + 2 * cap * 4 + 1024 + 1024 <= 227 * 1024 ? cap : ids_cap(cap / 2));
+  }
+  static constexpr int IDS_CAP = ids_cap(2048);
+  static constexpr int SMEM_BYTES = IDS_OFF + 2 * IDS_CAP * 4 + 1024;  // + alignment slack
   static constexpr int S_COL = 0;
   static constexpr int O_COL = 2 * BN;
   static constexpr int TMEM_COLS = 512;
@@ -378,39 +386,82 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
       };
       const int pos_off = rank * (kBM / p.gpack);  // this CTA's first position within an item
-      // L2 warming: Q tiles and first K / V tiles come from DRAM the first time
-      // they are read, with a latency several times a tile's MMA time.  The
-      // next item's Q and first kPrefetchAhead K / V tiles are prefetched while
-      // the current item runs, and every load prefetches the tile kPrefetchAhead
-      // steps further.  Each CTA of a pair warms its own half.
+      // L2 warming: an item's Q tile and first K / V tiles come from DRAM,
+      // with a latency several times a tile's MMA time, while its later tiles
+      // follow at the pace of the pipeline.  The next item's Q and (packed
+      // K / V) first kPrefetchAhead K / V tiles are prefetched while the
+      // current item runs; each CTA of a pair warms its own half.  Prefetching
+      // further tiles inside an item measured slower (extra TMA requests),
+      // and so did K / V prefetch for paged caches at every block size.
       constexpr int kPrefetchAhead = 2;
       // Paged K/V: loads go one block run at a time (box heights capped at the
-      // block size on the host), and the warming below is skipped.
-      constexpr bool paged = PAGED;
+      // block size on the host).
       const int kbox = PAGED ? min(C::KROWS, 1 << p.m.block_shift) : C::KROWS;
       const int vbox = PAGED ? min(BN, 1 << p.m.block_shift) : BN;
-      auto prefetch_k = [&](const PlanEntry& e, int j) {
-        const int krow = e.it.k0 + (e.pl.kb_lo + j) * BN + rank * C::KROWS;
-#pragma unroll
-        for (int c = 0; c < C::QCH; ++c) tma_prefetch_l2_3d(&map_k, c * 64, e.it.hkv, krow);
+      // Block ids of an item's key range, copied into shared memory by the
+      // whole warp (cp.async) while the item before it runs, so that the
+      // issuing lane never waits on a block-table load; buffer `buf` (items
+      // alternate) holds the ids of the blocks from the item's first one on.
+      int32_t* ids = reinterpret_cast<int32_t*>(smem + C::IDS_OFF);
+      int ids_plan = -1;  // plan whose ids are in flight into the other buffer
+      auto cache_ids = [&](const PlanEntry& e, int buf, bool wait) {
+        if constexpr (PAGED && C::IDS_CAP > 0) {
+          const int sh = p.m.block_shift;
+          const int fb = (e.pl.kb_lo * BN) >> sh;
+          const int last = e.it.k_len > 0 ? (e.it.k_len - 1) >> sh : 0;
+          const int nb = min((((e.pl.kb_lo + e.pl.n_tiles) * BN - 1) >> sh) - fb + 1, C::IDS_CAP);
+          const int32_t* row = p.m.block_table + static_cast<size_t>(e.it.b) * p.m.max_blocks;
+          for (int i = lane; i < nb; i += 32) cp_async_4(ids + buf * C::IDS_CAP + i, row + min(fb + i, last));
+          cp_async_commit();
+          if (wait) {
+            cp_async_wait_all();
+            __syncwarp();
+          }
+        }
       };
-      auto prefetch_v = [&](const PlanEntry& e, int j) {
-        const int krow = e.it.k0 + (e.pl.kb_lo + j) * BN;
+      // Cache row of key `key` of item e (packed: the packed row).
+      auto row_of = [&](const PlanEntry& e, int buf, int key) -> int {
+        if constexpr (PAGED) {
+          if constexpr (C::IDS_CAP > 0) {
+            const int sh = p.m.block_shift;
+            const int last = e.it.k_len > 0 ? (e.it.k_len - 1) >> sh : 0;
+            const int idx = min(key >> sh, last) - ((e.pl.kb_lo * BN) >> sh);
+            if (static_cast<unsigned>(idx) < static_cast<unsigned>(C::IDS_CAP))
+              return static_cast<int>((static_cast<unsigned>(ids[buf * C::IDS_CAP + idx]) << sh) +
+                                      static_cast<unsigned>(key & ((1 << sh) - 1)));
+          }
+          return kv_row(p.m, e.it.b, e.it.k0, e.it.k_len, key);
+        } else {
+          return e.it.k0 + key;
+        }
+      };
+      int cbuf = 0;  // ids buffer of the current item
+      auto prefetch_kv = [&](const PlanEntry& e, int j) {  // packed K / V only
+        const int key0 = e.it.k0 + (e.pl.kb_lo + j) * BN;
 #pragma unroll
-        for (int c = 0; c < C::VCH; ++c) tma_prefetch_l2_3d(&map_v, e.it.dv0 + rank * C::DVC + c * 64, e.it.hkv, krow);
+        for (int c = 0; c < C::QCH; ++c) tma_prefetch_l2_3d(&map_k, c * 64, e.it.hkv, key0 + rank * C::KROWS);
+#pragma unroll
+        for (int c = 0; c < C::VCH; ++c)
+          tma_prefetch_l2_3d(&map_v, e.it.dv0 + rank * C::DVC + c * 64, e.it.hkv, key0);
       };
       // Plan n (the next one to consume) if the scheduler has published it;
-      // never waits.  The slot cannot be reused before this warp consumes it.
+      // never waits (warp-collective: every lane observes the plan itself).
+      // The slot cannot be reused before this warp consumes it.  Paged: the
+      // plan's block ids start on their way into the other ids buffer, whose
+      // item issued its last load before the warp's last sync.
       auto prefetch_next_item = [&]() {
         const int slot = n % kPlanRing;
-        if (!mbar_try_wait(&sb.plan_full[slot], (n / kPlanRing) & 1)) return;
+        if (!__all_sync(kFullMask, mbar_try_wait(&sb.plan_full[slot], (n / kPlanRing) & 1))) return;
         const PlanEntry e = sb.plans[slot];
         if (e.last || e.pl.n_tiles == 0) return;
+        if (lane == 0) {
 #pragma unroll
-        for (int c = 0; c < C::QCH; ++c) tma_prefetch_l2_3d(&map_q, c * 64, e.it.h0, e.it.q0 + e.it.pos0 + pos_off);
-        for (int j = 0; !paged && j < kPrefetchAhead && j < e.pl.n_tiles; ++j) {
-          prefetch_k(e, j);
-          prefetch_v(e, j);
+          for (int c = 0; c < C::QCH; ++c) tma_prefetch_l2_3d(&map_q, c * 64, e.it.h0, e.it.q0 + e.it.pos0 + pos_off);
+          for (int j = 0; !PAGED && j < kPrefetchAhead && j < e.pl.n_tiles; ++j) prefetch_kv(e, j);
+        }
+        if constexpr (PAGED) {
+          cache_ids(e, cbuf ^ 1, false);
+          ids_plan = n;
         }
       };
       auto load_q = [&](const PlanEntry& e) -> bool {
@@ -431,7 +482,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         ++qn;
         return true;
       };
-      auto load_k = [&](const PlanEntry& e, int j) -> bool {
+      auto load_k = [&](const PlanEntry& e, int j, int buf) -> bool {
         const int s = kc % C::KST;
         if (kc >= C::KST) {
           const int tp = kc - C::KST;  // the tile that used this stage before
@@ -443,9 +494,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (leader) mbar_arrive_expect_tx(&sb.k_full[s], C::NCTA * C::K_BYTES);
         const int key0 = (e.pl.kb_lo + j) * BN + rank * C::KROWS;  // this CTA's first key of the tile
         if constexpr (PAGED) {
-          // one box per run of K rows inside one cache block
+          // one box per run of K rows inside one cache block (a rolled loop:
+          // the producer's code stays small next to the other roles')
+#pragma unroll 1
           for (int r = 0; r < C::KROWS; r += kbox) {
-            const int krow = kv_row(p.m, e.it.b, e.it.k0, e.it.k_len, key0 + r);
+            const int krow = row_of(e, buf, key0 + r);
 #pragma unroll
             for (int c = 0; c < C::QCH; ++c)
               tma_load<C>(sK + s * C::K_BYTES + c * (C::KROWS * 128) + r * 128, &map_k, &sb.k_full[s], c * 64,
@@ -457,12 +510,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             tma_load<C>(sK + s * C::K_BYTES + c * (C::KROWS * 128), &map_k, &sb.k_full[s], c * 64, e.it.hkv,
                         e.it.k0 + key0);
         }
-        if (!paged && j + kPrefetchAhead < e.pl.n_tiles) prefetch_k(e, j + kPrefetchAhead);
         ++k_armed[s];
         ++kc;
         return true;
       };
-      auto load_v = [&](const PlanEntry& e, int j) -> bool {
+      auto load_v = [&](const PlanEntry& e, int j, int buf) -> bool {
         const int s = vc % C::VST;
         if (vc >= C::VST) {
           const int tp = vc - C::VST;
@@ -474,8 +526,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (leader) mbar_arrive_expect_tx(&sb.v_full[s], C::NCTA * C::V_BYTES);
         const int key0 = (e.pl.kb_lo + j) * BN;
         if constexpr (PAGED) {
+#pragma unroll 1
           for (int r = 0; r < BN; r += vbox) {
-            const int vrow = kv_row(p.m, e.it.b, e.it.k0, e.it.k_len, key0 + r);
+            const int vrow = row_of(e, buf, key0 + r);
 #pragma unroll
             for (int c = 0; c < C::VCH; ++c)
               tma_load<C>(sV + s * C::V_BYTES + c * (BN * 128) + r * 128, &map_v, &sb.v_full[s],
@@ -487,34 +540,45 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             tma_load<C>(sV + s * C::V_BYTES + c * (BN * 128), &map_v, &sb.v_full[s], e.it.dv0 + rank * C::DVC + c * 64,
                         e.it.hkv, e.it.k0 + key0);
         }
-        if (!paged && j + kPrefetchAhead < e.pl.n_tiles) prefetch_v(e, j + kPrefetchAhead);
         ++v_armed[s];
         ++vc;
         return true;
       };
       PlanEntry cur;
       bool have = next_item(cur);
-      if (have && lane == 0) ok = load_q(cur) && load_k(cur, 0);
+      if (have) cache_ids(cur, cbuf, true);
+      if (have && lane == 0) ok = load_q(cur) && load_k(cur, 0, cbuf);
       ok = __shfl_sync(kFullMask, ok, 0);
       while (ok && have) {
         const int nt = cur.pl.n_tiles;
-        if (lane == 0) prefetch_next_item();
+        prefetch_next_item();
         if (lane == 0)
           for (int j = 0; ok && j + 1 < nt; ++j) {
-            ok = load_k(cur, j + 1);
-            if (ok) ok = load_v(cur, j);
+            ok = load_k(cur, j + 1, cbuf);
+            if (ok) ok = load_v(cur, j, cbuf);
           }
         ok = __shfl_sync(kFullMask, ok, 0);
         PlanEntry nxt;
         const bool have_next = ok && next_item(nxt);
+        if (PAGED && have_next) {
+          if (ids_plan == n - 1) {  // prefetched while the current item ran
+            cp_async_wait_all();
+            __syncwarp();
+          } else {
+            cache_ids(nxt, cbuf ^ 1, true);
+          }
+        }
+        ids_plan = -1;
         if (lane == 0 && ok) {
-          if (have_next) ok = load_q(nxt) && load_k(nxt, 0);
-          if (ok) ok = load_v(cur, nt - 1);
+          if (have_next) ok = load_q(nxt) && load_k(nxt, 0, cbuf ^ 1);
+          if (ok) ok = load_v(cur, nt - 1, cbuf);
         }
         ok = __shfl_sync(kFullMask, ok, 0);
         cur = nxt;
         have = have_next;
+        cbuf ^= 1;
       }
+      if constexpr (PAGED) cp_async_wait_all();  // block ids still in flight
       // Drain: never leave the CTA with a TMA write still in flight.  Each
       // full barrier's last armed phase is waited for, ignoring the CTA abort
       // flag (issued copies always complete, and must before the CTA exits).

@@ -204,35 +204,41 @@ def to_paged(k, v, k_lens, block_size: int, seed: int = 0, spare_blocks: int = 3
 
     k, v: [total_k, Hkv, D] packed by request (k_lens[b] rows each).  Returns
     (k_cache, v_cache, block_table, seq_lens): the caches are [num_blocks *
-    block_size, Hkv, D] (random bf16 in every unused slot), request b's keys
+    block_size, Hkv, D] (random bf16 in the unused slots of a small cache,
+    zeros in a large one), request b's keys
     occupy ceil(k_lens[b] / block_size) blocks drawn in a seeded random order
     from num_blocks = needed + spare_blocks, block_table is int32 [B,
     max_blocks + 1] with unused entries set to ``table_fill``, seq_lens int32
     [B].  Tensors live on k's device.
     """
     gen = np.random.default_rng(seed)
-    need = [(int(n) + block_size - 1) // block_size for n in k_lens]
-    num_blocks = sum(need) + spare_blocks
-    perm = gen.permutation(num_blocks)
-    max_blocks = max(max(need), 1) + 1
-    table = np.full((len(k_lens), max_blocks), table_fill, dtype=np.int32)
-    hkv, d = k.shape[1], k.shape[2]
-    tg = torch.Generator(device="cpu").manual_seed(seed)
-    k_cache = torch.randn(num_blocks * block_size, hkv, d, generator=tg).to(torch.bfloat16)
-    v_cache = torch.randn(num_blocks * block_size, hkv, d, generator=tg).to(torch.bfloat16)
-    kc, vc = k.cpu(), v.cpu()
-    used, row = 0, 0
-    for b, n in enumerate(k_lens):
-        for i in range(need[b]):
-            blk = int(perm[used])
-            used += 1
-            table[b, i] = blk
-            m = min(block_size, int(n) - i * block_size)
-            k_cache[blk * block_size: blk * block_size + m] = kc[row + i * block_size: row + i * block_size + m]
-            v_cache[blk * block_size: blk * block_size + m] = vc[row + i * block_size: row + i * block_size + m]
-        row += int(n)
+    lens = np.asarray([int(n) for n in k_lens], dtype=np.int64)
+    need = (lens + block_size - 1) // block_size
+    num_blocks = int(need.sum()) + spare_blocks
+    perm = gen.permutation(num_blocks).astype(np.int64)
+    max_blocks = max(int(need.max()) if len(need) else 1, 1) + 1
+    table = np.full((len(lens), max_blocks), table_fill, dtype=np.int32)
+    first = np.concatenate([[0], np.cumsum(need)[:-1]]) if len(need) else np.zeros(0, dtype=np.int64)
+    rows = []
+    for b in range(len(lens)):
+        ids = perm[first[b]: first[b] + need[b]]
+        table[b, :need[b]] = ids
+        j = np.arange(lens[b], dtype=np.int64)
+        rows.append(ids[j // block_size] * block_size + j % block_size)
     dev = k.device
-    return (k_cache.to(dev), v_cache.to(dev), torch.from_numpy(table).to(dev),
+    idx = torch.from_numpy(np.concatenate(rows) if rows else np.zeros(0, dtype=np.int64)).to(dev)
+    hkv, d = k.shape[1], k.shape[2]
+    n_rows = num_blocks * block_size
+    if n_rows * hkv * d <= (1 << 24):  # small caches: random filler in the unused slots
+        tg = torch.Generator(device="cpu").manual_seed(seed)
+        k_cache = torch.randn(n_rows, hkv, d, generator=tg).to(torch.bfloat16).to(dev)
+        v_cache = torch.randn(n_rows, hkv, d, generator=tg).to(torch.bfloat16).to(dev)
+    else:
+        k_cache = torch.zeros(n_rows, hkv, d, dtype=torch.bfloat16, device=dev)
+        v_cache = torch.zeros(n_rows, hkv, d, dtype=torch.bfloat16, device=dev)
+    k_cache[idx] = k
+    v_cache[idx] = v
+    return (k_cache, v_cache, torch.from_numpy(table).to(dev),
             torch.tensor([int(n) for n in k_lens], dtype=torch.int32, device=dev))
 
 
