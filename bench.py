@@ -95,9 +95,17 @@ def visible_counts_per_row(w, table):
     return counts
 
 
+KERNEL_HEADERS = ("mask.cuh", "mvp_internal.cuh", "ptx.cuh")
+
+
 def source_hash(path):
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """sha256 (first 16 hex digits) of a kernel's translation unit followed by
+    the headers it includes from the same folder, in KERNEL_HEADERS order."""
+    h = hashlib.sha256()
+    for p in (path,) + tuple(os.path.join(os.path.dirname(path), n) for n in KERNEL_HEADERS):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def load_traffic(kernel_src):
@@ -357,6 +365,94 @@ def _leading_decode(w):
     return n
 
 
+def graph_measure(args, w, q, k, v, sinks, flops, flush, stream, dev):
+    """The same step through the step-metadata path (StepMetadata: host
+    staging, one copy, the table fill) and attention sized for a capacity of
+    ``args.graph`` x the batch (requests, rows, q / k length bounds), once
+    captured in a CUDA graph and replayed, once launched eagerly.  The staging
+    (host) happens before each step's start event; wall times include it."""
+    import torch
+
+    import masked_varlen_prefill_gb300 as mvp
+
+    f = float(args.graph)
+    cap_r = math.ceil(w.num_reqs * f)
+    cap_t = math.ceil(w.total_q * f)
+    max_q = math.ceil(max(w.q_lens) * f)
+    max_k = math.ceil(max(w.k_lens) * f)
+    n_ranges = 0 if w.ranges is None else w.ranges.shape[1]
+    meta = mvp.StepMetadata(cap_r, cap_t, n_ranges, dev)
+    qsl, _ = w.cu_seqlens()
+    k_lens = np.asarray(w.k_lens, np.int32)
+    qc = torch.zeros(cap_t, w.num_heads_q, w.head_dim, dtype=q.dtype, device=dev)
+    qc[:w.total_q].copy_(q)
+    outs = [torch.zeros_like(qc) for _ in range(2)]
+    nbytes = mvp.attn_workspace_size(cap_r, w.num_heads_q, w.head_dim, max_k)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+    kw = dict(causal=w.causal, window_left=w.window_left, window_right=w.window_right, sinks=sinks,
+              sink_mode=w.sink_mode, scale=w.scale, workspace=ws)
+
+    def attention(o):
+        mvp.attn_fwd_varlen(qc, k, v, o, meta.query_start_loc, meta.cu_seqlens_k, max_q, max_k,
+                            range_table=meta.range_table if n_ranges else None,
+                            range_covered=meta.range_covered if n_ranges else None, **kw)
+        return mvp.last_launch_count()
+
+    def stage():
+        meta.stage(qsl, k_lens, None, w.ranges)
+
+    stage()
+    meta.upload()
+    n_attn = attention(outs[1])
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        meta.upload()
+        attention(outs[0])
+    torch.cuda.synchronize()
+    per_step = 1 + n_attn  # the fill kernel + the attention kernels
+
+    def timed(run):
+        for _ in range(args.warmup):
+            flush.zero_()
+            stage()
+            run()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        wall = 0.0
+        for a, b in ev:
+            flush.zero_()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            stage()
+            a.record(stream)
+            run()
+            b.record(stream)
+            torch.cuda.synchronize()
+            wall += time.perf_counter() - t0
+        return sum(a.elapsed_time(b) for a, b in ev) / len(ev), 1e3 * wall / len(ev)
+
+    g_ms, g_wall = timed(g.replay)
+
+    def eager():
+        meta.upload()
+        attention(outs[1])
+
+    e_ms, e_wall = timed(eager)
+    same = bool(torch.equal(outs[0][:w.total_q].view(torch.int16), outs[1][:w.total_q].view(torch.int16)))
+    if mvp.get_last_device_error() != 0:
+        raise RuntimeError("device timeout during graph replays")
+    meta.close()
+    return {"capacity_factor": f, "max_reqs": cap_r, "max_tokens": cap_t, "max_q_len": max_q, "max_k_len": max_k,
+            "kernels_per_step": per_step, "value": flops / (g_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+            "graph_ms_per_step": g_ms, "graph_wall_ms_per_step": g_wall,
+            "eager_ms_per_step": e_ms, "eager_wall_ms_per_step": e_wall,
+            "out_bitwise_equal_to_eager": same,
+            "timing": "device events around the replay (or eager launches); wall clock from before the host "
+                      "staging to after a synchronize"}
+
+
 def run_gpu(args, world, rank, local):
     import torch
 
@@ -563,6 +659,11 @@ def run_gpu(args, world, rank, local):
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": args.e2e_steps,
                "ms_per_step": 1e3 * e2e_s / args.e2e_steps}
 
+    # ------------------------------------------------------------- graph replays
+    graph = None
+    if args.graph is not None:
+        graph = graph_measure(args, w, q, k, v, sinks, flops, flush, stream, dev)
+
     # ------------------------------------------------------------- CPU baseline
     cpu_baseline = None
     if pool is not None:
@@ -587,6 +688,8 @@ def run_gpu(args, world, rank, local):
                 "visible_entries_per_step": visible, "sub_batches": sub,
                 "roofline": roofline, "cpu_baseline": cpu_baseline, "e2e": e2e,
                 "gpu_launches": launches, "clocks": sampler.summary()}
+        if graph is not None:
+            line["graph"] = graph
         print(json.dumps(line))
     if world > 1:
         import torch.distributed as dist
@@ -607,12 +710,17 @@ def main(argv=None):
     ap.add_argument("--cpu-rows-per-req", type=int, default=768)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--graph", type=float, default=None, metavar="CAPACITY",
+                    help="also run the step through the step-metadata path, captured in a CUDA graph sized for "
+                         "CAPACITY x the batch (>= 1), and eagerly; adds a 'graph' object to the line")
     ap.add_argument("--paged", type=int, default=0, metavar="BLOCK",
                     help="run the workload on a paged K/V cache with this block size (blocks in a seeded random "
                          "order; mvp_attn_fwd_paged) instead of packed K/V")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.graph is not None and (args.graph < 1.0 or args.paged):
+        ap.error("--graph takes a capacity factor >= 1 and a packed K/V layout")
     world, rank, local = dist_setup()
     if args.impl == "reference":
         return run_reference(args, world, rank)

@@ -69,8 +69,10 @@ typedef enum {
  * seq_lens        int32 [num_reqs], total key length of each request; the
  *                 request's first scheduled query sits at absolute position
  *                 seq_lens[b] - (query_start_loc[b+1] - query_start_loc[b]).
- * num_tokens      host int, == query_start_loc[num_reqs] (the caller knows it
- *                 on the host, as the page's builder does).
+ * num_tokens      host int, normally query_start_loc[num_reqs] (the caller
+ *                 knows it on the host, as the page's builder does); rows at
+ *                 or past query_start_loc[num_reqs] (a batch padded to a
+ *                 fixed capacity) are written as (-1, -1).
  * out             int32 [out_capacity, 2]: rows [0, num_tokens) are ALL
  *                 written: (start, end) of the range holding the row's
  *                 absolute position, clipped to nothing (the range itself is
@@ -217,6 +219,93 @@ int mvp_attn_fwd_varlen_static_ws(const void* q, const void* k, const void* v, v
 
 /* Size in bytes of the fixed scratch array used by mvp_attn_fwd_varlen_static_ws. */
 size_t mvp_static_scratch_bytes(void);
+
+/*
+ * Step metadata for CUDA-graph replays.  Source: vLLM PR #50294 review,
+ * "Implementation breakdown" step 3 (FlashAttentionMetadataBuilder): a pinned
+ * host staging area and a persistent device buffer are allocated once for
+ * the largest batch; each step fills the staging area on the host from the
+ * query offsets and an upper bound of the sequence lengths, then copies it to
+ * the device without blocking.  The optimistic bound places a decode row at
+ * or past its true position, which keeps it outside every range (ranges hold
+ * prompt tokens; a decoded token never lies in one).
+ *
+ * One "metadata block" (int32, mvp_meta_block_bytes bytes, identical layout
+ * on host and device) holds, at the element offsets mvp_meta_offsets gives:
+ *   [0] query_start_loc  [max_reqs + 1]   (cu_seqlens_q of the attention)
+ *   [1] seq_lens_k       [max_reqs]       (exact key lengths: the paged call)
+ *   [2] cu_seqlens_k     [max_reqs + 1]   (prefix sums of [1]: the packed call)
+ *   [3] seq_lens_bound   [max_reqs]       (the fill's key lengths)
+ *   [4] ranges           [max_reqs, max_ranges, 2]  (8-byte aligned)
+ * A batch of num_reqs <= max_reqs requests and query_start_loc[num_reqs] <=
+ * max_tokens rows is padded to the capacity with requests that have no rows,
+ * no keys and no ranges, so every step is the same two operations (one copy
+ * of the whole block, one fill of max_tokens table rows) on the same
+ * pointers, whatever the batch: capture them, and an attention call on the
+ * block's arrays sized for the capacity (num_reqs = max_reqs, total_q =
+ * max_tokens, max_q_len / max_k_len upper bounds), in one CUDA graph and
+ * replay it for every batch that fits.
+ */
+typedef struct mvp_meta mvp_meta;
+
+/* Bytes of a metadata block for this capacity (0 for max_reqs outside
+ * [1, 65535] or max_ranges outside [0, 4096]). */
+size_t mvp_meta_block_bytes(int max_reqs, int max_ranges);
+
+/* Element offsets of the five arrays of a block into offsets[0..4]. */
+int mvp_meta_offsets(int max_reqs, int max_ranges, size_t* offsets);
+
+/*
+ * Host only (no CUDA call): writes the padded block for one batch into
+ * `block` (host memory of mvp_meta_block_bytes bytes).  All inputs are HOST
+ * arrays:
+ *   query_start_loc [num_reqs + 1], starting at 0, non-decreasing;
+ *   seq_lens_k      [num_reqs] exact key lengths, or NULL (then [1] and [2]
+ *                   hold zeros and the caller supplies its own);
+ *   seq_lens_bound  [num_reqs] the fill's lengths (>= the exact ones; a
+ *                   prefill row needs the exact value, a decode row may take
+ *                   an upper bound), or NULL to use seq_lens_k;
+ *   ranges          [num_reqs, num_ranges, 2] as for mvp_fill_query_ranges,
+ *                   or NULL (no ranges).
+ * Errors (nothing written): MVP_ERR_ARG for NULL inputs a batch needs, a
+ * query_start_loc that does not start at 0 or decreases, a key length below
+ * the request's query count, keys summing past INT_MAX; MVP_ERR_CAPACITY for
+ * num_reqs > max_reqs, num_ranges > max_ranges or more than max_tokens rows.
+ */
+int mvp_meta_pack(const int32_t* query_start_loc, const int32_t* seq_lens_k, const int32_t* seq_lens_bound,
+                  const int32_t* ranges, int num_reqs, int num_ranges, int max_reqs, int max_tokens,
+                  int max_ranges, int32_t* block);
+
+/*
+ * Creates a builder on the current device.  The caller owns and keeps alive
+ * the device arrays: device_block (mvp_meta_block_bytes, 16-byte aligned),
+ * range_table (int32 [max_tokens, 2], 8-byte aligned) and range_covered
+ * (int32 scalar).  The builder allocates its pinned staging block here and
+ * nothing afterwards; the staged batch starts empty.
+ * Errors: MVP_ERR_ARG, MVP_ERR_UNSUPPORTED (alignment), MVP_ERR_CUDA.
+ */
+int mvp_meta_create(int max_reqs, int max_tokens, int max_ranges, int32_t* device_block, int32_t* range_table,
+                    int32_t* range_covered, mvp_meta** out);
+
+/* Waits for the builder's last copy and frees its staging block and event. */
+int mvp_meta_destroy(mvp_meta* meta);
+
+/*
+ * Host step: waits until the last upload's copy (eager or replayed from a
+ * graph) has read the staging block, then packs this batch into it
+ * (mvp_meta_pack's arguments and errors).  Not a stream operation: call it
+ * outside any capture.
+ */
+int mvp_meta_stage(mvp_meta* meta, const int32_t* query_start_loc, const int32_t* seq_lens_k,
+                   const int32_t* seq_lens_bound, const int32_t* ranges, int num_reqs, int num_ranges);
+
+/*
+ * Stream step (capturable): one asynchronous copy of the staged block into
+ * device_block, an event marking the staging block free, and the range-table
+ * fill over the block (max_reqs requests, max_tokens rows) into range_table
+ * and range_covered.  Two kernel-side operations and no allocation.
+ */
+int mvp_meta_upload(mvp_meta* meta, void* stream);
 
 /* Synchronises `stream`, returns MVP_ERR_DEVICE_TIMEOUT if a kernel recorded a
  * timeout since the last call (and clears it), MVP_ERR_CUDA on a CUDA error,

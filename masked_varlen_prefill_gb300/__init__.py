@@ -19,6 +19,7 @@ from ._lib import (  # noqa: F401
     SINK_NONE,
     SINK_NULL_LOGIT,
     MvpError,
+    StepMetadata,
     attn_fwd_varlen,
     attn_fwd_paged,
     attn_fwd_varlen_host,
@@ -29,4 +30,6 @@ from ._lib import (  # noqa: F401
     last_launch_count,
     library_path,
     load_library,
+    meta_block_layout,
+    meta_pack,
 )

@@ -6,6 +6,7 @@ import ctypes
 import os
 import threading
 
+import numpy as np
 import torch
 
 MVP_OK = 0
@@ -42,6 +43,13 @@ _SIGNATURES = {
     "mvp_get_last_device_error": (_i, [_vp]),
     "mvp_status_str": (ctypes.c_char_p, [_i]),
     "mvp_last_launch_count": (_i, []),
+    "mvp_meta_block_bytes": (_sz, [_i, _i]),
+    "mvp_meta_offsets": (_i, [_i, _i, ctypes.POINTER(_sz)]),
+    "mvp_meta_pack": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]),
+    "mvp_meta_create": (_i, [_i, _i, _i, _vp, _vp, _vp, ctypes.POINTER(_vp)]),
+    "mvp_meta_destroy": (_i, [_vp]),
+    "mvp_meta_stage": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i]),
+    "mvp_meta_upload": (_i, [_vp, _vp]),
 }
 
 
@@ -272,3 +280,121 @@ def get_last_device_error(stream=None) -> int:
 
 def last_launch_count() -> int:
     return int(load_library().mvp_last_launch_count())
+
+
+# ------------------------------------------------------------ step metadata
+def _host_i32(a, name, shape=None):
+    """Contiguous host int32 numpy array (or None) and its pointer."""
+    if a is None:
+        return None, None
+    if isinstance(a, torch.Tensor):
+        if a.is_cuda:
+            raise ValueError(f"{name} must be a host array")
+        a = a.numpy()
+    a = np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+    if shape is not None and a.shape != shape:
+        raise ValueError(f"{name} must have shape {shape}, got {a.shape}")
+    return a, ctypes.c_void_p(a.ctypes.data)
+
+
+def _meta_args(query_start_loc, seq_lens_k, seq_lens_bound, ranges):
+    qsl, p_qsl = _host_i32(query_start_loc, "query_start_loc")
+    if qsl is None or qsl.ndim != 1 or qsl.shape[0] < 1:
+        raise ValueError("query_start_loc must be a 1-D host array of num_reqs + 1 offsets")
+    n = qsl.shape[0] - 1
+    sk, p_sk = _host_i32(seq_lens_k, "seq_lens_k", (n,))
+    sb, p_sb = _host_i32(seq_lens_bound, "seq_lens_bound", (n,))
+    rg, p_rg = _host_i32(ranges, "ranges")
+    if rg is not None and (rg.ndim != 3 or rg.shape[0] != n or rg.shape[2] != 2):
+        raise ValueError("ranges must be [num_reqs, num_ranges, 2]")
+    keep = (qsl, sk, sb, rg)  # the arrays must outlive the call
+    return keep, (p_qsl, p_sk, p_sb, p_rg, n, 0 if rg is None else rg.shape[1])
+
+
+def meta_block_layout(max_reqs, max_ranges):
+    """(bytes, element offsets of query_start_loc, seq_lens_k, cu_seqlens_k,
+    seq_lens_bound, ranges) of a metadata block (``mvp_meta_offsets``)."""
+    lib = load_library()
+    nbytes = int(lib.mvp_meta_block_bytes(max_reqs, max_ranges))
+    offs = (_sz * 5)()
+    st = lib.mvp_meta_offsets(max_reqs, max_ranges, offs)
+    if st != MVP_OK:
+        raise MvpError("mvp_meta_offsets", st)
+    return nbytes, tuple(int(x) for x in offs)
+
+
+def meta_pack(query_start_loc, seq_lens_k, seq_lens_bound, ranges, max_reqs, max_tokens, max_ranges):
+    """Padded metadata block of one batch (``mvp_meta_pack``; host only, no
+    GPU needed).  Returns an int32 numpy array."""
+    lib = load_library()
+    nbytes, _ = meta_block_layout(max_reqs, max_ranges)
+    block = np.zeros(nbytes // 4, dtype=np.int32)
+    keep, (p_qsl, p_sk, p_sb, p_rg, n, nr) = _meta_args(query_start_loc, seq_lens_k, seq_lens_bound, ranges)
+    st = lib.mvp_meta_pack(p_qsl, p_sk, p_sb, p_rg, n, nr, max_reqs, max_tokens, max_ranges,
+                           ctypes.c_void_p(block.ctypes.data))
+    del keep
+    if st != MVP_OK:
+        raise MvpError("mvp_meta_pack", st)
+    return block
+
+
+class StepMetadata:
+    """Persistent step metadata for CUDA-graph replays (``mvp_meta_*``).
+
+    Owns the device block, the range table and the covered flag as torch
+    tensors whose addresses never change; ``stage`` packs a batch on the host
+    into the library's pinned staging block, ``upload`` enqueues the copy and
+    the table fill on a stream (capturable).  The views ``query_start_loc``,
+    ``seq_lens_k``, ``cu_seqlens_k``, ``range_table`` and ``range_covered``
+    are what an attention call captured with them reads."""
+
+    def __init__(self, max_reqs, max_tokens, max_ranges, device=None):
+        lib = load_library()
+        device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+        self.max_reqs, self.max_tokens, self.max_ranges = int(max_reqs), int(max_tokens), int(max_ranges)
+        nbytes, offs = meta_block_layout(self.max_reqs, self.max_ranges)
+        if nbytes == 0:
+            raise ValueError("capacity out of range")
+        self.device = device
+        self.block = torch.zeros(nbytes // 4, dtype=torch.int32, device=device)
+        self.range_table = torch.full((self.max_tokens, 2), -1, dtype=torch.int32, device=device)
+        self.range_covered = torch.zeros(1, dtype=torch.int32, device=device)
+        r = self.max_reqs
+        self.query_start_loc = self.block[offs[0]:offs[0] + r + 1]
+        self.seq_lens_k = self.block[offs[1]:offs[1] + r]
+        self.cu_seqlens_k = self.block[offs[2]:offs[2] + r + 1]
+        self.seq_lens_bound = self.block[offs[3]:offs[3] + r]
+        self.ranges = self.block[offs[4]:offs[4] + r * self.max_ranges * 2].view(r, self.max_ranges, 2)
+        handle = _vp()
+        with torch.cuda.device(device):
+            st = lib.mvp_meta_create(self.max_reqs, self.max_tokens, self.max_ranges, _ptr(self.block),
+                                     _ptr(self.range_table), _ptr(self.range_covered), ctypes.byref(handle))
+        if st != MVP_OK:
+            raise MvpError("mvp_meta_create", st)
+        self._handle = handle
+
+    def stage(self, query_start_loc, seq_lens_k, seq_lens_bound=None, ranges=None):
+        """Pack one batch (host arrays) into the staging block."""
+        keep, (p_qsl, p_sk, p_sb, p_rg, n, nr) = _meta_args(query_start_loc, seq_lens_k, seq_lens_bound, ranges)
+        st = load_library().mvp_meta_stage(self._handle, p_qsl, p_sk, p_sb, p_rg, n, nr)
+        del keep
+        if st != MVP_OK:
+            raise MvpError("mvp_meta_stage", st)
+
+    def upload(self, stream=None):
+        """Copy the staged block to the device and fill the range table."""
+        st = load_library().mvp_meta_upload(self._handle, _stream(stream, self.device))
+        if st != MVP_OK:
+            raise MvpError("mvp_meta_upload", st)
+
+    def close(self):
+        if getattr(self, "_handle", None) is not None and self._handle.value is not None:
+            load_library().mvp_meta_destroy(self._handle)
+            self._handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+

@@ -208,6 +208,47 @@ __device__ __forceinline__ Item item_geometry(int item, const PrefillParams& p) 
   return it;
 }
 
+// The scheduler's next item index after an invalid item `item` (geometry
+// `it`), in its static-stride class (item mod stride): the first item of
+// this (request, head) block whose q tile has rows, or, when the request has
+// no prefill rows at all, the first item of the next request that has (32
+// requests tested per step by the warp).  Item spaces sized for a capacity
+// (upper-bound q lengths, padding requests) then cost O(requests) per CTA,
+// not O(items).  Warp-collective; returns INT_MAX past the last item.
+template <class C>
+__device__ __forceinline__ int next_candidate(int item, const Item& it, const PrefillParams& p, int stride,
+                                              int lane) {
+  const int nz = p.hkv * p.n_hgroups * C::DV_SPLIT;
+  const long long per_req = static_cast<long long>(nz) * p.n_qtiles;
+  const int prows = C::ITEM_ROWS / p.gpack;  // query positions per item
+  long long target;
+  if (it.q_len > 0 && !(p.skip_decode && it.q_len == 1)) {
+    const int x_min = p.n_qtiles - (it.q_len + prows - 1) / prows;  // first x with pos0 < q_len
+    target = static_cast<long long>(item / p.n_qtiles) * p.n_qtiles + x_min;
+    if (target <= item) target = item + 1;  // (rows past max_q_len: not computed)
+  } else {
+    int b = it.b + 1;
+    for (;;) {
+      if (b >= p.num_reqs) return INT_MAX;
+      const int c = b + lane;
+      bool good = false;
+      if (c < p.num_reqs) {
+        const int ql = __ldg(p.m.cu_q + c + 1) - __ldg(p.m.cu_q + c);
+        good = ql > 0 && !(p.skip_decode && ql == 1);
+      }
+      const unsigned m = __ballot_sync(kFullMask, good);
+      if (m != 0u) {
+        b += __ffs(m) - 1;
+        break;
+      }
+      b += 32;
+    }
+    target = (b - p.req_offset) * per_req;
+  }
+  const long long next = item + ((target - item + stride - 1) / stride) * stride;
+  return next > INT_MAX ? INT_MAX : static_cast<int>(next);
+}
+
 // Key-tile plan of an item (warp-collective, over all NCTA * 128 rows, so
 // both CTAs of a pair walk the same tiles): the tiles between the smallest
 // and largest visible key of any row, and the tiles inside every row's
@@ -707,7 +748,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       for (int item = blockIdx.x / C::NCTA; ok && item < n_items; item += n_groups) {
         PlanEntry e;
         e.it = item_geometry<C, PAGED>(item, p);
-        if (!e.it.valid) continue;
+        if (!e.it.valid) {
+          item = next_candidate<C>(item, e.it, p, n_groups, lane) - n_groups;  // (the loop adds it back)
+          continue;
+        }
         e.pl = plan_tiles<C>(e.it, p, use_table, lane);
         e.last = 0;
         ok = publish(e);

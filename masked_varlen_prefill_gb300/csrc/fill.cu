@@ -10,7 +10,8 @@
 // span covers precisely the rows whose position lies in [start, end] within
 // the scheduled chunk.  Every row [0, num_tokens) is written (unlike the page,
 // which leaves the buffer untouched when nothing is covered), and
-// rows_written receives the page's return value.
+// rows_written receives the page's return value.  Rows at or past
+// query_start_loc[num_reqs] (a batch padded to a fixed capacity) get (-1, -1).
 #include "mvp_internal.cuh"
 
 namespace mvp {
@@ -22,6 +23,10 @@ constexpr int kFillThreads = 256;
 __global__ void __launch_bounds__(kFillThreads) fill_query_ranges_kernel(FillParams p) {
   const int t = blockIdx.x * kFillThreads + threadIdx.x;
   if (t >= p.num_tokens) return;
+  if (t >= __ldg(p.qsl + p.num_reqs)) {  // a row past the batch (capacity padding)
+    reinterpret_cast<int2*>(p.out)[t] = make_int2(-1, -1);
+    return;
+  }
   // request b with qsl[b] <= t < qsl[b + 1]; requests with q_len 0 have
   // qsl[b] == qsl[b + 1] and can never match.
   int lo = 0, hi = p.num_reqs - 1;
