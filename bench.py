@@ -108,16 +108,17 @@ def source_hash(path):
     return h.hexdigest()[:16]
 
 
-def load_traffic(kernel_src):
+def load_traffic(kernel_src, workload_name):
     """DRAM traffic per launch from the committed ncu summary, or None when
-    the kernel source changed since the counters were taken."""
+    the counters were taken on another workload or the kernel source changed
+    since."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
     except (OSError, ValueError):
         return None
-    if d.get("source_sha256_16") != source_hash(kernel_src):
+    if d.get("workload_name") != workload_name or d.get("source_sha256_16") != source_hash(kernel_src):
         return None
     return d.get("bytes_per_launch")
 
@@ -474,7 +475,7 @@ def run_gpu(args, world, rank, local):
     if rank == 0 and not args.no_cpu_baseline:
         pool = make_pool(cores, args.workload)
 
-    w = workloads.workload(args.workload)
+    w = workloads.scaled_workload(args.workload) if args.scaled else workloads.workload(args.workload)
     n_dec = _leading_decode(w)
     q, k, v, sinks = workloads.make_tensors(w, device=dev)
     cu_q_np, cu_k_np = w.cu_seqlens()
@@ -540,9 +541,28 @@ def run_gpu(args, world, rank, local):
         raise RuntimeError("device timeout during warm-up")
 
     # accounting (host), from the GPU-filled table, which the tests pin bit-exact
-    counts = visible_counts_per_row(w, None if table is None else table.cpu().numpy())
+    table_np = None if table is None else table.cpu().numpy()
+    counts = visible_counts_per_row(w, table_np)
     visible = int(counts.sum())
     flops = 4.0 * w.head_dim * w.num_heads_q * visible
+    acct = mvp.attn_accounting(cu_q_np, w.k_lens, w.num_heads_q, w.num_heads_kv, w.head_dim,
+                               range_table=table_np if (table_np is not None and int(covered.item())) else None,
+                               causal=w.causal, window_left=w.window_left, window_right=w.window_right)
+    if acct["exact_flops"] != flops:
+        raise RuntimeError("library accounting disagrees with the bench's visible count")
+    est = acct["est_attn_qk_flops"] + acct["est_attn_av_flops"]
+    accounting = {
+        "estimate_flops_pr55624": est, "exact_flops": flops, "executed_mma_flops": acct["prefill_mma_flops"],
+        "estimate_over_exact": est / flops if flops else None,
+        "exact_prefill_over_executed": (4.0 * w.head_dim * w.num_heads_q * acct["visible_prefill"]
+                                        / acct["prefill_mma_flops"]) if acct["prefill_mma_flops"] else None,
+        "prefill_items": acct["prefill_items"], "prefill_tiles": acct["prefill_tiles"],
+        "prefill_mma_instructions": acct["prefill_mma_instructions"],
+        "prefill_compulsory_bytes": acct["prefill_compulsory_bytes"],
+        "estimate_decode_kv_bytes_pr55624": acct["est_decode_kv_read_bytes"],
+        "exact_decode_kv_bytes": acct["exact_decode_kv_bytes"], "decode_read_bytes": acct["decode_read_bytes"],
+        "decode_cta_read_bytes": acct["decode_cta_read_bytes"],
+        "source": "mvp_attn_accounting (estimate: vLLM PR #55624 ExecutionContext with the window clamp)"}
 
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -613,8 +633,8 @@ def run_gpu(args, world, rank, local):
         achieved = pre_flops / pre_s / 1e12
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_t, "unit": "TFLOP/s",
                     "frac": achieved / peak_t,
-                    "traffic": (None if paged is not None
-                                else load_traffic(os.path.join(kernel_dir, "attn_prefill.cu"))),
+                    "traffic": (None if (paged is not None or args.scaled)
+                                else load_traffic(os.path.join(kernel_dir, "attn_prefill.cu"), args.workload)),
                     "kernel": f"attn_prefill_kernel (D={w.head_dim})",
                     "peak_source": f"bf16_tflops (burst) of {peak_src}", "kernel_ms_per_launch": 1e3 * pre_s}
     else:
@@ -675,7 +695,7 @@ def run_gpu(args, world, rank, local):
                                   f"over {cores} single-threaded workers"}
 
     if rank == 0:
-        desc = WORKLOAD_DESC if args.workload == WORKLOAD else args.workload
+        desc = WORKLOAD_DESC if (args.workload == WORKLOAD and not args.scaled) else w.name
         line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
@@ -686,7 +706,7 @@ def run_gpu(args, world, rank, local):
                            "parallelism": "replicas" if world > 1 else "single GPU"},
                 "pct_tensor_peak": 100.0 * value / peak_t, "tokens_per_s": tokens_per_s,
                 "visible_entries_per_step": visible, "sub_batches": sub,
-                "roofline": roofline, "cpu_baseline": cpu_baseline, "e2e": e2e,
+                "roofline": roofline, "cpu_baseline": cpu_baseline, "e2e": e2e, "accounting": accounting,
                 "gpu_launches": launches, "clocks": sampler.summary()}
         if graph is not None:
             line["graph"] = graph
@@ -710,6 +730,9 @@ def main(argv=None):
     ap.add_argument("--cpu-rows-per-req", type=int, default=768)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--scaled", action="store_true",
+                    help="run the small test-size version of the workload (for profiler and accounting checks; "
+                         "not a bench line)")
     ap.add_argument("--graph", type=float, default=None, metavar="CAPACITY",
                     help="also run the step through the step-metadata path, captured in a CUDA graph sized for "
                          "CAPACITY x the batch (>= 1), and eagerly; adds a 'graph' object to the line")
@@ -719,6 +742,8 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.scaled:
+        args.no_cpu_baseline = True  # the baseline samples the full workload
     if args.graph is not None and (args.graph < 1.0 or args.paged):
         ap.error("--graph takes a capacity factor >= 1 and a packed K/V layout")
     world, rank, local = dist_setup()

@@ -307,6 +307,61 @@ int mvp_meta_stage(mvp_meta* meta, const int32_t* query_start_loc, const int32_t
  */
 int mvp_meta_upload(mvp_meta* meta, void* stream);
 
+/*
+ * Work accounting of one attention call (host only, no CUDA call).
+ *
+ * Source: vLLM PR #55624 report ("Support Sliding Window Attention and hybrid
+ * layers in MFU/MBU estimation"), Implementation breakdown 2 and 4 and the
+ * ExecutionContext snippet: each request adds num_tokens x
+ * min(context_len, sliding_window) token-context products (the full context
+ * without a window); attn_qk and attn_av cost 2 x heads x head_dim FLOPs per
+ * product; decode requests read min(context_len, sliding_window) keys and
+ * values per KV head.  The report's risks name this an upper bound never
+ * reconciled with profiler counts; the exact and executed fields below are
+ * what closes that gap (the executed ones are the figures a profiler's
+ * tensor-instruction and DRAM counters measure for this library).
+ *
+ * Readings: context_len = the request's key count (seq_lens_k);
+ * sliding_window = window_left + 1 (the keys a causal window keeps), none
+ * when window_left < 0; requests with one query row are decode requests.
+ */
+typedef struct {
+  /* the page's estimate */
+  double est_token_context_product; /* sum num_tokens * min(context_len, window)      */
+  double est_attn_qk_flops;         /* 2 Hq D x the product                            */
+  double est_attn_av_flops;         /* 2 Hq D x the product                            */
+  double est_decode_kv_read_bytes;  /* decode rows: 2 (K, V) Hkv D 2 bytes min(ctx, W)  */
+  /* the exact mask of this library (per query row; every q head alike) */
+  long long visible_prefill;        /* visible (row, key) pairs of rows with q_len > 1 */
+  long long visible_decode;         /* ... of single-row (decode) requests             */
+  double exact_flops;               /* 4 D Hq (visible_prefill + visible_decode)      */
+  double exact_decode_kv_bytes;     /* 2 (K, V) Hkv D 2 bytes visible_decode           */
+  /* what the kernels execute */
+  long long prefill_items;          /* work items with at least one key tile           */
+  long long prefill_tiles;          /* key tiles visited, summed over items            */
+  long long prefill_mma_instructions; /* tcgen05.mma issued: tiles x (D/16 + BN/16)   */
+  double prefill_mma_flops;         /* 2 M BN (D + DV) per tile (M = 128 x CTAs/MMA)   */
+  double prefill_compulsory_bytes;  /* q and out once, K and V of the visited tiles    */
+                                    /* once (lse not included)                         */
+  long long decode_keys_walked;     /* keys read per KV head (tiles start on multiples */
+                                    /* of the decode tile size)                        */
+  double decode_read_bytes;         /* walked K and V once + q                         */
+  double decode_cta_read_bytes;     /* the same as the decode CTAs load it (a KV head  */
+                                    /* is read once per CTA of its q-head group)       */
+} mvp_attn_counts;
+
+/*
+ * Fills *out for an attention call with these HOST arrays: cu_seqlens_q
+ * [num_reqs + 1], seq_lens_k [num_reqs], context_lens [num_reqs] or NULL,
+ * range_table [total_q, 2] (as mvp_fill_query_ranges leaves it) or NULL, and
+ * the call's heads, head_dim and mask scalars.
+ * Errors: MVP_ERR_ARG (NULL out or arrays, negative lengths, a query offset
+ * array not starting at 0, bad mask scalars), MVP_ERR_UNSUPPORTED (head_dim).
+ */
+int mvp_attn_accounting(const int32_t* cu_seqlens_q, const int32_t* seq_lens_k, const int32_t* context_lens,
+                        const int32_t* range_table, int num_reqs, int num_heads_q, int num_heads_kv, int head_dim,
+                        int causal, int window_left, int window_right, mvp_attn_counts* out);
+
 /* Synchronises `stream`, returns MVP_ERR_DEVICE_TIMEOUT if a kernel recorded a
  * timeout since the last call (and clears it), MVP_ERR_CUDA on a CUDA error,
  * else MVP_OK. */

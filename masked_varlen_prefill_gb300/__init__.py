@@ -20,6 +20,7 @@ from ._lib import (  # noqa: F401
     SINK_NULL_LOGIT,
     MvpError,
     StepMetadata,
+    attn_accounting,
     attn_fwd_varlen,
     attn_fwd_paged,
     attn_fwd_varlen_host,

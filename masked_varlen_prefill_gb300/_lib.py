@@ -30,6 +30,19 @@ _i = ctypes.c_int
 _f = ctypes.c_float
 _sz = ctypes.c_size_t
 
+class AttnCounts(ctypes.Structure):
+    """``mvp_attn_counts`` (include/mvp.h)."""
+
+    _fields_ = [("est_token_context_product", ctypes.c_double), ("est_attn_qk_flops", ctypes.c_double),
+                ("est_attn_av_flops", ctypes.c_double), ("est_decode_kv_read_bytes", ctypes.c_double),
+                ("visible_prefill", ctypes.c_longlong), ("visible_decode", ctypes.c_longlong),
+                ("exact_flops", ctypes.c_double), ("exact_decode_kv_bytes", ctypes.c_double),
+                ("prefill_items", ctypes.c_longlong), ("prefill_tiles", ctypes.c_longlong),
+                ("prefill_mma_instructions", ctypes.c_longlong), ("prefill_mma_flops", ctypes.c_double),
+                ("prefill_compulsory_bytes", ctypes.c_double), ("decode_keys_walked", ctypes.c_longlong),
+                ("decode_read_bytes", ctypes.c_double), ("decode_cta_read_bytes", ctypes.c_double)]
+
+
 _SIGNATURES = {
     "mvp_fill_query_ranges": (_i, [_vp, _i, _i, _vp, _vp, _i, _vp, _i, _vp, _vp]),
     "mvp_attn_workspace_size": (_sz, [_i, _i, _i, _i]),
@@ -50,6 +63,7 @@ _SIGNATURES = {
     "mvp_meta_destroy": (_i, [_vp]),
     "mvp_meta_stage": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i]),
     "mvp_meta_upload": (_i, [_vp, _vp]),
+    "mvp_attn_accounting": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(AttnCounts)]),
 }
 
 
@@ -397,4 +411,34 @@ class StepMetadata:
             self.close()
         except Exception:
             pass
+
+
+def attn_accounting(cu_seqlens_q, seq_lens_k, num_heads_q, num_heads_kv, head_dim, *, context_lens=None,
+                    range_table=None, causal=True, window_left=-1, window_right=-1) -> dict:
+    """Work accounting of one attention call from host arrays
+    (``mvp_attn_accounting``): the PR #55624 estimate, the exact mask and the
+    kernels' executed work, as a dict.  No GPU needed."""
+    keep = []
+
+    def arr(a, name, shape=None):
+        x, ptr = _host_i32(a, name, shape)
+        keep.append(x)
+        return ptr
+
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens_q, dtype=np.int32))
+    n = cu.shape[0] - 1
+    p_cu = arr(cu, "cu_seqlens_q")
+    p_sk = arr(seq_lens_k, "seq_lens_k", (n,))
+    p_cl = arr(context_lens, "context_lens", (n,))
+    tbl = None if range_table is None else np.asarray(range_table)
+    if tbl is not None and (tbl.ndim != 2 or tbl.shape[1] != 2 or tbl.shape[0] < int(cu[-1])):
+        raise ValueError("range_table must be [>= total_q, 2]")
+    p_tb = arr(tbl, "range_table")
+    out = AttnCounts()
+    st = load_library().mvp_attn_accounting(p_cu, p_sk, p_cl, p_tb, n, num_heads_q, num_heads_kv, head_dim,
+                                            int(bool(causal)), window_left, window_right, ctypes.byref(out))
+    del keep
+    if st != MVP_OK:
+        raise MvpError("mvp_attn_accounting", st)
+    return {name: getattr(out, name) for name, _ in AttnCounts._fields_}
 
