@@ -501,7 +501,7 @@ def run_gpu(args, world, rank, local):
               sink_mode=w.sink_mode, scale=w.scale, workspace=ws)
 
     def fill():
-        if ranges is None:
+        if ranges is None or args.scan:
             return 0
         mvp.fill_query_ranges(ranges, cu_q, seq_lens, table, num_tokens=w.total_q, rows_written=covered)
         return mvp.last_launch_count()
@@ -509,7 +509,12 @@ def run_gpu(args, world, rank, local):
     def attn(lo=0, hi=None):
         """Attention over requests [lo, hi) of the batch (default: all)."""
         hi = w.num_reqs if hi is None else hi
-        if paged is not None:
+        if args.scan:
+            nd = max(0, min(n_dec, hi) - lo)
+            mvp.attn_fwd_varlen_scan(q, k, v, out, cu_q[lo:hi + 1], cu_k[lo:hi + 1], max(w.q_lens[lo:hi]),
+                                     max(w.k_lens[lo:hi]), None if ranges is None else ranges[lo:hi],
+                                     num_decode_reqs=nd, **kw)
+        elif paged is not None:
             nd = max(0, min(n_dec, hi) - lo)
             mvp.attn_fwd_paged(q, paged["k_cache"], paged["v_cache"], out, cu_q[lo:hi + 1],
                                paged["seq_lens_k"][lo:hi], paged["block_table"][lo:hi], args.paged,
@@ -533,6 +538,11 @@ def run_gpu(args, world, rank, local):
         return n + attn()
 
     marks["mid"] = torch.cuda.Event(enable_timing=True)
+    if args.scan and ranges is not None:
+        # scan mode has no fill step; the table is filled once, outside the
+        # timed steps, for the exact visible count (the workloads' ranges do
+        # not overlap, so the scan and the table see the same keys)
+        mvp.fill_query_ranges(ranges, cu_q, seq_lens, table, num_tokens=w.total_q, rows_written=covered)
     for _ in range(args.warmup):
         flush.zero_()
         step()
@@ -702,6 +712,8 @@ def run_gpu(args, world, rank, local):
                 "config": {"workload": desc, "global_batch": w.num_reqs * world, "seq_len": max_q,
                            "kv_layout": (f"paged, {args.paged}-token blocks in a seeded random order"
                                          if args.paged else "packed"),
+                           "ranges": ("scan mode: per-request range lists scanned in the kernels, no fill"
+                                      if args.scan else "per-row table filled on the GPU each step"),
                            "l2": "flushed between steps (256 MiB write, outside the events)",
                            "parallelism": "replicas" if world > 1 else "single GPU"},
                 "pct_tensor_peak": 100.0 * value / peak_t, "tokens_per_s": tokens_per_s,
@@ -730,6 +742,9 @@ def main(argv=None):
     ap.add_argument("--cpu-rows-per-req", type=int, default=768)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--scan", action="store_true",
+                    help="scan mode: pass the per-request range lists to the attention call instead of filling "
+                         "the per-row table (mvp_attn_fwd_varlen_scan)")
     ap.add_argument("--scaled", action="store_true",
                     help="run the small test-size version of the workload (for profiler and accounting checks; "
                          "not a bench line)")
@@ -744,6 +759,8 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     if args.scaled:
         args.no_cpu_baseline = True  # the baseline samples the full workload
+    if args.scan and (args.paged or args.graph is not None):
+        ap.error("--scan takes a packed K/V layout and no --graph")
     if args.graph is not None and (args.graph < 1.0 or args.paged):
         ap.error("--graph takes a capacity factor >= 1 and a packed K/V layout")
     world, rank, local = dist_setup()

@@ -189,6 +189,36 @@ int mvp_attn_fwd_paged(const void* q, const void* k_cache, const void* v_cache, 
                        size_t workspace_bytes, void* stream);
 
 /*
+ * Scan mode: the same attention with the request-level range list of vLLM's
+ * Triton path instead of the per-row table (PR #50294 review,
+ * "Implementation breakdown" 2: the (num_seqs, max_ranges, 2) tensor that
+ * compute_mm_prefix_range_tensor keeps for the Triton path; the metadata
+ * test's old per-score scan: keep iff some valid range, start < end, holds
+ * both the query position and the key).  No fill step: each query row scans
+ * its request's ranges once (not once per score) and keeps the union of the
+ * valid ranges holding its position, which is one interval because they all
+ * contain it.  Visible = base || (that interval, clamped by window_left on
+ * the past side), exactly as with the table.  With non-overlapping ranges
+ * (the invariant the page's O(1) table relies on) the results are
+ * bit-identical to mvp_fill_query_ranges + mvp_attn_fwd_varlen; overlapping
+ * ranges follow the scan (union), where the table keeps the last range.
+ *
+ * ranges      int32 [num_reqs, max_ranges, 2] row-major, 8-byte aligned,
+ *             closed (start, end) absolute positions; padding (0, 0).
+ * max_ranges  1..4096 (0: no ranges, as a call without a table).
+ * All other arguments, results and errors are those of mvp_attn_fwd_varlen
+ * (no range_table / range_covered); MVP_ERR_ARG also for max_ranges outside
+ * [0, 4096] or NULL ranges with max_ranges > 0.
+ */
+int mvp_attn_fwd_varlen_scan(const void* q, const void* k, const void* v, void* out, float* lse,
+                             const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, const int32_t* context_lens,
+                             int num_reqs, int total_q, int total_k, int max_q_len, int max_k_len,
+                             int num_decode_reqs, int num_heads_q, int num_heads_kv, int head_dim,
+                             const int32_t* ranges, int max_ranges, int causal, int window_left, int window_right,
+                             const float* sinks, int sink_mode, float scale, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
+/*
  * Allocation-free variant of mvp_attn_fwd_varlen.  The pages have no
  * counterpart of this call; it exists for callers that cannot allocate device
  * memory where they run attention (an engine whose free memory is already

@@ -24,6 +24,7 @@ from ._lib import (  # noqa: F401
     attn_fwd_varlen,
     attn_fwd_paged,
     attn_fwd_varlen_host,
+    attn_fwd_varlen_scan,
     attn_fwd_varlen_static_ws,
     attn_workspace_size,
     fill_query_ranges,

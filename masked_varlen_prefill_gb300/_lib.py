@@ -63,6 +63,8 @@ _SIGNATURES = {
     "mvp_meta_destroy": (_i, [_vp]),
     "mvp_meta_stage": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i]),
     "mvp_meta_upload": (_i, [_vp, _vp]),
+    "mvp_attn_fwd_varlen_scan": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i,
+                                      _vp, _i, _i, _i, _i, _vp, _i, _f, _vp, _sz, _vp]),
     "mvp_attn_accounting": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(AttnCounts)]),
 }
 
@@ -184,6 +186,44 @@ def attn_fwd_varlen(q, k, v, out, cu_seqlens_q, cu_seqlens_k, max_q_len, max_k_l
         _ptr(sinks), int(sink_mode), float(scale), _ptr(workspace), ws_bytes, _stream(stream, dev))
     if st != MVP_OK:
         raise MvpError("mvp_attn_fwd_varlen", st)
+
+
+def attn_fwd_varlen_scan(q, k, v, out, cu_seqlens_q, cu_seqlens_k, max_q_len, max_k_len, ranges, *, lse=None,
+                         context_lens=None, causal=True, window_left=-1, window_right=-1, sinks=None,
+                         sink_mode=SINK_NONE, scale=None, workspace=None, num_decode_reqs=-1, stream=None):
+    """Scan-mode attention (``mvp_attn_fwd_varlen_scan``): the request-level
+    range list ``ranges`` int32 [B, max_ranges, 2] instead of a range table."""
+    lib = load_library()
+    dev = q.device
+    for n, t in (("q", q), ("k", k), ("v", v), ("out", out)):
+        _check_cuda(n, t, torch.bfloat16, dev)
+    for n, t in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k), ("context_lens", context_lens),
+                 ("ranges", ranges)):
+        _check_cuda(n, t, torch.int32, dev)
+    _check_cuda("lse", lse, torch.float32, dev)
+    _check_cuda("sinks", sinks, torch.float32, dev)
+    if workspace is not None and (not workspace.is_cuda or not workspace.is_contiguous()):
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    if q.dim() != 3 or k.dim() != 3 or v.shape != k.shape or out.shape != q.shape:
+        raise ValueError("q/out must be [total_q, Hq, D] and k/v [total_k, Hkv, D]")
+    total_q, hq, d = q.shape
+    total_k, hkv, dk = k.shape
+    if dk != d:
+        raise ValueError("q and k head_dim differ")
+    num_reqs = cu_seqlens_q.shape[0] - 1
+    if ranges is not None and (ranges.dim() != 3 or ranges.shape[0] != num_reqs or ranges.shape[2] != 2):
+        raise ValueError("ranges must be [num_reqs, max_ranges, 2]")
+    max_ranges = 0 if ranges is None else ranges.shape[1]
+    if scale is None:
+        scale = d ** -0.5
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.mvp_attn_fwd_varlen_scan(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+        _ptr(context_lens), num_reqs, total_q, total_k, int(max_q_len), int(max_k_len), int(num_decode_reqs),
+        hq, hkv, d, _ptr(ranges), max_ranges, int(bool(causal)), int(window_left), int(window_right),
+        _ptr(sinks), int(sink_mode), float(scale), _ptr(workspace), ws_bytes, _stream(stream, dev))
+    if st != MVP_OK:
+        raise MvpError("mvp_attn_fwd_varlen_scan", st)
 
 
 def attn_fwd_paged(q, k_cache, v_cache, out, cu_seqlens_q, seq_lens_k, block_table, block_size, max_q_len,

@@ -163,7 +163,8 @@ int attn_fwd_impl(const void* q, void* out, float* lse, const int32_t* cu_seqlen
                   int num_reqs, int total_q, int max_q_len, int max_k_len, int num_decode_reqs, int num_heads_q,
                   int num_heads_kv, int head_dim, const int32_t* range_table, const int32_t* range_covered,
                   int causal, int window_left, int window_right, const float* sinks, int sink_mode, float scale,
-                  void* workspace, size_t workspace_bytes, void* stream, const KVArgs& kv) {
+                  void* workspace, size_t workspace_bytes, void* stream, const KVArgs& kv,
+                  const int32_t* scan_ranges = nullptr, int max_ranges = 0) {
   const void* k = kv.k;
   const void* v = kv.v;
   const bool paged = kv.block_table != nullptr;
@@ -185,6 +186,10 @@ int attn_fwd_impl(const void* q, void* out, float* lse, const int32_t* cu_seqlen
   const int total_k = static_cast<int>(kv.rows);
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return MVP_ERR_UNSUPPORTED;
   if (range_table != nullptr && (reinterpret_cast<uintptr_t>(range_table) & 7u) != 0) return MVP_ERR_UNSUPPORTED;
+  if (max_ranges < 0 || max_ranges > 4096 || (max_ranges > 0 && scan_ranges == nullptr)) return MVP_ERR_ARG;
+  if (max_ranges == 0) scan_ranges = nullptr;
+  if (scan_ranges != nullptr && range_table != nullptr) return MVP_ERR_ARG;
+  if (scan_ranges != nullptr && (reinterpret_cast<uintptr_t>(scan_ranges) & 7u) != 0) return MVP_ERR_UNSUPPORTED;
   if (static_cast<long long>(total_q) * num_heads_q * head_dim >= (1LL << 40)) return MVP_ERR_UNSUPPORTED;
 
   // Paged: a TMA box never crosses a cache block.
@@ -204,6 +209,8 @@ int attn_fwd_impl(const void* q, void* out, float* lse, const int32_t* cu_seqlen
   m.ctx_lens = context_lens;
   m.table = range_table;
   m.covered = range_table ? range_covered : nullptr;
+  m.ranges = scan_ranges;
+  m.max_ranges = scan_ranges ? max_ranges : 0;
   m.sinks = sink_mode ? sinks : nullptr;
   m.causal = causal;
   m.window_left = window_left;
@@ -266,7 +273,7 @@ int attn_fwd_impl(const void* q, void* out, float* lse, const int32_t* cu_seqlen
     // Keys a decode row's CTA walks: its visible hull, started on a multiple
     // of the tile size (the kernel aligns it down by up to kt - 1 keys).
     long long span = max_k_len;
-    if (causal && window_left >= 0 && range_table == nullptr && context_lens == nullptr)
+    if (causal && window_left >= 0 && range_table == nullptr && scan_ranges == nullptr && context_lens == nullptr)
       span = (window_left + static_cast<long long>(kt) < span) ? window_left + static_cast<long long>(kt) : span;
     int splits = static_cast<int>((span + kDecodeChunk - 1) / kDecodeChunk);
     if (splits > kMaxSplits) splits = kMaxSplits;
@@ -333,6 +340,21 @@ int mvp_attn_fwd_paged(const void* q, const void* k_cache, const void* v_cache, 
   return attn_fwd_impl(q, out, lse, cu_seqlens_q, context_lens, num_reqs, total_q, max_q_len, max_k_len,
                        num_decode_reqs, num_heads_q, num_heads_kv, head_dim, range_table, range_covered, causal,
                        window_left, window_right, sinks, sink_mode, scale, workspace, workspace_bytes, stream, kv);
+}
+
+int mvp_attn_fwd_varlen_scan(const void* q, const void* k, const void* v, void* out, float* lse,
+                             const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, const int32_t* context_lens,
+                             int num_reqs, int total_q, int total_k, int max_q_len, int max_k_len,
+                             int num_decode_reqs, int num_heads_q, int num_heads_kv, int head_dim,
+                             const int32_t* ranges, int max_ranges, int causal, int window_left, int window_right,
+                             const float* sinks, int sink_mode, float scale, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  g_last_launches = 0;
+  KVArgs kv{k, v, total_k, cu_seqlens_k, nullptr, nullptr, 0, 0};
+  return attn_fwd_impl(q, out, lse, cu_seqlens_q, context_lens, num_reqs, total_q, max_q_len, max_k_len,
+                       num_decode_reqs, num_heads_q, num_heads_kv, head_dim, nullptr, nullptr, causal, window_left,
+                       window_right, sinks, sink_mode, scale, workspace, workspace_bytes, stream, kv, ranges,
+                       max_ranges);
 }
 
 int mvp_get_last_device_error(void* stream) {

@@ -121,7 +121,7 @@ __global__ void __launch_bounds__(kThreads)
     k_len = __ldg(p.m.cu_k + b + 1) - k0;
   }
   const int pos = p.m.ctx_lens ? __ldg(p.m.ctx_lens + b) : (k_len - 1);
-  const RowVis vis = row_visibility(p.m, pos, k_len, table_active(p.m) ? q0 : -1);
+  const RowVis vis = row_visibility(p.m, pos, k_len, table_active(p.m), q0, b);
   int lo, hi;
   vis.hull(lo, hi);
   // Tiles start on multiples of KT (the keys before the visible set are

@@ -261,7 +261,7 @@ __device__ __forceinline__ Plan plan_tiles(const Item& it, const PrefillParams& 
     const int row = lane + 32 * k;
     const int qi = it.pos0 + row / p.gpack;
     if (qi < it.q_len) {
-      const RowVis v = row_visibility(p.m, it.ctx + qi, it.k_len, use_table ? (it.q0 + qi) : -1);
+      const RowVis v = row_visibility(p.m, it.ctx + qi, it.k_len, use_table, it.q0 + qi, it.b);
       int hl, hh, cl, ch;
       v.hull(hl, hh);
       v.core(cl, ch);
@@ -799,7 +799,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       RowLoads l;
       const int qi = e.it.pos0 + pos_off + row / p.gpack;
       const bool valid = !e.last && qi < e.it.q_len;
-      l.tab = (valid && use_table) ? __ldg(reinterpret_cast<const int2*>(p.m.table) + e.it.q0 + qi) : make_int2(1, 0);
+      l.tab = (valid && use_table) ? range_entry(p.m, e.it.q0 + qi, e.it.b, e.it.ctx + qi) : make_int2(1, 0);
       l.sink = (!e.last && p.m.sink_mode != 0 && p.m.sinks != nullptr) ? __ldg(p.m.sinks + e.it.h0 + (row % p.gpack))
                                                                        : 0.f;
       return l;

@@ -67,11 +67,38 @@ __device__ __forceinline__ RowVis empty_row() {
 // The same from an already loaded table entry (use_range false: range off).
 __device__ __forceinline__ RowVis row_visibility_from(const MaskParams& m, int p, int k_len, bool use_range, int2 e);
 
-// p: absolute query position; k_len: keys of the request; table_row: packed
-// row index of this query, or -1 when the range part is off.
-__device__ __forceinline__ RowVis row_visibility(const MaskParams& m, int p, int k_len, int table_row) {
-  const int2 e = table_row >= 0 ? __ldg(reinterpret_cast<const int2*>(m.table) + table_row) : make_int2(1, 0);
-  return row_visibility_from(m, p, k_len, table_row >= 0, e);
+// Scan mode (the per-request range list of vLLM's Triton path, PR #50294
+// "Implementation breakdown" 2): a key is in range iff some valid range
+// (start < end) holds both the query position p and the key.  Every range
+// that holds p contains p, so their union is one interval: [min start,
+// max end] over those ranges, or (-1, -1) when none holds p.  With
+// non-overlapping ranges (the page's invariant) it is the table row.
+__device__ __forceinline__ int2 scan_ranges(const MaskParams& m, int b, int p) {
+  const int2* r = reinterpret_cast<const int2*>(m.ranges) + static_cast<size_t>(b) * m.max_ranges;
+  int lo = INT_MAX, hi = INT_MIN;
+  for (int i = 0; i < m.max_ranges; ++i) {
+    const int2 e = __ldg(r + i);
+    if (e.x < e.y && e.x <= p && p <= e.y) {
+      lo = min(lo, e.x);
+      hi = max(hi, e.y);
+    }
+  }
+  return lo <= hi ? make_int2(lo, hi) : make_int2(-1, -1);
+}
+
+// The range entry of packed query row `row` (request b, position p): its
+// table row, or in scan mode the scan of its request's ranges.
+__device__ __forceinline__ int2 range_entry(const MaskParams& m, int row, int b, int p) {
+  if (m.ranges != nullptr) return scan_ranges(m, b, p);
+  return __ldg(reinterpret_cast<const int2*>(m.table) + row);
+}
+
+// p: absolute query position; k_len: keys of the request; use_range: the
+// range part is on (row: packed row index, b: request, for range_entry).
+__device__ __forceinline__ RowVis row_visibility(const MaskParams& m, int p, int k_len, bool use_range, int row,
+                                                 int b) {
+  const int2 e = use_range ? range_entry(m, row, b, p) : make_int2(1, 0);
+  return row_visibility_from(m, p, k_len, use_range, e);
 }
 
 __device__ __forceinline__ RowVis row_visibility_from(const MaskParams& m, int p, int k_len, bool use_range, int2 e) {
@@ -113,7 +140,10 @@ __device__ __forceinline__ int kv_row(const MaskParams& m, int b, int /*k0*/, in
                           static_cast<unsigned>(l & ((1 << m.block_shift) - 1)));
 }
 
+// Whether the range part of the mask is on: scan mode, or a table whose
+// covered flag (when given) is non-zero.
 __device__ __forceinline__ bool table_active(const MaskParams& m) {
+  if (m.ranges != nullptr) return true;
   if (m.table == nullptr) return false;
   if (m.covered == nullptr) return true;
   return *reinterpret_cast<const volatile int32_t*>(m.covered) != 0;

@@ -34,6 +34,8 @@ struct MaskParams {
   const int32_t* ctx_lens;   // or null
   const int32_t* table;      // [total_q, 2] or null
   const int32_t* covered;    // device scalar or null
+  const int32_t* ranges;     // scan mode: [num_reqs, max_ranges, 2] or null (then table is null)
+  int max_ranges;
   const float* sinks;        // [hq] or null
   int causal;
   int window_left;           // -1 = unbounded

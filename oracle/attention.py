@@ -16,6 +16,11 @@ Definitions restated here, each from the page that fixes it:
   when it lies in the closed ``[start, end]`` of the query row's range-table
   entry; the window clamps that part on the past side only.  The visible set
   is ``base OR range``.  ``(-1, -1)`` never matches a key ``>= 0``.
+* Scan mode -- the request-level range list that PR #50294 keeps for the
+  Triton path (``(num_seqs, max_ranges, 2)``, "Implementation breakdown" 2)
+  and the old per-score rule its metadata test restates: a key is also
+  visible when some valid range (``start < end``) holds both the query
+  position and the key, with the same past-side window clamp.
 * Scores, sinks, softmax -- PR #49815 review, "Key source snippets": scores are
   ``scale * q.k`` with KV head ``h // G`` (``repeat_interleave`` grouping).
   Key-0-bias mode adds ``sink[h]`` to the logit of key 0 when key 0 is
@@ -68,6 +73,26 @@ def visible_mask(q_rows, k_len, ctx, causal, window_left, window_right, row_rang
     return base | in_range
 
 
+def visible_mask_scan(q_rows, k_len, ctx, causal, window_left, window_right, req_ranges):
+    """Dense mask of scan mode: ``base OR any(range holds query and key)``.
+
+    ``req_ranges`` is the request's list of closed ``(start, end)``; entries
+    with ``start >= end`` are skipped, as the scan skips them.
+    """
+    base = visible_mask(q_rows, k_len, ctx, causal, window_left, window_right, None)
+    i = np.asarray(q_rows, dtype=np.int64).reshape(-1, 1)
+    j = np.arange(k_len, dtype=np.int64).reshape(1, -1)
+    p = ctx + i
+    keep = np.zeros_like(base)
+    for start, end in req_ranges:
+        if not start < end:
+            continue
+        keep |= (start <= p) & (p <= end) & (start <= j) & (j <= end)
+    if window_left >= 0:
+        keep &= j >= p - window_left
+    return base | keep
+
+
 def _as_f64(x):
     """Widen a torch/numpy bf16/fp32 array to float64 exactly."""
     try:
@@ -81,11 +106,13 @@ def _as_f64(x):
 
 
 def attend_rows(q_rows, q, k, v, ctx, causal, window_left, window_right,
-                row_ranges, sinks, sink_mode, scale):
+                row_ranges, sinks, sink_mode, scale, req_ranges=None):
     """Attention for some query rows of ONE request, every query head.
 
     q: ``[q_len, Hq, D]``; k: ``[k_len, Hkv, D]``; v: ``[k_len, Hkv, Dv]``
     (float64).  Returns ``out [rows, Hq, Dv]`` and ``lse [Hq, rows]``.
+    ``req_ranges`` (the request's range list) selects scan mode instead of
+    the per-row ``row_ranges``.
     """
     q_rows = np.asarray(q_rows, dtype=np.int64)
     n_rows = q_rows.shape[0]
@@ -93,7 +120,10 @@ def attend_rows(q_rows, q, k, v, ctx, causal, window_left, window_right,
     hq = q.shape[1]
     group = hq // hkv
     dv = v.shape[2]
-    mask = visible_mask(q_rows, k_len, ctx, causal, window_left, window_right, row_ranges)
+    if req_ranges is not None:
+        mask = visible_mask_scan(q_rows, k_len, ctx, causal, window_left, window_right, req_ranges)
+    else:
+        mask = visible_mask(q_rows, k_len, ctx, causal, window_left, window_right, row_ranges)
     out = np.zeros((n_rows, hq, dv), dtype=np.float64)
     lse = np.full((hq, n_rows), -np.inf, dtype=np.float64)
     for h in range(hq):
@@ -119,11 +149,12 @@ def attend_rows(q_rows, q, k, v, ctx, causal, window_left, window_right,
 
 def attention_forward(q, k, v, cu_seqlens_q, cu_seqlens_k, causal, window_left,
                       window_right, scale, context_lens=None, range_table=None,
-                      sinks=None, sink_mode=SINK_NONE, rows=None):
+                      sinks=None, sink_mode=SINK_NONE, rows=None, scan_ranges=None):
     """Whole packed batch (or the packed rows listed in ``rows``).
 
     q ``[total_q, Hq, D]``, k/v ``[total_k, Hkv, D]`` (any dtype; widened to
-    float64); ``range_table`` ``[total_q, 2]`` int or None.  Returns
+    float64); ``range_table`` ``[total_q, 2]`` int or None; ``scan_ranges``
+    ``[B, max_ranges, 2]`` (scan mode, instead of a table) or None.  Returns
     ``out [total_q, Hq, Dv]`` and ``lse [Hq, total_q]`` in float64.  With
     ``rows`` given, only those packed rows are computed; the others stay 0 /
     NaN and callers compare only the requested rows.
@@ -154,8 +185,9 @@ def attention_forward(q, k, v, cu_seqlens_q, cu_seqlens_k, causal, window_left,
                 continue
             local = sel - q0
         rr = None if table is None else table[q0 + local]
+        req = None if scan_ranges is None else [(int(s_), int(e_)) for s_, e_ in np.asarray(scan_ranges)[b]]
         o, l = attend_rows(local, q[q0:q1], k[k0:k1], v[k0:k1], ctx, causal,
-                           window_left, window_right, rr, sinks, sink_mode, scale)
+                           window_left, window_right, rr, sinks, sink_mode, scale, req_ranges=req)
         out[q0 + local] = o
         lse[:, q0 + local] = l
     return out, lse

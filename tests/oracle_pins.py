@@ -126,6 +126,53 @@ def check_range_lookup_random(fill, scan_keep, cases=1500, seed=7):
         assert n == (int(qsl[-1]) if any_cover else 0), (n, any_cover)
 
 
+def check_scan_mask(visible_mask_scan, visible_mask, fill, cases=600, seed=13):
+    """Scan mode against element-by-element loops of its definition (base
+    rule OR some valid range holds query and key, past-side window clamp),
+    with overlapping and degenerate ranges; and, for non-overlapping ranges,
+    against the table mask of the same batch (the page's O(1) equivalence).
+    Includes the page's printed example."""
+    rng = np.random.default_rng(seed)
+    g = _golden_json("range_table_example.json")
+    printed = (g["query_lens"], g["seq_lens"], {int(k): [tuple(r) for r in v] for k, v in g["mm_ranges"].items()})
+    for case in range(cases + 1):
+        if case == 0:
+            qlens, seqs, mm = printed
+            causal, wl, wr = True, -1, -1
+            overlap = False
+        else:
+            nb = int(rng.integers(1, 4))
+            qlens = [int(rng.integers(1, 7)) for _ in range(nb)]
+            seqs = [q + int(rng.integers(0, 6)) for q in qlens]
+            overlap = bool(rng.integers(0, 2))
+            if overlap:
+                mm = {b: [(int(rng.integers(0, seqs[b] + 2)), int(rng.integers(-1, seqs[b] + 3)))
+                          for _ in range(int(rng.integers(0, 5)))] for b in range(nb)}
+            else:
+                mm = {b: _random_nonoverlap(rng, seqs[b] + 3) for b in range(nb)}
+            causal = bool(rng.integers(0, 2))
+            wl = int(rng.choice([-1, 0, 1, 3]))
+            wr = 0 if causal else int(rng.choice([-1, 0, 2]))
+        qsl = np.array([0] + list(np.cumsum(qlens)), dtype=np.int32)
+        table = np.full((max(1, int(qsl[-1])), 2), -1, dtype=np.int32)
+        n = fill(table, mm, qsl, np.array(seqs, dtype=np.int32))
+        for b in range(len(qlens)):
+            ctx = seqs[b] - qlens[b]
+            got = visible_mask_scan(np.arange(qlens[b]), seqs[b], ctx, causal, wl, wr, mm[b])
+            for i in range(qlens[b]):
+                p = ctx + i
+                for j in range(seqs[b]):
+                    base = (j <= p) if causal else (wr < 0 or j <= p + wr)
+                    base = base and (wl < 0 or j >= p - wl)
+                    rng_keep = any(s < e and s <= p <= e and s <= j <= e for s, e in mm[b])
+                    rng_keep = rng_keep and (wl < 0 or j >= p - wl)
+                    assert got[i, j] == (base or rng_keep), (case, b, i, j)
+            if not overlap:
+                rows = table[qsl[b]:qsl[b + 1]] if n else np.full((qlens[b], 2), -1, dtype=np.int32)
+                ref = visible_mask(np.arange(qlens[b]), seqs[b], ctx, causal, wl, wr, rows)
+                assert np.array_equal(got, ref), (case, b)
+
+
 def check_fill_edge_cases(fill):
     P = 12345
 

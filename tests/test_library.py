@@ -101,6 +101,27 @@ def test_paged_argument_errors(lib):
     assert _paged(lib, total_q=0) == mvp.MVP_OK  # nothing to do
 
 
+def _scan(lib, **over):
+    args = dict(q=1 << 20, k=1 << 20, v=1 << 20, out=1 << 20, lse=None, cu_q=1 << 20, cu_k=1 << 20, ctx=None,
+                num_reqs=1, total_q=4, total_k=64, max_q=4, max_k=64, ndec=-1, hq=4, hkv=2, d=128,
+                ranges=1 << 20, max_ranges=2, causal=1, wl=-1, wr=-1, sinks=None, sink_mode=0, scale=0.1, ws=None,
+                ws_bytes=0, stream=None)
+    args.update(over)
+    return lib.mvp_attn_fwd_varlen_scan(*[args[k] for k in (
+        "q", "k", "v", "out", "lse", "cu_q", "cu_k", "ctx", "num_reqs", "total_q", "total_k", "max_q", "max_k",
+        "ndec", "hq", "hkv", "d", "ranges", "max_ranges", "causal", "wl", "wr", "sinks", "sink_mode", "scale", "ws",
+        "ws_bytes", "stream")])
+
+
+def test_scan_argument_errors(lib):
+    assert _scan(lib, ranges=None) == mvp.MVP_ERR_ARG           # max_ranges > 0 without ranges
+    assert _scan(lib, max_ranges=-1) == mvp.MVP_ERR_ARG
+    assert _scan(lib, max_ranges=4097) == mvp.MVP_ERR_ARG
+    assert _scan(lib, ranges=(1 << 20) + 4) == mvp.MVP_ERR_UNSUPPORTED  # not 8-byte aligned
+    assert _scan(lib, d=96) == mvp.MVP_ERR_UNSUPPORTED
+    assert _scan(lib, total_q=0) == mvp.MVP_OK
+
+
 def test_fill_argument_errors(lib):
     f = lib.mvp_fill_query_ranges
     assert f(None, 1, 1, 1 << 20, 1 << 20, 10, 1 << 20, 4, None, None) == mvp.MVP_ERR_ARG  # ranges null

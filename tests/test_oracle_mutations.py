@@ -80,6 +80,16 @@ ATTENTION_MUTANTS = [
     # LSE without the max shift
     ("lse_shift", "safe_max + np.log(z)", "np.log(z)",
      lambda m: pins.check_sdpa(m.attention_forward)),
+    # scan mode: only the first listed range consulted
+    ("scan_first_only", "for start, end in req_ranges:", "for start, end in req_ranges[:1]:",
+     lambda m: pins.check_scan_mask(m.visible_mask_scan, m.visible_mask, real_range_table.fill_by_spans)),
+    # scan mode: the query side of "holds both" dropped
+    ("scan_query_unchecked", "keep |= (start <= p) & (p <= end) & (start <= j) & (j <= end)",
+     "keep |= (start <= j) & (j <= end)",
+     lambda m: pins.check_scan_mask(m.visible_mask_scan, m.visible_mask, real_range_table.fill_by_spans)),
+    # scan mode: the window clamp on the range part dropped
+    ("scan_unclamped", "keep &= j >= p - window_left", "keep &= True",
+     lambda m: pins.check_scan_mask(m.visible_mask_scan, m.visible_mask, real_range_table.fill_by_spans)),
 ]
 
 

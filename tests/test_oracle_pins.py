@@ -36,6 +36,10 @@ def test_range_lookup_equals_scan_random():
     pins.check_range_lookup_random(range_table.fill_by_spans, range_table.scan_keep)
 
 
+def test_scan_mode_mask():
+    pins.check_scan_mask(attention.visible_mask_scan, attention.visible_mask, range_table.fill_by_spans)
+
+
 def test_fill_edge_cases():
     pins.check_fill_edge_cases(range_table.fill_by_spans)
     pins.check_fill_edge_cases(range_table.fill_by_scan)
