@@ -102,8 +102,7 @@ extern "C" int mvp_attn_accounting(const int32_t* cu_seqlens_q, const int32_t* s
   const PrefillShape shape = prefill_tile_shape(head_dim);
   const int gpack = pow2_divisor(group, 8);
   const int n_hgroups = group / gpack;
-  const long long m_rows = 128LL * shape.ncta;   // MMA rows of an item
-  const long long item_pos = m_rows / gpack;      // query positions of an item
+  const long long item_pos = shape.item_rows / gpack;  // query positions of an item
   const long long bn = shape.bn;
   const int kt = decode_keys_per_tile(head_dim);
   const int per_cta = decode_heads_per_cta(head_dim, group);
@@ -181,9 +180,11 @@ extern "C" int mvp_attn_accounting(const int32_t* cu_seqlens_q, const int32_t* s
   out->exact_decode_kv_bytes = 2.0 * hkv * d * 2.0 * static_cast<double>(vis_dec);
   out->prefill_items = static_cast<long long>(items * heads_items);
   out->prefill_tiles = static_cast<long long>(tiles * heads_items);
-  out->prefill_mma_instructions = out->prefill_tiles * (head_dim / 16 + shape.bn / 16);
-  out->prefill_mma_flops = static_cast<double>(out->prefill_tiles) * 2.0 * static_cast<double>(m_rows) *
-                           static_cast<double>(bn) * (d + shape.dv_cta);
+  // per tile, each issuing CTA: qk_k / 16 QK MMAs (M x BN x 16) and BN / 16
+  // PV MMAs (M x oc x 16)
+  out->prefill_mma_instructions = out->prefill_tiles * shape.issuers * (shape.qk_k / 16 + shape.bn / 16);
+  out->prefill_mma_flops = static_cast<double>(out->prefill_tiles) * shape.issuers * 2.0 * shape.mma_m *
+                           static_cast<double>(bn) * (shape.qk_k + shape.oc);
   out->prefill_compulsory_bytes = 2.0 * static_cast<double>(rows_pre) * hq * d * 2.0 +  // q in, out
                                   2.0 * static_cast<double>(touched_pre) * hkv * d * 2.0;  // k, v
   out->decode_keys_walked = keys_walked;

@@ -241,7 +241,7 @@ int attn_fwd_impl(const void* q, void* out, float* lse, const int32_t* cu_seqlen
     pp.hkv = num_heads_kv;
     pp.gpack = gpack;
     pp.n_hgroups = group / gpack;
-    const int item_pos = bmp * shape.ncta;  // query positions per work item
+    const int item_pos = shape.item_rows / gpack;  // query positions per work item
     pp.n_qtiles = (max_q_len + item_pos - 1) / item_pos;
     pp.skip_decode = 1;
     pp.req_offset = prefill_first;

@@ -45,6 +45,8 @@
 // * Every mbarrier wait is bounded (ptx.cuh).
 #include <cuda_bf16.h>
 
+#include <cstdlib>
+
 #include "mask.cuh"
 #include "mvp_internal.cuh"
 #include "ptx.cuh"
@@ -57,23 +59,34 @@ constexpr int kBM = 128;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr unsigned kFullMask = 0xffffffffu;
 
-template <int D_, int DV_, int BN_, int KST_, int VST_, int NCTA_>
+template <int D_, int DV_, int BN_, int KST_, int VST_, int NCTA_, int SPLITD_ = 0>
 struct Cfg {
   static constexpr int D = D_;
   static constexpr int DV = DV_;        // value columns handled by one item
   static constexpr int BN = BN_;        // keys per tile
   static constexpr int KST = KST_;      // K tile stages
   static constexpr int VST = VST_;      // V tile stages
-  static constexpr int NCTA = NCTA_;    // CTAs sharing each MMA (1, or 2 for a CTA pair)
-  static constexpr int KROWS = BN / NCTA;   // keys of a K tile loaded by one CTA
-  static constexpr int DVC = DV / NCTA;     // value columns of a V tile loaded by one CTA
-  static constexpr int ITEM_ROWS = kBM * NCTA;
-  static constexpr int QCH = D / 64;    // 64-dim chunks of Q and K (one TMA box each)
+  static constexpr int NCTA = NCTA_;    // CTAs of a cluster working on one item (1 or 2)
+  // Two ways for two CTAs to share an item: a pair (M split: each CTA owns
+  // 128 of the 256 rows, rank 0 issues .cta_group::2 MMAs) or a head-dim
+  // split (SPLITD: both CTAs own the same 128 rows; each multiplies its half
+  // of the head dimension into a partial score and its half of the value
+  // columns into its own O, issuing its own MMAs; the partial scores are
+  // summed through distributed shared memory).
+  static constexpr bool SPLITD = SPLITD_ != 0;
+  static constexpr bool PAIR = NCTA == 2 && !SPLITD;
+  static constexpr int MMA_CTAS = PAIR ? 2 : 1;  // CTAs one MMA spans
+  static constexpr int DQ = SPLITD ? D / 2 : D;  // head dims of Q and K held by one CTA
+  static constexpr int KROWS = BN / MMA_CTAS;    // keys of a K tile loaded by one CTA
+  static constexpr int DVC = DV / NCTA;          // value columns of a V tile loaded by one CTA
+  static constexpr int OC = SPLITD ? DVC : DV;   // O columns in this CTA's TMEM
+  static constexpr int ITEM_ROWS = kBM * MMA_CTAS;
+  static constexpr int QCH = DQ / 64;   // 64-dim chunks of Q and K (one TMA box each)
   static constexpr int VCH = DVC / 64;  // 64-column chunks of this CTA's part of a V tile
   static constexpr int DV_SPLIT = D / DV;
   static constexpr int SPLIT = BN / 64;         // softmax warpgroups (column halves of a row)
   static constexpr int HC = BN / SPLIT;         // score columns per softmax thread (64)
-  static constexpr int HDV = DV / SPLIT;        // O columns per softmax thread (rescale)
+  static constexpr int HDV = OC / SPLIT;        // O columns per softmax thread (rescale)
   // Warp layout: warpgroup 0 = TMA producer (warp 0), MMA issuer (1), plan
   // scheduler (2), one idle warp; SPLIT softmax warpgroups; one epilogue
   // warpgroup that reads O out of TMEM and stores the output rows.
@@ -94,14 +107,17 @@ struct Cfg {
   static constexpr int REGS_EPI = 88;
   static_assert(!REG_SPLIT || (THREADS == 512 && REGS_CTRL + 2 * REGS_SOFTMAX + REGS_EPI <= 4 * 128),
                 "register split");
-  static constexpr int Q_BYTES = kBM * D * 2;
-  static constexpr int K_BYTES = KROWS * D * 2;  // per CTA
+  static constexpr int Q_BYTES = kBM * DQ * 2;
+  static constexpr int K_BYTES = KROWS * DQ * 2;  // per CTA
   static constexpr int V_BYTES = BN * DVC * 2;    // per CTA
   static constexpr int Q_OFF = 0;
   static constexpr int K_OFF = Q_BYTES;
   static constexpr int V_OFF = K_OFF + KST * K_BYTES;
   static constexpr int TILE_BYTES = V_OFF + VST * V_BYTES;
-  static constexpr int RED_OFF = TILE_BYTES;  // pair exchange slots: [2 parity][SPLIT][128] float2
+  // SPLITD: the peer's partial scores of two tiles, [2][128 rows][BN] fp32
+  static constexpr int XS_OFF = TILE_BYTES;
+  static constexpr int XS_BYTES = SPLITD ? 2 * kBM * BN * 4 : 0;
+  static constexpr int RED_OFF = XS_OFF + XS_BYTES;  // column-half exchange slots: [2 parity][SPLIT][128] float2
   static constexpr int RED_BYTES = SPLIT > 1 ? 2 * SPLIT * kBM * 8 : 0;
   // Hand-off slots softmax -> epilogue: (1 / l, LSE) per row and item.  Two
   // when they fit (the D = 512 tiles leave room for one).
@@ -119,11 +135,12 @@ struct Cfg {
   static constexpr int S_COL = 0;
   static constexpr int O_COL = 2 * BN;
   static constexpr int TMEM_COLS = 512;
-  static_assert(O_COL + DV <= TMEM_COLS, "TMEM budget");
+  static_assert(O_COL + OC <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM_BYTES <= 227 * 1024, "smem budget");
   static_assert(BN == 64 || BN == 128, "BN");
-  static_assert(DV % 64 == 0 && DV <= 256 && DVC % 64 == 0, "DV");
+  static_assert(DV % 64 == 0 && OC <= 256 && DVC % 64 == 0, "DV");
   static_assert(NCTA == 1 || NCTA == 2, "NCTA");
+  static_assert(!SPLITD || (NCTA == 2 && SPLIT == 1 && DV == D), "head-dim split: one softmax warpgroup, no DV split");
   static_assert(HDV % 32 == 0, "O columns per thread");
   static_assert(KST >= 1 && KST <= 4 && VST >= 1 && VST <= 4, "stages");
   // With two K and two V stages, "K stage of tile t free" is exactly "S_t
@@ -172,6 +189,8 @@ struct __align__(8) Barriers {
   uint64_t epi_full[2];   // an item's (1 / l, LSE) rows are written (half-0 softmax warps)
   uint64_t epi_empty[2];  // ... and read (epilogue warps)
   uint64_t o_free;        // O of the previous item is out of TMEM (rank 0; arrivals from both CTAs)
+  uint64_t x_full[2];     // head-dim split: the peer's partial scores of a tile are in slot i
+  uint64_t x_empty[2];    // ... the peer has read what this CTA sent into its slot i
   uint64_t xchg[4][2];  // softmax column-half pairs (per TMEM lane quarter), by parity
   uint32_t tmem_base;
   int abort_flag;
@@ -257,7 +276,7 @@ template <class C>
 __device__ __forceinline__ Plan plan_tiles(const Item& it, const PrefillParams& p, bool use_table, int lane) {
   int hl_min = INT_MAX, hh_max = INT_MIN, cl_max = INT_MIN, ch_min = INT_MAX;
 #pragma unroll
-  for (int k = 0; k < 4 * C::NCTA; ++k) {
+  for (int k = 0; k < C::ITEM_ROWS / 32; ++k) {
     const int row = lane + 32 * k;
     const int qi = it.pos0 + row / p.gpack;
     if (qi < it.q_len) {
@@ -321,10 +340,10 @@ __device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t* r) {
                : "memory");
 }
 
-// With NCTA == 2, TMA copies of both CTAs complete on rank 0's barrier.
+// In a pair, TMA copies of both CTAs complete on rank 0's barrier.
 template <class C>
 __device__ __forceinline__ void tma_load(void* dst, const CUtensorMap* map, uint64_t* full, int x, int y, int z) {
-  if constexpr (C::NCTA == 2) tma_load_3d_pair(dst, map, mapa_shared(smem_u32(full), 0), x, y, z);
+  if constexpr (C::PAIR) tma_load_3d_pair(dst, map, mapa_shared(smem_u32(full), 0), x, y, z);
   else tma_load_3d(dst, map, full, x, y, z);
 }
 
@@ -344,7 +363,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   const int n_items = p.n_qtiles * (p.num_reqs - p.req_offset) * p.hkv * p.n_hgroups * C::DV_SPLIT;
   constexpr int BN = C::BN;
   const int rank = C::NCTA == 2 ? static_cast<int>(cluster_rank()) : 0;
-  const bool leader = rank == 0;  // issues the MMAs and owns the "full" barriers
+  const bool leader = !C::PAIR || rank == 0;  // issues its MMAs and owns the "full" barriers
+  // This CTA's first query position within an item (a pair's rank 1 owns the
+  // second 128 rows) and first head dim of Q and K (a head-dim split's rank 1
+  // owns the second half); evaluated inside each role, so that no register
+  // stays live across the roles' register split.
+  auto row_pos_off = [&]() { return C::PAIR ? rank * (kBM / p.gpack) : 0; };
+  auto dq_off = [&]() { return C::SPLITD ? rank * C::DQ : 0; };
 
   // ---------------------------------------------------------------- setup
   if (threadIdx.x == 0) {
@@ -362,7 +387,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sb.s_full[i], 1);
-      mbar_init(&sb.p_full[i], 4 * C::SPLIT * C::NCTA);  // one arrival per softmax warp
+      mbar_init(&sb.p_full[i], 4 * C::SPLIT * C::MMA_CTAS);  // one arrival per softmax warp
       mbar_init(&sb.o_done[i], 1);
     }
     mbar_init(&sb.final_mma, 1);
@@ -370,7 +395,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       mbar_init(&sb.epi_full[i], 4);
       mbar_init(&sb.epi_empty[i], 4);
     }
-    mbar_init(&sb.o_free, 4 * C::NCTA);
+    mbar_init(&sb.o_free, 4 * C::MMA_CTAS);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sb.x_full[i], 4);   // head-dim split: the peer's four softmax warps wrote their partial scores
+      mbar_init(&sb.x_empty[i], 4);  // ... and read this CTA's
+    }
     for (int i = 0; i < 4; ++i) {
       mbar_init(&sb.xchg[i][0], 64);
       mbar_init(&sb.xchg[i][1], 64);
@@ -379,7 +408,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     mbar_fence_init();
   }
   if (warp == 1) {
-    if constexpr (C::NCTA == 2) {
+    if constexpr (C::PAIR) {
       tmem_alloc_pair(&sb.tmem_base, C::TMEM_COLS);
       tmem_relinquish_pair();
     } else {
@@ -426,7 +455,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           if (e.pl.n_tiles > 0) return true;
         }
       };
-      const int pos_off = rank * (kBM / p.gpack);  // this CTA's first position within an item
+      const int pos_off = row_pos_off();
+      const int dq0 = dq_off();
       // L2 warming: an item's Q tile and first K / V tiles come from DRAM,
       // with a latency several times a tile's MMA time, while its later tiles
       // follow at the pace of the pipeline.  The next item's Q and (packed
@@ -480,7 +510,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       auto prefetch_kv = [&](const PlanEntry& e, int j) {  // packed K / V only
         const int key0 = e.it.k0 + (e.pl.kb_lo + j) * BN;
 #pragma unroll
-        for (int c = 0; c < C::QCH; ++c) tma_prefetch_l2_3d(&map_k, c * 64, e.it.hkv, key0 + rank * C::KROWS);
+        for (int c = 0; c < C::QCH; ++c)
+          tma_prefetch_l2_3d(&map_k, dq0 + c * 64, e.it.hkv, key0 + (C::PAIR ? rank * C::KROWS : 0));
 #pragma unroll
         for (int c = 0; c < C::VCH; ++c)
           tma_prefetch_l2_3d(&map_v, e.it.dv0 + rank * C::DVC + c * 64, e.it.hkv, key0);
@@ -497,7 +528,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (e.last || e.pl.n_tiles == 0) return;
         if (lane == 0) {
 #pragma unroll
-          for (int c = 0; c < C::QCH; ++c) tma_prefetch_l2_3d(&map_q, c * 64, e.it.h0, e.it.q0 + e.it.pos0 + pos_off);
+          for (int c = 0; c < C::QCH; ++c)
+            tma_prefetch_l2_3d(&map_q, dq0 + c * 64, e.it.h0, e.it.q0 + e.it.pos0 + pos_off);
           for (int j = 0; !PAGED && j < kPrefetchAhead && j < e.pl.n_tiles; ++j) prefetch_kv(e, j);
         }
         if constexpr (PAGED) {
@@ -516,10 +548,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           }
           if (!free) return false;
         }
-        if (leader) mbar_arrive_expect_tx(&sb.q_full, C::NCTA * C::Q_BYTES);
+        if (leader) mbar_arrive_expect_tx(&sb.q_full, C::MMA_CTAS * C::Q_BYTES);
 #pragma unroll
         for (int c = 0; c < C::QCH; ++c)
-          tma_load<C>(sQ + c * (kBM * 128), &map_q, &sb.q_full, c * 64, e.it.h0, e.it.q0 + e.it.pos0 + pos_off);
+          tma_load<C>(sQ + c * (kBM * 128), &map_q, &sb.q_full, dq0 + c * 64, e.it.h0, e.it.q0 + e.it.pos0 + pos_off);
         ++qn;
         return true;
       };
@@ -532,8 +564,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                                 : mbar_wait(&sb.k_empty[s], (tp / C::KST) & 1, &sb.abort_flag, p.err, kDevTimeoutLoad);
           if (!free) return false;
         }
-        if (leader) mbar_arrive_expect_tx(&sb.k_full[s], C::NCTA * C::K_BYTES);
-        const int key0 = (e.pl.kb_lo + j) * BN + rank * C::KROWS;  // this CTA's first key of the tile
+        if (leader) mbar_arrive_expect_tx(&sb.k_full[s], C::MMA_CTAS * C::K_BYTES);
+        const int key0 = (e.pl.kb_lo + j) * BN + (C::PAIR ? rank * C::KROWS : 0);  // this CTA's first key of the tile
         if constexpr (PAGED) {
           // one box per run of K rows inside one cache block (a rolled loop:
           // the producer's code stays small next to the other roles')
@@ -542,13 +574,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             const int krow = row_of(e, buf, key0 + r);
 #pragma unroll
             for (int c = 0; c < C::QCH; ++c)
-              tma_load<C>(sK + s * C::K_BYTES + c * (C::KROWS * 128) + r * 128, &map_k, &sb.k_full[s], c * 64,
-                          e.it.hkv, krow);
+              tma_load<C>(sK + s * C::K_BYTES + c * (C::KROWS * 128) + r * 128, &map_k, &sb.k_full[s],
+                          dq0 + c * 64, e.it.hkv, krow);
           }
         } else {
 #pragma unroll
           for (int c = 0; c < C::QCH; ++c)
-            tma_load<C>(sK + s * C::K_BYTES + c * (C::KROWS * 128), &map_k, &sb.k_full[s], c * 64, e.it.hkv,
+            tma_load<C>(sK + s * C::K_BYTES + c * (C::KROWS * 128), &map_k, &sb.k_full[s], dq0 + c * 64, e.it.hkv,
                         e.it.k0 + key0);
         }
         ++k_armed[s];
@@ -564,7 +596,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
                                 : mbar_wait(&sb.v_empty[s], (tp / C::VST) & 1, &sb.abort_flag, p.err, kDevTimeoutLoad);
           if (!free) return false;
         }
-        if (leader) mbar_arrive_expect_tx(&sb.v_full[s], C::NCTA * C::V_BYTES);
+        if (leader) mbar_arrive_expect_tx(&sb.v_full[s], C::MMA_CTAS * C::V_BYTES);
         const int key0 = (e.pl.kb_lo + j) * BN;
         if constexpr (PAGED) {
 #pragma unroll 1
@@ -644,7 +676,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       // t % VST.  In a pair, the same descriptors and TMEM addresses name the
       // operands in both CTAs.
       constexpr uint32_t idesc_qk = idesc_bf16_f32(C::ITEM_ROWS, C::BN, false, false);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(C::ITEM_ROWS, C::DV, false, true);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(C::ITEM_ROWS, C::OC, false, true);
       const uint64_t dq = smem_desc_sw128(smem_u32(sQ), 16, 1024);
       const uint64_t dk0 = smem_desc_sw128(smem_u32(sK), 16, 1024);
       const uint64_t dv0 = smem_desc_sw128(smem_u32(sV), BN * 128, 1024);
@@ -674,14 +706,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
               for (int k16 = 0; k16 < 4; ++k16) {
                 const uint64_t a = dq + static_cast<uint64_t>((c * (kBM * 128) + k16 * 32) >> 4);
                 const uint64_t b = dk + static_cast<uint64_t>((c * (C::KROWS * 128) + k16 * 32) >> 4);
-                mma_ss_elect<C::NCTA>(d, a, b, idesc_qk, (c | k16) != 0 ? 1u : 0u);
+                mma_ss_elect<C::MMA_CTAS>(d, a, b, idesc_qk, (c | k16) != 0 ? 1u : 0u);
               }
             }
             if constexpr (!C::MERGED_RELEASE) {
-              mma_commit_elect<C::NCTA>(&sb.k_empty[s]);
-              if (j == pl.n_tiles - 1) mma_commit_elect<C::NCTA>(&sb.q_empty);  // Q free for the next item
+              mma_commit_elect<C::MMA_CTAS>(&sb.k_empty[s]);
+              if (j == pl.n_tiles - 1) mma_commit_elect<C::MMA_CTAS>(&sb.q_empty);  // Q free for the next item
             }
-            mma_commit_elect<C::NCTA>(&sb.s_full[t & 1]);
+            mma_commit_elect<C::MMA_CTAS>(&sb.s_full[t & 1]);
           }
           if (j >= 1) {
             const int t = T + j - 1;
@@ -708,10 +740,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk) {
               const uint64_t b = dv + static_cast<uint64_t>((kk * 16 * 128) >> 4);
-              mma_ts_elect<C::NCTA>(tmem + C::O_COL, pcol + kk * 8, b, idesc_pv, kk == 0 ? first : 1u);
+              mma_ts_elect<C::MMA_CTAS>(tmem + C::O_COL, pcol + kk * 8, b, idesc_pv, kk == 0 ? first : 1u);
             }
-            if constexpr (!C::MERGED_RELEASE) mma_commit_elect<C::NCTA>(&sb.v_empty[s]);
-            mma_commit_elect<C::NCTA>(&sb.o_done[t & 1]);
+            if constexpr (!C::MERGED_RELEASE) mma_commit_elect<C::MMA_CTAS>(&sb.v_empty[s]);
+            mma_commit_elect<C::MMA_CTAS>(&sb.o_done[t & 1]);
           }
         }
         T += pl.n_tiles;
@@ -719,7 +751,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       if (!ok && lane == 0) sb.abort_flag = 1;
       // All issued MMAs must finish before TMEM is released (and, in a pair,
       // before the peer's shared memory and TMEM go away).
-      mma_commit_elect<C::NCTA>(&sb.final_mma);
+      mma_commit_elect<C::MMA_CTAS>(&sb.final_mma);
       volatile int own_flag = 0;
       mbar_wait(&sb.final_mma, 0, &own_flag, p.err, kDevTimeoutMma);
     } else if (warp == 1) {
@@ -786,9 +818,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       RowVis vis;
       float sink;
     };
-    const int pos_off = rank * (kBM / p.gpack);  // this CTA's first position within an item
+    const int pos_off = row_pos_off();
     // p_full lives in rank 0: one arrival per warp (released at cluster scope in a pair)
-    const uint32_t p_full_addr0 = C::NCTA == 2 ? mapa_shared(smem_u32(&sb.p_full[0]), 0) : 0u;
+    const uint32_t p_full_addr0 = C::PAIR ? mapa_shared(smem_u32(&sb.p_full[0]), 0) : 0u;
+    // head-dim split: the peer's score buffer and barriers, and the exchanges done
+    const uint32_t xs_peer = C::SPLITD ? mapa_shared(smem_u32(smem + C::XS_OFF), rank ^ 1) : 0u;
+    const uint32_t x_full_peer = C::SPLITD ? mapa_shared(smem_u32(&sb.x_full[0]), rank ^ 1) : 0u;
+    const uint32_t x_empty_peer = C::SPLITD ? mapa_shared(smem_u32(&sb.x_empty[0]), rank ^ 1) : 0u;
+    int xs = 0, xr = 0;  // tiles of partial scores sent to / received from the peer
     // The row's global inputs (range-table entry, sink), loaded one item
     // ahead so that their latency hides behind the current item's tiles.
     struct RowLoads {
@@ -817,7 +854,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     ok = consume_plan(sb, n++, lane, cur, p.err);
     RowCtx rc = row_ctx(cur, row_loads(cur));
     while (ok && !cur.last) {
-      const Item& it = cur.it;
       // Take the next item's plan now and start its row loads; they are
       // used only after this item's tiles.
       PlanEntry nxt;
@@ -825,9 +861,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       if (!ok) nxt.last = 1;
       const RowLoads nloads = row_loads(nxt);
       const Plan& pl = cur.pl;
-      const int head = rc.head;
-      const int qi = rc.qi;
-      const bool row_valid = rc.valid;
       const RowVis vis = rc.vis;
       const float sink_l2 = rc.sink * 1.4426950408889634f;  // log2 units
       const float sink_raw = rc.sink / p.m.scale;            // units of the raw q.k score
@@ -838,11 +871,48 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       float l_sum = (null_mode && half == 0) ? 1.f : 0.f;
       float l_lse = l_sum;
 
-      for (int j = 0; j < pl.n_tiles; ++j) {
+      // A head-dim split runs one tile behind: step js sends tile js's
+      // partial scores to the peer, then finishes tile js - 1, whose peer
+      // partial has had a whole step to arrive.
+      const int steps = pl.n_tiles + (C::SPLITD ? 1 : 0);
+      for (int js = 0; js < steps; ++js) {
+        if constexpr (C::SPLITD) {
+          if (js < pl.n_tiles) {
+            const int ts = T + js;
+            if (!mbar_wait(&sb.s_full[ts & 1], (ts >> 1) & 1, &sb.abort_flag, p.err, kDevTimeoutMma)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            uint32_t ps[HC];
+            const uint32_t pcol = tmem + lane_base + C::S_COL + (ts & 1) * BN;
+#pragma unroll
+            for (int c = 0; c < HC / 32; ++c)
+              tmem_ld_32x32b_x32(pcol + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&ps[c * 32]));
+#pragma unroll
+            for (int c = 0; c < HC / 32; ++c) tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(&ps[c * 32]));
+            // the slot's previous tile (two back) must have been read by the peer
+            const int slot = xs & 1;
+            if (xs >= 2 &&
+                !mbar_wait_cluster(&sb.x_empty[slot], ((xs - 2) >> 1) & 1, &sb.abort_flag, p.err, kDevTimeoutSoftmax)) {
+              ok = false;
+              break;
+            }
+            const uint32_t dst = xs_peer + static_cast<uint32_t>(slot * kBM * BN * 4 + quarter * (BN / 4) * 512 + lane * 16);
+#pragma unroll
+            for (int c = 0; c < BN / 4; ++c)
+              st_cluster_v4(dst + c * 512, ps[4 * c], ps[4 * c + 1], ps[4 * c + 2], ps[4 * c + 3]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster_release(x_full_peer + slot * 8);
+            ++xs;
+          }
+          if (js == 0) continue;
+        }
+        const int j = C::SPLITD ? js - 1 : js;
         const int t = T + j;
         const int kb = pl.kb_lo + j;
         const uint32_t scol = tmem + lane_base + C::S_COL + (t & 1) * BN;
-        if (!mbar_wait(&sb.s_full[t & 1], (t >> 1) & 1, &sb.abort_flag, p.err, kDevTimeoutMma)) {
+        if (!C::SPLITD && !mbar_wait(&sb.s_full[t & 1], (t >> 1) & 1, &sb.abort_flag, p.err, kDevTimeoutMma)) {
           ok = false;
           break;
         }
@@ -853,6 +923,34 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           tmem_ld_32x32b_x32(scol + half * HC + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[c * 32]));
 #pragma unroll
         for (int c = 0; c < HC / 32; ++c) tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(&s[c * 32]));
+
+        if constexpr (C::SPLITD) {
+          // The row's scores are the sum of both CTAs' partial products over
+          // their halves of the head dimension: add the peer's partial of this
+          // tile (sent a step ago) to this CTA's.  Both CTAs add the same two
+          // fp32 values, so both go on with identical scores.  A slot holds,
+          // per warp quarter and 4-score chunk, the 32 lanes' 16 bytes side by
+          // side, so every warp-wide remote store and local load covers 512
+          // contiguous bytes.
+          const int slot = xr & 1;
+          if (!mbar_wait_cluster(&sb.x_full[slot], (xr >> 1) & 1, &sb.abort_flag, p.err, kDevTimeoutSoftmax)) {
+            ok = false;
+            break;
+          }
+          const uint4* src = reinterpret_cast<const uint4*>(smem + C::XS_OFF + slot * kBM * BN * 4 +
+                                                            quarter * (BN / 4) * 512) + lane;
+#pragma unroll
+          for (int c = 0; c < BN / 4; ++c) {
+            const uint4 v = src[c * 32];
+            s[4 * c] = __float_as_uint(__uint_as_float(s[4 * c]) + __uint_as_float(v.x));
+            s[4 * c + 1] = __float_as_uint(__uint_as_float(s[4 * c + 1]) + __uint_as_float(v.y));
+            s[4 * c + 2] = __float_as_uint(__uint_as_float(s[4 * c + 2]) + __uint_as_float(v.z));
+            s[4 * c + 3] = __float_as_uint(__uint_as_float(s[4 * c + 3]) + __uint_as_float(v.w));
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster_release(x_empty_peer + slot * 8);
+          ++xr;
+        }
 
         // Mask: one bit per key of this thread's columns.  Scores stay in raw
         // q.k units; the scale folds into the exponent's FFMA (scale > 0).
@@ -951,7 +1049,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          if constexpr (C::NCTA == 2) mbar_arrive_cluster(p_full_addr0 + (t & 1) * 8);
+          if constexpr (C::PAIR) mbar_arrive_cluster(p_full_addr0 + (t & 1) * 8);
           else mbar_arrive(&sb.p_full[t & 1]);
         }
         if (!ok) break;
@@ -999,10 +1097,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-    const int pos_off = rank * (kBM / p.gpack);
+    const int pos_off = row_pos_off();
     const bool out_v8 = (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0;
     const float2* rowinfo = reinterpret_cast<const float2*>(smem + C::ROW_OFF);
-    const uint32_t o_free_addr0 = C::NCTA == 2 ? mapa_shared(smem_u32(&sb.o_free), 0) : 0u;
+    const uint32_t o_free_addr0 = C::PAIR ? mapa_shared(smem_u32(&sb.o_free), 0) : 0u;
+    const int oc0 = C::SPLITD ? rank * C::OC : 0;  // this CTA's first output column of the item
     bool ok = true;
     int T = 0, hk = 0;
     for (int n = 0; ok; ++n) {
@@ -1031,10 +1130,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         tc_fence_after();
       }
       __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.out) +
-                            (static_cast<size_t>(e.it.q0 + qi) * p.hq + head) * C::D + e.it.dv0;
+                            (static_cast<size_t>(e.it.q0 + qi) * p.hq + head) * C::D + e.it.dv0 + oc0;
       const uint32_t ocol = tmem + lane_base + C::O_COL;
 #pragma unroll 1
-      for (int c = 0; c < C::DV / 32; ++c) {
+      for (int c = 0; c < C::OC / 32; ++c) {
         uint32_t o[32];
         if (has_tiles) {
           tmem_ld_32x32b_x32(ocol + c * 32, o);
@@ -1043,12 +1142,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 #pragma unroll
           for (int v = 0; v < 32; ++v) o[v] = 0u;
         }
-        if (has_tiles && c == C::DV / 32 - 1) {
+        if (has_tiles && c == C::OC / 32 - 1) {
           // O is out of TMEM: the next item's first PV may overwrite it.
           tc_fence_before();
           __syncwarp();
           if (lane == 0) {
-            if constexpr (C::NCTA == 2) mbar_arrive_cluster(o_free_addr0);
+            if constexpr (C::PAIR) mbar_arrive_cluster(o_free_addr0);
             else mbar_arrive(&sb.o_free);
           }
         }
@@ -1068,7 +1167,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           }
         }
       }
-      if (valid && p.lse != nullptr && e.it.dv0 == 0)
+      if (valid && p.lse != nullptr && e.it.dv0 == 0 && oc0 == 0)
         p.lse[static_cast<size_t>(head) * p.total_q + e.it.q0 + qi] = info.y;
       T += e.pl.n_tiles;
     }
@@ -1077,10 +1176,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
-  if constexpr (C::NCTA == 2) cluster_sync_all();  // rank 0's MMAs and drain are complete
+  // a pair: rank 0's MMAs and drain are complete; a head-dim split: the peer
+  // no longer writes into this CTA's shared memory
+  if constexpr (C::NCTA == 2) cluster_sync_all();
   tc_fence_after();
   if (warp == 1) {
-    if constexpr (C::NCTA == 2) tmem_dealloc_pair(tmem, C::TMEM_COLS);
+    if constexpr (C::PAIR) tmem_dealloc_pair(tmem, C::TMEM_COLS);
     else tmem_dealloc(tmem, C::TMEM_COLS);
   }
 }
@@ -1088,7 +1189,20 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 using Cfg64 = Cfg<64, 64, 128, 4, 4, 1>;
 using Cfg128 = Cfg<128, 128, 128, 4, 4, 2>;
 using Cfg256 = Cfg<256, 256, 128, 2, 2, 2>;
+// D = 512: O of all 512 value columns does not fit TMEM next to S, so the
+// default splits the value dimension over two items (each recomputes S).  The
+// alternative keeps O resident by splitting the head dimension over a 2-CTA
+// cluster (no recomputation, partial scores exchanged every tile); it meets
+// the same tolerances but measured slower on GB300 (the exchange and its
+// cluster-scope release cost more per tile than the recomputed QK), so it is
+// opt-in (environment MVP_D512_HEAD_SPLIT=1).
 using Cfg512 = Cfg<512, 256, 64, 1, 1, 1>;
+using Cfg512S = Cfg<512, 512, 64, 2, 1, 2, 1>;
+
+bool d512_head_split() {
+  const char* v = getenv("MVP_D512_HEAD_SPLIT");
+  return v != nullptr && v[0] == '1';
+}
 
 template <class C>
 cudaError_t launch_cfg(const PrefillParams& p, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
@@ -1138,13 +1252,19 @@ cudaError_t launch_cfg(const PrefillParams& p, const CUtensorMap& mq, const CUte
 
 }  // namespace
 
+template <class C>
+PrefillShape shape_of() {
+  return {C::BN, C::DV, C::DV_SPLIT, C::BN, C::KROWS, C::NCTA, C::ITEM_ROWS, C::SPLITD ? 2 : 1, C::DQ, C::OC,
+          C::ITEM_ROWS};
+}
+
 PrefillShape prefill_tile_shape(int head_dim) {
   switch (head_dim) {
-    case 64: return {Cfg64::BN, Cfg64::DV, Cfg64::DV_SPLIT, Cfg64::BN, Cfg64::KROWS, Cfg64::NCTA};
-    case 128: return {Cfg128::BN, Cfg128::DV, Cfg128::DV_SPLIT, Cfg128::BN, Cfg128::KROWS, Cfg128::NCTA};
-    case 256: return {Cfg256::BN, Cfg256::DV, Cfg256::DV_SPLIT, Cfg256::BN, Cfg256::KROWS, Cfg256::NCTA};
-    case 512: return {Cfg512::BN, Cfg512::DV, Cfg512::DV_SPLIT, Cfg512::BN, Cfg512::KROWS, Cfg512::NCTA};
-    default: return {0, 0, 0, 0, 0, 0};
+    case 64: return shape_of<Cfg64>();
+    case 128: return shape_of<Cfg128>();
+    case 256: return shape_of<Cfg256>();
+    case 512: return d512_head_split() ? shape_of<Cfg512S>() : shape_of<Cfg512>();
+    default: return {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
   }
 }
 
@@ -1154,7 +1274,8 @@ cudaError_t launch_prefill(int head_dim, const PrefillParams& p, const CUtensorM
     case 64: return launch_cfg<Cfg64>(p, mq, mk, mv, stream);
     case 128: return launch_cfg<Cfg128>(p, mq, mk, mv, stream);
     case 256: return launch_cfg<Cfg256>(p, mq, mk, mv, stream);
-    case 512: return launch_cfg<Cfg512>(p, mq, mk, mv, stream);
+    case 512:
+      return d512_head_split() ? launch_cfg<Cfg512S>(p, mq, mk, mv, stream) : launch_cfg<Cfg512>(p, mq, mk, mv, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -71,7 +71,12 @@ struct PrefillShape {
   int dv_split;  // CTAs per (q tile, head group) along the value dimension
   int v_box_keys;  // keys per V TMA box
   int k_box_keys;  // keys per K TMA box (a CTA pair's CTA loads half a tile)
-  int ncta;        // CTAs sharing each MMA: 1, or 2 (a cluster pair)
+  int ncta;        // CTAs of a cluster working on one item: 1 or 2
+  int item_rows;   // query rows (position x head) of one item
+  int issuers;     // CTAs of an item that issue MMAs (2 for a head-dim split)
+  int qk_k;        // head dims one issuing CTA multiplies in QK
+  int oc;          // O columns one issuing CTA accumulates
+  int mma_m;       // M of each MMA
 };
 PrefillShape prefill_tile_shape(int head_dim);
 

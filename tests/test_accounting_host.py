@@ -21,12 +21,19 @@ from masked_varlen_prefill_gb300 import workloads
 from oracle import attention as oatt
 from oracle import range_table as ort
 
-# tile shapes of the kernels (keys per prefill tile, query rows per MMA,
-# value columns per item, items per q tile along the value dimension,
-# keys per decode tile)
+# tile shapes of the kernels: keys per prefill tile; per key tile, the
+# tcgen05.mma instructions and their FLOPs (D 64: one CTA, M 128; D 128 / 256:
+# a CTA pair, M 256; D 512: one CTA, M 128, half the value columns per item);
+# keys per decode tile
 BN = {64: 128, 128: 128, 256: 128, 512: 64}
-M_ROWS = {64: 128, 128: 256, 256: 256, 512: 128}
-DV = {64: 64, 128: 128, 256: 256, 512: 256}
+INSTR_PER_TILE = {64: 64 // 16 + 128 // 16, 128: 128 // 16 + 128 // 16, 256: 256 // 16 + 128 // 16,
+                  512: 512 // 16 + 64 // 16}
+FLOPS_PER_TILE = {64: 2 * 128 * 128 * (64 + 64), 128: 2 * 256 * 128 * (128 + 128), 256: 2 * 256 * 128 * (256 + 256),
+                  512: 2 * 128 * 64 * (512 + 256)}
+# the opt-in D 512 head-dim split: two CTAs, each M 128 over half the head
+# dimension and half the value columns
+HEAD_SPLIT_INSTR = 2 * (256 // 16 + 64 // 16)
+HEAD_SPLIT_FLOPS = 2 * (2 * 128 * 64 * (256 + 256))
 KT = {64: 128, 128: 64, 256: 32, 512: 32}
 
 
@@ -102,8 +109,23 @@ def test_scaled_workloads_exact_and_executed(name):
     d = w.head_dim
     # every visible pair of a prefill row is inside a visited tile
     assert c["prefill_mma_flops"] >= 4.0 * d * w.num_heads_q * pre
-    assert c["prefill_mma_instructions"] == c["prefill_tiles"] * (d // 16 + BN[d] // 16)
-    assert c["prefill_mma_flops"] == c["prefill_tiles"] * 2.0 * M_ROWS[d] * BN[d] * (d + DV[d])
+    assert c["prefill_mma_instructions"] == c["prefill_tiles"] * INSTR_PER_TILE[d]
+    assert c["prefill_mma_flops"] == c["prefill_tiles"] * FLOPS_PER_TILE[d]
+
+
+def test_d512_head_split_accounting(monkeypatch):
+    w = workloads.scaled_workload("global_causal_d512")
+    base = _counts(w)
+    monkeypatch.setenv("MVP_D512_HEAD_SPLIT", "1")
+    split = _counts(w)
+    # the same visible pairs; half the items (no value split), each covering
+    # the same tiles; no recomputed QK
+    assert split["visible_prefill"] == base["visible_prefill"]
+    assert split["prefill_items"] * 2 == base["prefill_items"]
+    assert split["prefill_tiles"] * 2 == base["prefill_tiles"]
+    assert split["prefill_mma_instructions"] == split["prefill_tiles"] * HEAD_SPLIT_INSTR
+    assert split["prefill_mma_flops"] == split["prefill_tiles"] * HEAD_SPLIT_FLOPS
+    assert split["prefill_mma_flops"] * 3 == base["prefill_mma_flops"] * 2
 
 
 @pytest.mark.parametrize("seed", range(16))
