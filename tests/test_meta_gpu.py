@@ -253,3 +253,41 @@ def test_empty_stage_writes_an_all_padding_table():
     assert int(meta.range_covered.item()) == 0
     assert (meta.query_start_loc.cpu().numpy() == 0).all()
     meta.close()
+
+
+def test_stage_waits_for_the_copy_in_flight():
+    """Stage a new batch right after a replay was launched (no synchronize):
+    the staging call waits for the replay's copy, so the replay reads the
+    first batch and the next replay the second."""
+    dev = torch.device("cuda")
+    sinks = torch.randn(HQ, generator=torch.Generator(device=dev).manual_seed(6), device=dev)
+    g = _Graphed(dev, sinks)
+    g.capture()
+    b1 = _batch(41, 2, 2)
+    b2 = _batch(42, 1, 3)
+    q1, k1, v1 = _inputs(b1[0], b1[1], 41, dev)
+    n1 = int(b1[0][-1])
+    g.q[:n1].copy_(q1)
+    g.k[:k1.shape[0]].copy_(k1)
+    g.v[:v1.shape[0]].copy_(v1)
+    g.meta.stage(*b1)
+    g.graph.replay()
+    out1 = g.out.clone()  # stream-ordered after the first replay
+    g.meta.stage(*b2)     # waits for the first replay's metadata copy only
+    q2, k2, v2 = _inputs(b2[0], b2[1], 42, dev)
+    n2 = int(b2[0][-1])
+    g.q[:n2].copy_(q2)
+    g.k[:k2.shape[0]].copy_(k2)
+    g.v[:v2.shape[0]].copy_(v2)
+    g.graph.replay()
+    torch.cuda.synchronize()
+    assert mvp.get_last_device_error() == 0
+    for (qsl, k_lens, bound, ranges), q, k, v, out, n in [(b1, q1, k1, v1, out1, n1), (b2, q2, k2, v2, g.out, n2)]:
+        ref_table, written = _oracle_table(qsl, bound, ranges)
+        cu_k = np.zeros(len(k_lens) + 1, np.int32)
+        cu_k[1:] = np.cumsum(k_lens)
+        ro, rl = oatt.attention_forward(q.cpu(), k.cpu(), v.cpu(), qsl, cu_k, True, WINDOW_LEFT, -1, D ** -0.5,
+                                        range_table=ref_table if written else None, sinks=sinks.cpu(),
+                                        sink_mode=mvp.SINK_NULL_LOGIT)
+        gh.compare(out[:n], None, ro, rl, what="in-flight staging")
+    g.meta.close()
