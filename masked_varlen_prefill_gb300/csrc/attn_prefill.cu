@@ -359,7 +359,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const bool use_table = table_active(p.m);
   const int n_items = p.n_qtiles * (p.num_reqs - p.req_offset) * p.hkv * p.n_hgroups * C::DV_SPLIT;
   constexpr int BN = C::BN;
   const int rank = C::NCTA == 2 ? static_cast<int>(cluster_rank()) : 0;
@@ -421,6 +420,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
   if constexpr (C::NCTA == 2) cluster_sync_all();  // the peer's barriers are initialised
   tc_fence_after();
   const uint32_t tmem = sb.tmem_base;
+  // Launched with programmatic serialization: the setup above overlapped the
+  // previous kernel in the stream (the range fill); every global input,
+  // including the table's covered flag, is read after this point.
+  griddep_wait();
+  const bool use_table = table_active(p.m);
 
   uint8_t* sQ = smem + C::Q_OFF;
   uint8_t* sK = smem + C::K_OFF;
@@ -1215,7 +1219,7 @@ cudaError_t launch_cfg(const PrefillParams& p, const CUtensorMap& mq, const CUte
   if (n_items <= 0) return cudaSuccess;
   if (n_items > INT_MAX) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = C::NCTA;
   attr[0].val.clusterDim.y = 1;
@@ -1223,8 +1227,10 @@ cudaError_t launch_cfg(const PrefillParams& p, const CUtensorMap& mq, const CUte
   cfg.blockDim = dim3(C::THREADS);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = stream;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 1;  // (the occupancy query below sees the cluster shape only)
   // Persistent groups: as many CTAs (pairs) as can be resident at once (the
   // pair count is queried once per device; clusters must fit within a GPC).
   int groups = p.n_ctas / C::NCTA;
@@ -1245,6 +1251,7 @@ cudaError_t launch_cfg(const PrefillParams& p, const CUtensorMap& mq, const CUte
   }
   if (n_items < groups) groups = static_cast<int>(n_items);
   cfg.gridDim = dim3(groups * C::NCTA);
+  cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

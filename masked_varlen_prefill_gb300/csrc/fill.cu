@@ -13,6 +13,7 @@
 // rows_written receives the page's return value.  Rows at or past
 // query_start_loc[num_reqs] (a batch padded to a fixed capacity) get (-1, -1).
 #include "mvp_internal.cuh"
+#include "ptx.cuh"
 
 namespace mvp {
 
@@ -21,6 +22,9 @@ namespace {
 constexpr int kFillThreads = 256;
 
 __global__ void __launch_bounds__(kFillThreads) fill_query_ranges_kernel(FillParams p) {
+  // The attention call that follows may set up while this kernel runs (it
+  // waits for this kernel's writes before reading the table).
+  griddep_launch_dependents();
   const int t = blockIdx.x * kFillThreads + threadIdx.x;
   if (t >= p.num_tokens) return;
   if (t >= __ldg(p.qsl + p.num_reqs)) {  // a row past the batch (capacity padding)

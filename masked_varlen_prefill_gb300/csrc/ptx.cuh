@@ -120,6 +120,16 @@ __device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, v
   }
 }
 
+// --------------------------------------------------- programmatic launch
+// A kernel launched with programmatic stream serialization may start while
+// the kernel before it in the stream still runs; griddep_wait blocks until
+// that kernel has completed and its memory operations are visible.
+// griddep_launch_dependents lets the next such kernel start early.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
