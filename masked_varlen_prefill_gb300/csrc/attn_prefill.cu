@@ -1200,7 +1200,7 @@ using Cfg256 = Cfg<256, 256, 128, 2, 2, 2>;
 // the same tolerances but measured slower on GB300 (the exchange and its
 // cluster-scope release cost more per tile than the recomputed QK), so it is
 // opt-in (environment MVP_D512_HEAD_SPLIT=1).
-using Cfg512 = Cfg<512, 256, 64, 1, 1, 1>;
+using Cfg512 = Cfg<512, 256, 64, 2, 2, 2>;
 using Cfg512S = Cfg<512, 512, 64, 2, 1, 2, 1>;
 
 bool d512_head_split() {

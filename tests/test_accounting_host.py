@@ -23,13 +23,13 @@ from oracle import range_table as ort
 
 # tile shapes of the kernels: keys per prefill tile; per key tile, the
 # tcgen05.mma instructions and their FLOPs (D 64: one CTA, M 128; D 128 / 256:
-# a CTA pair, M 256; D 512: one CTA, M 128, half the value columns per item);
+# a CTA pair, M 256; D 512: a CTA pair, M 256, half the value columns per item);
 # keys per decode tile
 BN = {64: 128, 128: 128, 256: 128, 512: 64}
 INSTR_PER_TILE = {64: 64 // 16 + 128 // 16, 128: 128 // 16 + 128 // 16, 256: 256 // 16 + 128 // 16,
                   512: 512 // 16 + 64 // 16}
 FLOPS_PER_TILE = {64: 2 * 128 * 128 * (64 + 64), 128: 2 * 256 * 128 * (128 + 128), 256: 2 * 256 * 128 * (256 + 256),
-                  512: 2 * 128 * 64 * (512 + 256)}
+                  512: 2 * 256 * 64 * (512 + 256)}
 # the opt-in D 512 head-dim split: two CTAs, each M 128 over half the head
 # dimension and half the value columns
 HEAD_SPLIT_INSTR = 2 * (256 // 16 + 64 // 16)
@@ -118,14 +118,14 @@ def test_d512_head_split_accounting(monkeypatch):
     base = _counts(w)
     monkeypatch.setenv("MVP_D512_HEAD_SPLIT", "1")
     split = _counts(w)
-    # the same visible pairs; half the items (no value split), each covering
-    # the same tiles; no recomputed QK
+    # the same visible pairs; items of 128 rows with every value column (the
+    # default's items are 256 rows with half of them); QK is not recomputed
+    # per value half, so at most two thirds of the default's MMA work (less
+    # where the narrower items skip more causal tiles)
     assert split["visible_prefill"] == base["visible_prefill"]
-    assert split["prefill_items"] * 2 == base["prefill_items"]
-    assert split["prefill_tiles"] * 2 == base["prefill_tiles"]
     assert split["prefill_mma_instructions"] == split["prefill_tiles"] * HEAD_SPLIT_INSTR
     assert split["prefill_mma_flops"] == split["prefill_tiles"] * HEAD_SPLIT_FLOPS
-    assert split["prefill_mma_flops"] * 3 == base["prefill_mma_flops"] * 2
+    assert split["prefill_mma_flops"] * 3 <= base["prefill_mma_flops"] * 2
 
 
 @pytest.mark.parametrize("seed", range(16))
