@@ -487,10 +487,10 @@ def run_gpu(args, world, rank, local):
     covered = torch.empty(1, dtype=torch.int32, device=dev) if ranges is not None else None
     out = torch.empty_like(q)
     max_q, max_k = max(w.q_lens), max(w.k_lens)
-    ws = None
-    if n_dec > 0:
-        nbytes = mvp.attn_workspace_size(n_dec, w.num_heads_q, w.head_dim, max_k)
-        ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev) if nbytes else None
+    # workspace: the prefill work queue (header) and the decode split partials;
+    # uninitialised, as a serving engine would allocate it once
+    nbytes = mvp.attn_workspace_size(n_dec, w.num_heads_q, w.head_dim, max_k)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev) if nbytes else None
     paged = None
     if args.paged:
         kc, vc, bt, sl = workloads.to_paged(k, v, w.k_lens, args.paged, seed=w.seed)

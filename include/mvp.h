@@ -25,7 +25,8 @@
  *     nothing is written then.  Return values are mvp_status codes.
  *   - The library keeps one 4-byte device error word per device (allocated on
  *     the first call on that device).  Kernels that hit a bounded-wait
- *     timeout record a code there and unwind instead of hanging;
+ *     timeout record a code there and unwind instead of hanging (so does a
+ *     prefill kernel whose workspace queue another launch took over);
  *     mvp_get_last_device_error() reads and clears it.
  */
 #ifndef MVP_H_
@@ -44,7 +45,8 @@ typedef enum {
   MVP_ERR_CAPACITY = -2,     /* out_capacity < num_tokens (the page asserts)    */
   MVP_ERR_UNSUPPORTED = -3,  /* head_dim / head ratio / alignment not supported */
   MVP_ERR_CUDA = -4,         /* a CUDA runtime call or launch failed            */
-  MVP_ERR_DEVICE_TIMEOUT = -5 /* a kernel recorded a bounded-wait timeout       */
+  MVP_ERR_DEVICE_TIMEOUT = -5 /* a kernel recorded a bounded-wait timeout (or a
+                                 work queue shared by overlapping calls)     */
 } mvp_status;
 
 typedef enum {
@@ -91,11 +93,23 @@ int mvp_fill_query_ranges(const int32_t* ranges, int num_reqs, int max_ranges,
                           int32_t* rows_written, void* stream);
 
 /*
- * Bytes of caller-provided workspace that mvp_attn_fwd_varlen can use to
- * split long single-token (decode) rows across several CTAs.  num_reqs is the
+ * Bytes of caller-provided workspace that mvp_attn_fwd_varlen can use.  The
+ * first 256 bytes hold the prefill kernel's work queue: its persistent CTAs
+ * then claim work items one at a time (whichever CTA frees up first takes the
+ * next item) instead of walking a static stride, which evens out batches
+ * whose items differ in length.  The rest holds partial results that let long
+ * single-token (decode) rows be split across several CTAs.  num_reqs is the
  * number of requests the decode kernel covers (num_decode_reqs, or the whole
- * batch when that is -1).  0 is valid everywhere: without workspace every
- * decode row is handled by one CTA per KV head.
+ * batch when that is -1; 0: header only).  Returns 0 for negative num_reqs
+ * or non-positive sizes.
+ * The workspace needs no initialisation and is left valid for the next call
+ * (the queue word carries a per-launch tag, so no reset is needed).  Two calls
+ * that may run at the same time on the GPU (different streams) need separate
+ * workspaces; a kernel that finds its queue taken over records a device
+ * error (mvp_get_last_device_error) and stops claiming.  Workspace is
+ * optional: without it (NULL, fewer than 256 bytes, or not 16-byte aligned)
+ * the prefill items are walked with a static stride and every decode row is
+ * handled by one CTA per KV head.
  */
 size_t mvp_attn_workspace_size(int num_reqs, int num_heads_q, int head_dim, int max_k_len);
 

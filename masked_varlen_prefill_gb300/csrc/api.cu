@@ -133,11 +133,11 @@ int mvp_fill_query_ranges(const int32_t* ranges, int num_reqs, int max_ranges, c
 }
 
 size_t mvp_attn_workspace_size(int num_reqs, int num_heads_q, int head_dim, int max_k_len) {
-  if (num_reqs <= 0 || num_heads_q <= 0 || head_dim <= 0 || max_k_len <= 0) return 0;
+  if (num_reqs < 0 || num_heads_q <= 0 || head_dim <= 0 || max_k_len <= 0) return 0;
   int splits = (max_k_len + kDecodeChunk - 1) / kDecodeChunk;
   if (splits > kMaxSplits) splits = kMaxSplits;
-  if (splits < 2) return 0;
-  return static_cast<size_t>(num_reqs) * num_heads_q * splits * (head_dim + 2) * sizeof(float);
+  if (splits < 2 || num_reqs == 0) return mvp::kWorkspaceHeader;
+  return mvp::kWorkspaceHeader + static_cast<size_t>(num_reqs) * num_heads_q * splits * (head_dim + 2) * sizeof(float);
 }
 
 }  // extern "C"
@@ -221,6 +221,18 @@ int attn_fwd_impl(const void* q, void* out, float* lse, const int32_t* cu_seqlen
 
   const int group = num_heads_q / num_heads_kv;
   int launches = 0;
+  // Workspace: the prefill work-queue word in its header, the decode split
+  // partials after it.  Without a usable header, static scheduling and no
+  // split.
+  unsigned long long* queue = nullptr;
+  void* partials = nullptr;
+  size_t partial_bytes = 0;
+  if (workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 15u) == 0 &&
+      workspace_bytes >= kWorkspaceHeader) {
+    queue = static_cast<unsigned long long*>(workspace);
+    partials = static_cast<unsigned char*>(workspace) + kWorkspaceHeader;
+    partial_bytes = workspace_bytes - kWorkspaceHeader;
+  }
 
   const int prefill_first = num_decode_reqs < 0 ? 0 : num_decode_reqs;
   const int decode_count = num_decode_reqs < 0 ? num_reqs : num_decode_reqs;
@@ -246,6 +258,7 @@ int attn_fwd_impl(const void* q, void* out, float* lse, const int32_t* cu_seqlen
     pp.skip_decode = 1;
     pp.req_offset = prefill_first;
     pp.n_ctas = num_sms;
+    pp.queue = queue;
 
     CUtensorMap mq, mk, mv;
     if (!encode_3d(&mq, q, head_dim, num_heads_q, total_q, 64, gpack, bmp, true) ||
@@ -278,16 +291,16 @@ int attn_fwd_impl(const void* q, void* out, float* lse, const int32_t* cu_seqlen
     int splits = static_cast<int>((span + kDecodeChunk - 1) / kDecodeChunk);
     if (splits > kMaxSplits) splits = kMaxSplits;
     const size_t per_split = static_cast<size_t>(decode_count) * num_heads_q * (head_dim + 2) * sizeof(float);
-    if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 15u) != 0) splits = 1;
-    else if (static_cast<size_t>(splits) * per_split > workspace_bytes)
-      splits = static_cast<int>(workspace_bytes / per_split);
+    if (partials == nullptr) splits = 1;
+    else if (static_cast<size_t>(splits) * per_split > partial_bytes)
+      splits = static_cast<int>(partial_bytes / per_split);
     if (splits < 2) splits = 1;
     long long chunk = (span + splits - 1) / splits;
     chunk = ((chunk + kt - 1) / kt) * kt;
     if (chunk > INT_MAX) chunk = INT_MAX;
     dp.n_splits = splits;
     dp.chunk = static_cast<int>(chunk);
-    dp.partial = splits > 1 ? static_cast<float*>(workspace) : nullptr;
+    dp.partial = splits > 1 ? static_cast<float*>(partials) : nullptr;
     const int per_cta = decode_heads_per_cta(head_dim, group);
     if (static_cast<long long>(num_heads_kv) * ((group + per_cta - 1) / per_cta) > 65535) return MVP_ERR_UNSUPPORTED;
     CUtensorMap mk, mv;

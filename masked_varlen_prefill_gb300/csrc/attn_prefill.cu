@@ -13,15 +13,18 @@
 //   head share a tile: row r is (position r / G_pack, head h0 + r % G_pack), so
 //   a K/V tile read from L2 serves G_pack heads.  The Q tile is a single 3-D
 //   TMA box (64 dims, G_pack heads, 128 / G_pack positions), 128-byte swizzled.
-// * D = 128 and 256 run as CTA pairs (a 2-CTA cluster, tcgen05 .cta_group::2):
-//   each MMA is M = 256 (each CTA's 128 rows, scores and O in its own TMEM),
-//   each CTA loads only half of every K tile (its keys) and half of every V
-//   tile (its value columns), and rank 0 issues the MMAs for both.  A tile
-//   costs each SM half the L2 -> shared-memory bytes and half the shared
-//   memory, which buys two K and two V stages at D = 256.
-// * Persistent CTAs (one per SM) walk the items with a static stride, q tile
-//   fastest so that concurrent CTAs share K/V windows in L2.  Every role computes each item's geometry
-//   and key-tile plan itself (a warp reduction over the tile's 128 rows), and
+// * D = 128, 256 and 512 run as CTA pairs (a 2-CTA cluster, tcgen05
+//   .cta_group::2): each MMA is M = 256 (each CTA's 128 rows, scores and O in
+//   its own TMEM), each CTA loads only half of every K tile (its keys) and half
+//   of every V tile (its value columns), and rank 0 issues the MMAs for both.
+//   A tile costs each SM half the L2 -> shared-memory bytes and half the
+//   shared memory, which buys two K and two V stages at D = 256 and 512.
+// * Persistent CTAs (one per SM) take the items, numbered q tile fastest so
+//   that concurrent CTAs share K/V windows in L2, from a work queue in the
+//   caller's workspace (one item ahead of the work in progress), or without
+//   workspace with a static stride.  A scheduler warp computes each item's
+//   geometry and key-tile plan (a warp reduction over the item's rows) into a
+//   ring that every role reads, and
 //   all barrier phases run on CTA-wide counters, so the producer and the MMA
 //   issuer move on to the next item's Q, K and QK while the softmax warps
 //   still finish the current item.
@@ -171,11 +174,24 @@ struct PlanEntry {
 };
 
 constexpr int kPlanRing = 4;
+// Work queue: items claimed ahead of the producer's loads.  The softmax warps
+// take the next item's plan as they start an item (to load its rows' inputs
+// early), so one claim ahead leaves them waiting on the claim and plan at
+// every item start; two hide that behind a whole item.
+constexpr int kClaimAhead = 2;
+// Rounds of items (one per CTA or pair) at the end of the item space that
+// come from the work queue; the rounds before keep the static stride.
+constexpr int kQueueRounds = 1;
 
 struct __align__(8) Barriers {
   uint64_t plan_full[kPlanRing];
   uint64_t plan_empty[kPlanRing];
   PlanEntry plans[kPlanRing];
+  uint64_t claim_full[kPlanRing];   // work queue, pair: rank 0 wrote the item it claimed into claims[i] of rank 1
+  uint64_t claim_empty[kPlanRing];  // ... and rank 1 has read it (rank 0's barrier)
+  int claims[kPlanRing];
+  uint64_t plan_taken[kPlanRing];  // work queue: the producer took the entry in slot i
+  int n_static;                    // scheduler: items walked with the static stride
   uint64_t q_full;
   uint64_t q_empty;
   uint64_t k_full[4];
@@ -266,6 +282,48 @@ __device__ __forceinline__ int next_candidate(int item, const Item& it, const Pr
   }
   const long long next = item + ((target - item + stride - 1) / stride) * stride;
   return next > INT_MAX ? INT_MAX : static_cast<int>(next);
+}
+
+// Work-queue words (the prefill scheduler's, in the caller's workspace):
+// (launch tag << 32) | counter, the tag being this launch's %gridid.
+// queue_add adds 1 to the counter and returns its old value, or -1 when the
+// word keeps changing hands (another launch uses it at the same time; a
+// device error is recorded).  check: first use in this launch; a word that
+// carries another tag gets this one with the counter at 1 (returns 0).
+__device__ __forceinline__ long long queue_add(unsigned long long* word, bool check, int* err) {
+  const unsigned long long tag = grid_launch_id() << 32;
+  if (check) {
+    for (int tries = 0;; ++tries) {
+      const unsigned long long cur = atomicAdd(word, 0ull);
+      if ((cur & 0xffffffff00000000ull) == tag) break;
+      if (atomicCAS(word, cur, tag | 1ull) == cur) return 0;
+      if (tries > (1 << 16)) {
+        atomicCAS(err, 0, kDevQueueConflict);
+        return -1;
+      }
+    }
+  }
+  const unsigned long long v = atomicAdd(word, 1ull);
+  if ((v & 0xffffffff00000000ull) != tag) {
+    atomicCAS(err, 0, kDevQueueConflict);
+    return -1;
+  }
+  return static_cast<long long>(v & 0xffffffffull);
+}
+
+// A claiming CTA is done (also after an abort): count it in the second
+// word; the launch's last one resets both counters under its tag, so that a
+// later launch carrying the same tag (a graph replay) starts at item 0.  The
+// fences order every CTA's claims before its count, and the last count before
+// the reset.
+__device__ __forceinline__ void queue_finish(unsigned long long* words, int n_claimers, int* err) {
+  __threadfence();
+  if (queue_add(words + 1, true, err) == n_claimers - 1) {
+    __threadfence();
+    const unsigned long long tag = grid_launch_id() << 32;
+    atomicExch(words, tag);
+    atomicExch(words + 1, tag);
+  }
 }
 
 // Key-tile plan of an item (warp-collective, over all NCTA * 128 rows, so
@@ -376,6 +434,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       mbar_init(&sb.plan_full[i], 1);
       mbar_init(&sb.plan_empty[i], C::CONSUMER_WARPS - (leader ? 0 : 1));  // a pair's rank 1 issues no MMAs
     }
+    for (int i = 0; i < kPlanRing; ++i) {
+      mbar_init(&sb.claim_full[i], 1);
+      mbar_init(&sb.claim_empty[i], 1);
+    }
     mbar_init(&sb.q_full, 1);
     mbar_init(&sb.q_empty, 1);
     for (int i = 0; i < 4; ++i) {
@@ -404,6 +466,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       mbar_init(&sb.xchg[i][1], 64);
     }
     sb.abort_flag = 0;
+    for (int i = 0; i < kPlanRing; ++i) mbar_init(&sb.plan_taken[i], 1);
     mbar_fence_init();
   }
   if (warp == 1) {
@@ -447,7 +510,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       }
       bool ok = true;
       int n = 0, qn = 0, kc = 0, vc = 0;  // plans taken, Q / K / V tiles issued
-      int k_armed[4] = {0, 0, 0, 0}, v_armed[4] = {0, 0, 0, 0};
       // Next item that has key tiles (warp-collective); false at the end.
       auto next_item = [&](PlanEntry& e) -> bool {
         for (;;) {
@@ -455,6 +517,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             ok = false;
             return false;
           }
+          if (lane == 0 && p.queue != nullptr) mbar_arrive(&sb.plan_taken[(n - 1) % kPlanRing]);
           if (e.last) return false;
           if (e.pl.n_tiles > 0) return true;
         }
@@ -525,11 +588,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       // The slot cannot be reused before this warp consumes it.  Paged: the
       // plan's block ids start on their way into the other ids buffer, whose
       // item issued its last load before the warp's last sync.
-      auto prefetch_next_item = [&]() {
+      // Returns false while plan n is not published yet (then retried; the
+      // test is non-blocking, so the loads it sits between are not delayed).
+      auto prefetch_next_item = [&]() -> bool {
         const int slot = n % kPlanRing;
-        if (!__all_sync(kFullMask, mbar_try_wait(&sb.plan_full[slot], (n / kPlanRing) & 1))) return;
+        if (!__all_sync(kFullMask, mbar_test_wait(&sb.plan_full[slot], (n / kPlanRing) & 1))) return false;
         const PlanEntry e = sb.plans[slot];
-        if (e.last || e.pl.n_tiles == 0) return;
+        if (e.last || e.pl.n_tiles == 0) return true;
         if (lane == 0) {
 #pragma unroll
           for (int c = 0; c < C::QCH; ++c)
@@ -540,6 +605,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           cache_ids(e, cbuf ^ 1, false);
           ids_plan = n;
         }
+        return true;
       };
       auto load_q = [&](const PlanEntry& e) -> bool {
         if (qn > 0) {
@@ -587,7 +653,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             tma_load<C>(sK + s * C::K_BYTES + c * (C::KROWS * 128), &map_k, &sb.k_full[s], dq0 + c * 64, e.it.hkv,
                         e.it.k0 + key0);
         }
-        ++k_armed[s];
         ++kc;
         return true;
       };
@@ -617,7 +682,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             tma_load<C>(sV + s * C::V_BYTES + c * (BN * 128), &map_v, &sb.v_full[s], e.it.dv0 + rank * C::DVC + c * 64,
                         e.it.hkv, e.it.k0 + key0);
         }
-        ++v_armed[s];
         ++vc;
         return true;
       };
@@ -628,13 +692,17 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       ok = __shfl_sync(kFullMask, ok, 0);
       while (ok && have) {
         const int nt = cur.pl.n_tiles;
-        prefetch_next_item();
-        if (lane == 0)
-          for (int j = 0; ok && j + 1 < nt; ++j) {
+        // (the next plan may be published while this item's tiles are issued)
+        bool prefetched = false;
+        for (int j = 0;; ++j) {
+          if (!prefetched) prefetched = prefetch_next_item();
+          if (!ok || j + 1 >= nt) break;
+          if (lane == 0) {
             ok = load_k(cur, j + 1, cbuf);
             if (ok) ok = load_v(cur, j, cbuf);
           }
-        ok = __shfl_sync(kFullMask, ok, 0);
+          ok = __shfl_sync(kFullMask, ok, 0);
+        }
         PlanEntry nxt;
         const bool have_next = ok && next_item(nxt);
         if (PAGED && have_next) {
@@ -667,8 +735,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         volatile int own_flag = 0;
         if (qn > 0) mbar_wait(&sb.q_full, (qn - 1) & 1, &own_flag, nullptr, 0);
         for (int i = 0; i < 4; ++i) {
-          if (k_armed[i] > 0) mbar_wait(&sb.k_full[i], (k_armed[i] - 1) & 1, &own_flag, nullptr, 0);
-          if (v_armed[i] > 0) mbar_wait(&sb.v_full[i], (v_armed[i] - 1) & 1, &own_flag, nullptr, 0);
+          // stage i was last armed by tile i + KST * m, m = (issued - 1 - i) / KST (phase parity m)
+          if (i < C::KST && kc > i) mbar_wait(&sb.k_full[i], ((kc - 1 - i) / C::KST) & 1, &own_flag, nullptr, 0);
+          if (i < C::VST && vc > i) mbar_wait(&sb.v_full[i], ((vc - 1 - i) / C::VST) & 1, &own_flag, nullptr, 0);
         }
       }
     } else if (warp == 1 && leader) {
@@ -762,9 +831,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       // A pair's rank 1: its TMEM is allocated by this warp; rank 0 issues the MMAs.
     } else if (warp == C::SCHED_WARP) {
       // ------------------------------------------------------------ scheduler
-      // Walks this CTA's items (static stride), computes each valid item's
-      // geometry and key-tile plan, and publishes them through the plan ring,
-      // up to kPlanRing items ahead of the slowest consumer warp.
+      // Finds this CTA's items, computes each valid item's geometry and
+      // key-tile plan, and publishes them through the plan ring.  Items come
+      // from a static stride (up to kPlanRing items ahead of the slowest
+      // consumer warp) or, given a work-queue word, are claimed one at a time
+      // from it.
       int n = 0;
       bool ok = true;
       auto publish = [&](const PlanEntry& e) -> bool {
@@ -781,13 +852,104 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         return good;
       };
       const int n_groups = gridDim.x / C::NCTA;  // clusters (single CTAs when NCTA == 1)
-      for (int item = blockIdx.x / C::NCTA; ok && item < n_items; item += n_groups) {
+      // Items [0, n_static) are walked with a static stride, which keeps the
+      // CTAs in lockstep on neighbouring items; the last kQueueRounds rounds
+      // (all items when the stride leaves fewer) come from the work queue, so
+      // that the tail goes to whichever CTA frees up first.  Without a queue
+      // every item is static.
+      //
+      // Work queue: two 64-bit words, (launch tag << 32) | next item - n_static
+      // and (launch tag << 32) | CTAs done.  The last claiming CTA to finish
+      // resets the item counter to 0 under its tag, ready for the next launch
+      // (a graph replay may carry the same tag).  A launch that finds another
+      // tag (an uninitialised workspace, or one last used by another kernel)
+      // installs its own with the counter at 1, taking the first queued item;
+      // so the words need no initialisation.  Rank 0 claims entry c's item
+      // once the producer has taken entry c - kClaimAhead (it starts loading an
+      // item as the one before computes).  In a cluster of two, rank 1
+      // receives each claim (or the end) through its claim slots.  Items
+      // without rows are skipped by jumping to the next candidate
+      // (next_candidate; in the queue by moving its counter with atomicMax).
+      constexpr bool TWO = C::NCTA == 2;
+      const bool dyn = p.queue != nullptr;
+      // (kept in shared memory rather than a register: the control warps run
+      // on a reduced register budget)
+      if (lane == 0) sb.n_static = dyn ? max(0, n_items / n_groups - kQueueRounds) * n_groups : n_items;
+      __syncwarp();
+      const volatile int& n_static = sb.n_static;
+      auto claim = [&](bool first) -> int {  // lane 0; first: this CTA's first claim
+        const long long idx = queue_add(p.queue, first, p.err);
+        return idx >= 0 && idx < n_items - n_static ? n_static + static_cast<int>(idx) : INT_MAX;
+      };
+      int item = -1;
+      int qc = 0;  // claims made (rank 0) / received (rank 1)
+      for (int c = 0; ok; ++c) {  // c: plan entries
         PlanEntry e;
-        e.it = item_geometry<C, PAGED>(item, p);
-        if (!e.it.valid) {
-          item = next_candidate<C>(item, e.it, p, n_groups, lane) - n_groups;  // (the loop adds it back)
-          continue;
+        if (!dyn || item < n_static) {  // static phase
+          const int first = blockIdx.x / C::NCTA;
+          item = item < 0 ? first : (item >= n_items - n_groups ? INT_MAX : item + n_groups);
+          while (item < n_static) {  // skip items without rows
+            e.it = item_geometry<C, PAGED>(item, p);
+            if (e.it.valid) break;
+            item = next_candidate<C>(item, e.it, p, n_groups, lane);
+          }
         }
+        if (dyn && item >= n_static) {  // queue phase
+          const int slot = qc % kPlanRing;
+          if (!TWO || rank == 0) {
+            bool good = true;
+            const int ct = c - kClaimAhead;  // entry the producer must have taken
+            // (a suspending wait: a polling one takes issue slots from the
+            // softmax warps; the producer cannot be past entry c - 1 here, so
+            // the slot's phase parity is exact)
+            if (lane == 0 && ct >= 0)
+              good = mbar_wait(&sb.plan_taken[ct % kPlanRing], (ct / kPlanRing) & 1, &sb.abort_flag, p.err,
+                               kDevTimeoutOther);
+            if (lane == 0 && good) item = claim(qc == 0);
+            ok = __shfl_sync(kFullMask, good, 0);
+            item = __shfl_sync(kFullMask, item, 0);
+            while (ok && item < n_items) {  // skip items without rows
+              e.it = item_geometry<C, PAGED>(item, p);
+              if (e.it.valid) break;
+              const int target = next_candidate<C>(item, e.it, p, 1, lane);
+              if (target >= n_items) {
+                item = INT_MAX;
+              } else {
+                if (lane == 0) {
+                  atomicMax(p.queue, (grid_launch_id() << 32) | static_cast<unsigned long long>(target - n_static));
+                  item = claim(false);
+                }
+                item = __shfl_sync(kFullMask, item, 0);
+              }
+            }
+            if constexpr (TWO) {
+              if (lane == 0 && ok) {
+                if (qc >= kPlanRing)
+                  ok = mbar_wait_remote(&sb.claim_empty[slot], ((qc / kPlanRing) - 1) & 1, &sb.abort_flag, p.err,
+                                        kDevTimeoutOther, 256);
+                if (ok) {
+                  st_cluster_u32(mapa_shared(smem_u32(&sb.claims[slot]), 1), static_cast<uint32_t>(item));
+                  mbar_arrive_cluster_release(mapa_shared(smem_u32(&sb.claim_full[slot]), 1));
+                }
+              }
+              ok = __shfl_sync(kFullMask, ok, 0);
+            }
+          } else {
+            if (lane == 0) {
+              ok = mbar_wait_remote(&sb.claim_full[slot], (qc / kPlanRing) & 1, &sb.abort_flag, p.err,
+                                    kDevTimeoutOther, 256);
+              if (ok) {
+                item = sb.claims[slot];
+                mbar_arrive_cluster_release(mapa_shared(smem_u32(&sb.claim_empty[slot]), 0));  // (after the read)
+              }
+            }
+            ok = __shfl_sync(kFullMask, ok, 0);
+            item = __shfl_sync(kFullMask, item, 0);
+            if (ok && item < n_items) e.it = item_geometry<C, PAGED>(item, p);
+          }
+          ++qc;
+        }
+        if (!ok || item >= n_items) break;
         e.pl = plan_tiles<C>(e.it, p, use_table, lane);
         e.last = 0;
         ok = publish(e);
@@ -1180,6 +1342,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
+  // This CTA claims no more items (also after an abort): count it, and the
+  // launch's last claiming CTA resets the work queue.
+  // (The rank is read again: keeping it live through the roles costs registers.)
+  if (p.queue != nullptr && threadIdx.x == C::SCHED_WARP * 32 && (C::NCTA == 1 || cluster_rank() == 0))
+    queue_finish(p.queue, gridDim.x / C::NCTA, p.err);
   // a pair: rank 0's MMAs and drain are complete; a head-dim split: the peer
   // no longer writes into this CTA's shared memory
   if constexpr (C::NCTA == 2) cluster_sync_all();

@@ -9,13 +9,15 @@
 // is part of the library's device image instead: every GPU that loads the
 // library holds kStaticScratchBytes for it until the process exits.
 //
-// The scratch only carries the split-KV partial results (max, sum and
+// The scratch is used like a caller's workspace: a header with the prefill
+// kernel's work-queue word, then the split-KV partial results (max, sum and
 // unnormalised output per split) from the decode kernel to the combine kernel
-// of the same call.  Every partial slot the combine reads is written by that
-// call's decode kernel (empty splits write a neutral partial), so nothing has
-// to be cleared between calls.  All calls share the one array: two calls whose
-// kernels overlap on the GPU (different streams, no ordering between them)
-// race on it and may return wrong results.
+// of the same call.  The queue word carries a per-launch tag and every
+// partial slot the combine reads is written by that call's decode kernel
+// (empty splits write a neutral partial), so nothing has to be cleared
+// between calls.  All calls share the one array: two calls whose kernels
+// overlap on the GPU (different streams, no ordering between them) race on
+// it and may return wrong results.
 #include <cuda_runtime.h>
 
 #include <mutex>

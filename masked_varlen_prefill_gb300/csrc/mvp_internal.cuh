@@ -46,6 +46,10 @@ struct MaskParams {
 };
 
 // ----------------------------------------------------------------- prefill
+// Caller workspace layout: this many bytes of header (the prefill kernel's
+// work-queue word at offset 0), then the decode kernel's split partials.
+constexpr size_t kWorkspaceHeader = 256;
+
 struct PrefillParams {
   MaskParams m;
   void* out;          // bf16 [total_q, hq, D]
@@ -61,6 +65,7 @@ struct PrefillParams {
   int skip_decode;    // requests with q_len == 1 are left to the decode kernel
   int req_offset;     // first request covered (items walk [req_offset, num_reqs))
   int n_ctas;         // persistent CTAs to launch (SM count)
+  unsigned long long* queue;  // work-queue word (caller's workspace), or null: static stride
 };
 
 // head_dim in {64, 128, 256, 512}.  Tensor maps are encoded by the caller

@@ -21,6 +21,7 @@ enum DeviceError : int {
   kDevTimeoutSoftmax = 3,   // a softmax/correction hand-off never arrived
   kDevTimeoutOther = 4,
   kDevTimeoutStore = 5,     // the epilogue warps never released a hand-off slot
+  kDevQueueConflict = 6,    // the prefill work queue was taken over by another launch
 };
 
 // Wall-clock budget of one barrier wait.  Legitimate waits in these kernels
@@ -308,6 +309,19 @@ __device__ __forceinline__ void mbar_arrive_cluster_release(uint32_t bar_cluster
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster_addr) : "memory");
 }
 
+// 4-byte store to shared memory of a CTA in this cluster (address from mapa).
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Temporal number of this grid's launch in the context: the same in every
+// CTA of one launch, different for every launch (graph replays included).
+__device__ __forceinline__ uint64_t grid_launch_id() {
+  uint64_t r;
+  asm volatile("mov.u64 %0, %%gridid;" : "=l"(r));
+  return r;
+}
+
 // 16-byte store to shared memory of a CTA in this cluster (address from mapa).
 __device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
@@ -324,6 +338,40 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
       : "r"(smem_u32(bar)), "r"(parity)
       : "memory");
   return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_test_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for a phase completed by the peer CTA's remote arrivals, with acquire
+// at cluster scope, polling the non-suspending test_wait (with `sleep_ns`
+// between polls; 0 spins): a thread suspended in try_wait can resume well
+// after a remote arrival.  Same bound and abort rules as mbar_wait.
+__device__ __forceinline__ bool mbar_wait_remote(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err,
+                                                 int code, unsigned sleep_ns) {
+  if (mbar_test_wait_cluster(bar, parity)) return true;
+  unsigned long long t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (sleep_ns) __nanosleep(sleep_ns);
+    if (mbar_test_wait_cluster(bar, parity)) return true;
+    if ((it & 255u) == 0) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+        if (err) atomicCAS(err, 0, code);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
 }
 
 // mbar_wait with acquire at cluster scope (arrivals from the peer CTA).

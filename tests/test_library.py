@@ -131,9 +131,13 @@ def test_fill_argument_errors(lib):
 
 
 def test_workspace_size(lib):
-    assert mvp.attn_workspace_size(4, 16, 256, 1000) == 0  # one split: no workspace needed
+    # a 256-byte header (the prefill work queue), then the decode partials
+    assert mvp.attn_workspace_size(4, 16, 256, 1000) == 256  # one split: header only
+    assert mvp.attn_workspace_size(0, 16, 256, 100000) == 256  # no decode rows
     n = mvp.attn_workspace_size(260, 32, 128, 32769)
-    assert n == 260 * 32 * 17 * 130 * 4
+    assert n == 256 + 260 * 32 * 17 * 130 * 4
+    assert mvp.attn_workspace_size(-1, 16, 256, 1000) == 0
+    assert mvp.attn_workspace_size(4, 0, 256, 1000) == 0
 
 
 def test_binding_has_no_cpu_path():
