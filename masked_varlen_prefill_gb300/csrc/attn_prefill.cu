@@ -899,9 +899,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           if (!TWO || rank == 0) {
             bool good = true;
             const int ct = c - kClaimAhead;  // entry the producer must have taken
-            // (a suspending wait: a polling one takes issue slots from the
-            // softmax warps; the producer cannot be past entry c - 1 here, so
-            // the slot's phase parity is exact)
+            // (the producer cannot be past entry c - 1 here, and publishing
+            // entry c - 1 needed entry c - 5 consumed, so the slot's phase
+            // parity is exact)
             if (lane == 0 && ct >= 0)
               good = mbar_wait(&sb.plan_taken[ct % kPlanRing], (ct / kPlanRing) & 1, &sb.abort_flag, p.err,
                                kDevTimeoutOther);
@@ -925,8 +925,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             if constexpr (TWO) {
               if (lane == 0 && ok) {
                 if (qc >= kPlanRing)
-                  ok = mbar_wait_remote(&sb.claim_empty[slot], ((qc / kPlanRing) - 1) & 1, &sb.abort_flag, p.err,
-                                        kDevTimeoutOther, 256);
+                  ok = mbar_wait_cluster(&sb.claim_empty[slot], ((qc / kPlanRing) - 1) & 1, &sb.abort_flag, p.err,
+                                         kDevTimeoutOther);
                 if (ok) {
                   st_cluster_u32(mapa_shared(smem_u32(&sb.claims[slot]), 1), static_cast<uint32_t>(item));
                   mbar_arrive_cluster_release(mapa_shared(smem_u32(&sb.claim_full[slot]), 1));
@@ -936,8 +936,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             }
           } else {
             if (lane == 0) {
-              ok = mbar_wait_remote(&sb.claim_full[slot], (qc / kPlanRing) & 1, &sb.abort_flag, p.err,
-                                    kDevTimeoutOther, 256);
+              ok = mbar_wait_cluster(&sb.claim_full[slot], (qc / kPlanRing) & 1, &sb.abort_flag, p.err,
+                                     kDevTimeoutOther);
               if (ok) {
                 item = sb.claims[slot];
                 mbar_arrive_cluster_release(mapa_shared(smem_u32(&sb.claim_empty[slot]), 0));  // (after the read)

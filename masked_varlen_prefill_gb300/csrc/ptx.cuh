@@ -340,40 +340,6 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
   return ok != 0;
 }
 
-__device__ __forceinline__ bool mbar_test_wait_cluster(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Wait for a phase completed by the peer CTA's remote arrivals, with acquire
-// at cluster scope, polling the non-suspending test_wait (with `sleep_ns`
-// between polls; 0 spins): a thread suspended in try_wait can resume well
-// after a remote arrival.  Same bound and abort rules as mbar_wait.
-__device__ __forceinline__ bool mbar_wait_remote(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err,
-                                                 int code, unsigned sleep_ns) {
-  if (mbar_test_wait_cluster(bar, parity)) return true;
-  unsigned long long t0 = global_timer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (sleep_ns) __nanosleep(sleep_ns);
-    if (mbar_test_wait_cluster(bar, parity)) return true;
-    if ((it & 255u) == 0) {
-      if (*abort_flag) return false;
-      if (global_timer_ns() - t0 > kWaitTimeoutNs) {
-        if (err) atomicCAS(err, 0, code);
-        *abort_flag = 1;
-        return false;
-      }
-    }
-  }
-}
-
 // mbar_wait with acquire at cluster scope (arrivals from the peer CTA).
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                                   int* err, int code) {
