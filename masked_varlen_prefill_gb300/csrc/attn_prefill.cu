@@ -1419,7 +1419,11 @@ cudaError_t launch_cfg(const PrefillParams& p, const CUtensorMap& mq, const CUte
   if (n_items < groups) groups = static_cast<int>(n_items);
   cfg.gridDim = dim3(groups * C::NCTA);
   cfg.numAttrs = 2;
-  e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, p);
+  // Fewer than two rounds of items: every CTA takes at most two, the static
+  // stride is as good, and the queue's atomics would only add latency.
+  PrefillParams pq = p;
+  if (n_items < 2LL * groups) pq.queue = nullptr;
+  e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, pq);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

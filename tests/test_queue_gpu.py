@@ -1,8 +1,10 @@
 """The prefill work queue in the workspace header through the C-ABI (GPU).
 
-With a workspace the prefill kernel's CTAs take the last round of items (all
-of them when there are fewer than two rounds) from a tagged counter in its
-first 256 bytes instead of the static stride.  Every item is
+With a workspace the prefill kernel's CTAs take the last round of items
+from a tagged counter in its first 256 bytes instead of the static stride
+(batches of fewer than two rounds keep the static stride, so the cases here
+have at least two rounds: the full-size workloads and many-request random
+batches).  Every item is
 computed the same way whichever CTA takes it, so the output must be the
 static-stride output bit for bit: from an uninitialised workspace, from words
 left by earlier calls or planted stale values, over item spaces that are
@@ -60,14 +62,43 @@ def _static_and_queue(w, ws_fill=None, max_q=None, repeats=1):
 
 
 @pytest.mark.parametrize("name", ["mm_prefix_sliding", "chunked_prefill_ranges", "mixed_serving_b",
-                                  "global_causal_d512", "tiny_window_sinks"])
-def test_scaled_workloads(name):
-    _static_and_queue(workloads.scaled_workload(name), repeats=3)
+                                  "global_causal_d512"])
+def test_full_workloads(name):
+    _static_and_queue(workloads.workload(name), repeats=3)
 
 
-@pytest.mark.parametrize("seed", range(12))
-def test_random_cases(seed):
-    _static_and_queue(workloads.random_case(1300 + seed), repeats=2)
+def _many_items_case(seed):
+    """A random batch of 24-40 requests (every mask, sink and range option
+    of the random cases) with enough work items for two rounds."""
+    rng = np.random.default_rng(5000 + seed)
+    d = [64, 128, 256, 512][seed % 4]
+    group = int(rng.choice([1, 2, 4] if d == 512 else [1, 2, 4, 8]))
+    hkv = 4
+    n = int(rng.integers(24, 41))
+    q_lens = [0 if rng.integers(0, 8) == 0 else (1 if rng.integers(0, 6) == 0 else int(rng.integers(2, 700)))
+              for _ in range(n)]
+    q_lens[0] = max(q_lens[0], 5)
+    k_lens = [ql + (int(rng.integers(0, 2000)) if rng.integers(0, 2) else 0) for ql in q_lens]
+    causal = bool(rng.integers(0, 3) > 0)
+    ranges = None
+    if rng.integers(0, 2):
+        per_req = []
+        for kl in k_lens:
+            rl, cur = [], int(rng.integers(0, max(1, kl // 2 + 1)))
+            for _ in range(int(rng.integers(0, 5))):
+                length = int(rng.integers(1, 200))
+                rl.append((cur, cur + length - 1))
+                cur += length + int(rng.integers(1, 40))
+            per_req.append(rl)
+        ranges = workloads.pad_ranges(per_req)
+    return workloads.Workload(f"many{seed}", 6000 + seed, q_lens, k_lens, hkv * group, hkv, d, causal,
+                              int(rng.choice([-1, 63, 400])), -1 if causal else int(rng.choice([-1, 77])),
+                              int(rng.integers(0, 3)), ranges)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_many_request_batches(seed):
+    _static_and_queue(_many_items_case(seed), repeats=2)
 
 
 # stale words a workspace may hold: zeros, all ones, a tag with the counter
@@ -77,7 +108,7 @@ STALE = [0, -1, (0x1234 << 32) | 0x7fffff00, 0x7ffffffe << 32, 0x5a5a5a5a5a5a5a5
 
 @pytest.mark.parametrize("word", STALE)
 def test_stale_queue_words(word):
-    _static_and_queue(workloads.scaled_workload("mm_prefix_sliding"), ws_fill=word)
+    _static_and_queue(workloads.workload("mm_prefix_sliding"), ws_fill=word)
 
 
 def test_mostly_empty_item_space():
@@ -93,11 +124,11 @@ def test_mostly_empty_item_space():
 
 def test_head_split_cluster(monkeypatch):
     monkeypatch.setenv("MVP_D512_HEAD_SPLIT", "1")
-    _static_and_queue(workloads.scaled_workload("global_causal_d512"), repeats=2)
+    _static_and_queue(workloads.workload("global_causal_d512"), repeats=2)
 
 
 def test_paged():
-    w = workloads.scaled_workload("chunked_prefill_ranges")
+    w = workloads.workload("chunked_prefill_ranges")
     q, k, v, sinks = gh.make_inputs(w)
     _, _, table, covered = gh.run_gpu(w, q, k, v, sinks, use_workspace=False)
     kc, vc, bt, sl = workloads.to_paged(k, v, w.k_lens, 16, seed=5)
@@ -119,7 +150,7 @@ def test_paged():
 def test_back_to_back_graph_replays():
     """Replays of one captured call with nothing in between: each must start
     from item 0 whatever tag the previous replay left."""
-    w = workloads.scaled_workload("mm_prefix_sliding")
+    w = workloads.workload("mm_prefix_sliding")
     q, k, v, sinks = gh.make_inputs(w)
     _, _, table, covered = gh.run_gpu(w, q, k, v, sinks, use_workspace=False)
     ws = torch.empty(HEADER, dtype=torch.uint8, device=q.device)
@@ -151,7 +182,7 @@ def test_header_only_workspace_leaves_decode_unsplit():
     workspace).  A full-size workspace also splits the long decode rows,
     which rounds differently: its prefill rows must still be identical and its
     decode rows within the parity tolerance of the unsplit ones."""
-    w = workloads.scaled_workload("mixed_serving_a")
+    w = workloads.workload("mixed_serving_a")
     q, k, v, sinks, table, covered, ref = _static_and_queue(w)
     n_dec = sum(1 for x in w.q_lens if x == 1)
     nbytes = mvp.attn_workspace_size(w.num_reqs, w.num_heads_q, w.head_dim, max(w.k_lens))
