@@ -95,15 +95,17 @@ int mvp_fill_query_ranges(const int32_t* ranges, int num_reqs, int max_ranges,
 /*
  * Bytes of caller-provided workspace that mvp_attn_fwd_varlen can use.  The
  * first 256 bytes hold the prefill kernel's work queue: its persistent CTAs
- * then claim work items one at a time (whichever CTA frees up first takes the
- * next item) instead of walking a static stride, which evens out batches
- * whose items differ in length.  The rest holds partial results that let long
+ * walk the work items with a static stride but claim the last round one at a
+ * time from the queue (whichever CTA frees up first takes the next item),
+ * which evens out the end of batches whose items differ in length (batches
+ * of fewer than two rounds keep the stride).  The rest holds partial results that let long
  * single-token (decode) rows be split across several CTAs.  num_reqs is the
  * number of requests the decode kernel covers (num_decode_reqs, or the whole
  * batch when that is -1; 0: header only).  Returns 0 for negative num_reqs
  * or non-positive sizes.
  * The workspace needs no initialisation and is left valid for the next call
- * (the queue word carries a per-launch tag, so no reset is needed).  Two calls
+ * (the queue words carry a per-launch tag, and each launch resets its
+ * counter when its last CTA is done).  Two calls
  * that may run at the same time on the GPU (different streams) need separate
  * workspaces; a kernel that finds its queue taken over records a device
  * error (mvp_get_last_device_error) and stops claiming.  Workspace is

@@ -20,9 +20,9 @@
 //   A tile costs each SM half the L2 -> shared-memory bytes and half the
 //   shared memory, which buys two K and two V stages at D = 256 and 512.
 // * Persistent CTAs (one per SM) take the items, numbered q tile fastest so
-//   that concurrent CTAs share K/V windows in L2, from a work queue in the
-//   caller's workspace (one item ahead of the work in progress), or without
-//   workspace with a static stride.  A scheduler warp computes each item's
+//   that concurrent CTAs share K/V windows in L2, with a static stride; the
+//   last round comes from a work queue in the caller's workspace, so the tail
+//   goes to whichever CTA frees up first.  A scheduler warp computes each item's
 //   geometry and key-tile plan (a warp reduction over the item's rows) into a
 //   ring that every role reads, and
 //   all barrier phases run on CTA-wide counters, so the producer and the MMA
@@ -832,10 +832,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     } else if (warp == C::SCHED_WARP) {
       // ------------------------------------------------------------ scheduler
       // Finds this CTA's items, computes each valid item's geometry and
-      // key-tile plan, and publishes them through the plan ring.  Items come
-      // from a static stride (up to kPlanRing items ahead of the slowest
-      // consumer warp) or, given a work-queue word, are claimed one at a time
-      // from it.
+      // key-tile plan, and publishes them through the plan ring (up to
+      // kPlanRing items ahead of the slowest consumer warp).  Items come from
+      // a static stride and, for the last round, given a work-queue word, are
+      // claimed one at a time from it.
       int n = 0;
       bool ok = true;
       auto publish = [&](const PlanEntry& e) -> bool {
