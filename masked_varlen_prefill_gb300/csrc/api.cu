@@ -81,7 +81,7 @@ int largest_pow2_divisor(int g, int cap) {
   return p;
 }
 
-constexpr int kDecodeChunk = 2048;
+constexpr int kDecodeChunk = 4096;
 constexpr int kMaxSplits = 64;
 
 }  // namespace

@@ -102,6 +102,21 @@ def test_prefill_only_and_decode_only_batches():
     _parity_full(d, num_decode_reqs=-1)
 
 
+@pytest.mark.parametrize("sink_mode", [workloads.SINK_NONE, workloads.SINK_KEY0_BIAS, workloads.SINK_NULL_LOGIT])
+def test_split_decode_rows(sink_mode):
+    """Decode rows longer than one split-KV chunk (4096 keys): 1 to 4 chunks,
+    chunk-boundary lengths, a window that starts inside a chunk, ranges, next
+    to a prefill request."""
+    k_lens = [4096, 4097, 8192, 9001, 12289, 100, 16000, 700]
+    q_lens = [1] * 7 + [300]
+    ranges = workloads.pad_ranges([[(10, 5000)], [], [(4000, 4200)], [], [(0, 3)], [], [(15000, 15999)],
+                                   [(20, 80), (400, 650)]])
+    for wl in (-1, 5000):
+        w = workloads.Workload(f"split{sink_mode}_{wl}", 88 + sink_mode, q_lens, k_lens, 16, 4, 128, True, wl, 0,
+                               sink_mode, ranges)
+        _parity_full(w, num_decode_reqs=7)
+
+
 FULL = ["tiny_window_sinks", "mm_prefix_sliding", "global_causal_d512", "chunked_prefill_ranges",
         "mixed_serving_a", "mixed_serving_b"]
 

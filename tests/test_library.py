@@ -134,8 +134,8 @@ def test_workspace_size(lib):
     # a 256-byte header (the prefill work queue), then the decode partials
     assert mvp.attn_workspace_size(4, 16, 256, 1000) == 256  # one split: header only
     assert mvp.attn_workspace_size(0, 16, 256, 100000) == 256  # no decode rows
-    n = mvp.attn_workspace_size(260, 32, 128, 32769)
-    assert n == 256 + 260 * 32 * 17 * 130 * 4
+    n = mvp.attn_workspace_size(260, 32, 128, 32769)  # 4096-key split chunks: 9
+    assert n == 256 + 260 * 32 * 9 * 130 * 4
     assert mvp.attn_workspace_size(-1, 16, 256, 1000) == 0
     assert mvp.attn_workspace_size(4, 0, 256, 1000) == 0
 
