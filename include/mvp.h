@@ -98,7 +98,8 @@ int mvp_fill_query_ranges(const int32_t* ranges, int num_reqs, int max_ranges,
  * walk the work items with a static stride but claim the last round one at a
  * time from the queue (whichever CTA frees up first takes the next item),
  * which evens out the end of batches whose items differ in length (batches
- * of fewer than two rounds keep the stride).  The rest holds partial results that let long
+ * of fewer than two rounds, and masks with a window shorter than max_k_len,
+ * whose items are even already, keep the stride).  The rest holds partial results that let long
  * single-token (decode) rows be split across several CTAs.  num_reqs is the
  * number of requests the decode kernel covers (num_decode_reqs, or the whole
  * batch when that is -1; 0: header only).  Returns 0 for negative num_reqs

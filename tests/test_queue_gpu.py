@@ -2,9 +2,10 @@
 
 With a workspace the prefill kernel's CTAs take the last round of items
 from a tagged counter in its first 256 bytes instead of the static stride
-(batches of fewer than two rounds keep the static stride, so the cases here
-have at least two rounds: the full-size workloads and many-request random
-batches).  Every item is
+(batches of fewer than two rounds, and masks with a window shorter than the
+longest key run, keep the static stride, so the queue cases here have at
+least two rounds and no such window; the windowed ones check that the
+workspace changes nothing).  Every item is
 computed the same way whichever CTA takes it, so the output must be the
 static-stride output bit for bit: from an uninitialised workspace, from words
 left by earlier calls or planted stale values, over item spaces that are
@@ -61,8 +62,8 @@ def _static_and_queue(w, ws_fill=None, max_q=None, repeats=1):
     return q, k, v, sinks, table, covered, ref
 
 
-@pytest.mark.parametrize("name", ["mm_prefix_sliding", "chunked_prefill_ranges", "mixed_serving_b",
-                                  "global_causal_d512"])
+@pytest.mark.parametrize("name", ["mm_prefix_sliding", "chunked_prefill_ranges", "mixed_serving_a",
+                                  "mixed_serving_b", "global_causal_d512"])
 def test_full_workloads(name):
     _static_and_queue(workloads.workload(name), repeats=3)
 
@@ -92,7 +93,8 @@ def _many_items_case(seed):
             per_req.append(rl)
         ranges = workloads.pad_ranges(per_req)
     return workloads.Workload(f"many{seed}", 6000 + seed, q_lens, k_lens, hkv * group, hkv, d, causal,
-                              int(rng.choice([-1, 63, 400])), -1 if causal else int(rng.choice([-1, 77])),
+                              -1 if seed % 2 == 0 else int(rng.choice([-1, 63, 400])),
+                              -1 if causal else int(rng.choice([-1, 77])),
                               int(rng.integers(0, 3)), ranges)
 
 
@@ -108,7 +110,7 @@ STALE = [0, -1, (0x1234 << 32) | 0x7fffff00, 0x7ffffffe << 32, 0x5a5a5a5a5a5a5a5
 
 @pytest.mark.parametrize("word", STALE)
 def test_stale_queue_words(word):
-    _static_and_queue(workloads.workload("mm_prefix_sliding"), ws_fill=word)
+    _static_and_queue(workloads.workload("global_causal_d512"), ws_fill=word)
 
 
 def test_mostly_empty_item_space():
@@ -117,7 +119,7 @@ def test_mostly_empty_item_space():
     rows and the queue skips past them."""
     q_lens = [0, 1, 0, 200, 1, 0, 0, 37, 0, 1] * 6
     k_lens = [5, 300, 0, 900, 64, 0, 3, 37, 1, 2000] * 6
-    w = workloads.Workload("sparse_items", 4242, q_lens, k_lens, 8, 2, 128, True, 300, 0, workloads.SINK_NULL_LOGIT,
+    w = workloads.Workload("sparse_items", 4242, q_lens, k_lens, 8, 2, 128, True, -1, 0, workloads.SINK_NULL_LOGIT,
                            None)
     _static_and_queue(w, max_q=8192, repeats=2)
 
@@ -128,7 +130,7 @@ def test_head_split_cluster(monkeypatch):
 
 
 def test_paged():
-    w = workloads.workload("chunked_prefill_ranges")
+    w = workloads.workload("global_causal_d512")
     q, k, v, sinks = gh.make_inputs(w)
     _, _, table, covered = gh.run_gpu(w, q, k, v, sinks, use_workspace=False)
     kc, vc, bt, sl = workloads.to_paged(k, v, w.k_lens, 16, seed=5)
@@ -150,7 +152,7 @@ def test_paged():
 def test_back_to_back_graph_replays():
     """Replays of one captured call with nothing in between: each must start
     from item 0 whatever tag the previous replay left."""
-    w = workloads.workload("mm_prefix_sliding")
+    w = workloads.workload("global_causal_d512")
     q, k, v, sinks = gh.make_inputs(w)
     _, _, table, covered = gh.run_gpu(w, q, k, v, sinks, use_workspace=False)
     ws = torch.empty(HEADER, dtype=torch.uint8, device=q.device)
