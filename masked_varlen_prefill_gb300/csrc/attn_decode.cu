@@ -195,8 +195,10 @@ __global__ void __launch_bounds__(kThreads)
   }
 
   // ------------------------------------------------------------------ compute
-  // q for this lane's dims, every head of the CTA, pre-scaled to log2 units.
-  float qf[GP][DPL];
+  // q for this lane's dims, every head of the CTA, pre-scaled to log2 units;
+  // kept as (even, odd) dim pairs for the packed fp32x2 FMAs below.
+  constexpr int DP2 = DPL / 2;
+  uint64_t q2[GP][DP2];
 #pragma unroll
   for (int g = 0; g < GP; ++g) {
     float tmp[DPL];
@@ -208,20 +210,21 @@ __global__ void __launch_bounds__(kThreads)
       load_row<DPL>(src, tmp);
     }
 #pragma unroll
-    for (int d = 0; d < DPL; ++d) qf[g][d] = tmp[d] * p.m.scale_log2;
+    for (int i = 0; i < DP2; ++i) q2[g][i] = f2_pack(tmp[2 * i] * p.m.scale_log2, tmp[2 * i + 1] * p.m.scale_log2);
   }
   const int my_g = lane % GP;
   const bool key0_mode = p.m.sink_mode == 1 && p.m.sinks != nullptr;
   float my_sink = 0.f;
   if (key0_mode && my_g < heads_here) my_sink = __ldg(p.m.sinks + hq0 + my_g) * 1.4426950408889634f;
 
-  float m[GP], acc[GP][DPL];
+  float m[GP];
+  uint64_t acc2[GP][DP2];  // O partial sums, (even, odd) dim pairs
   float l_part = 0.f;
 #pragma unroll
   for (int g = 0; g < GP; ++g) {
     m[g] = -INFINITY;
 #pragma unroll
-    for (int d = 0; d < DPL; ++d) acc[g][d] = 0.f;
+    for (int i = 0; i < DP2; ++i) acc2[g][i] = 0ull;  // (+0.f, +0.f)
   }
 
   bool ok = true;
@@ -239,12 +242,18 @@ __global__ void __launch_bounds__(kThreads)
       for (int kk = 0; kk < KG; ++kk) {
         float kr[DPL];
         load_row<DPL>(ks + row_off<D>(gi * KG + kk, lane), kr);
+        uint64_t k2[DP2];
+#pragma unroll
+        for (int i = 0; i < DP2; ++i) k2[i] = f2_pack(kr[2 * i], kr[2 * i + 1]);
 #pragma unroll
         for (int g = 0; g < GP; ++g) {
-          float a = 0.f;
+          // even and odd dims summed separately, then added
+          uint64_t a2 = f2_mul(q2[g][0], k2[0]);
 #pragma unroll
-          for (int d = 0; d < DPL; ++d) a = fmaf(qf[g][d], kr[d], a);
-          v[kk * GP + g] = a;
+          for (int i = 1; i < DP2; ++i) a2 = f2_fma(q2[g][i], k2[i], a2);
+          float ae, ao;
+          f2_unpack(a2, ae, ao);
+          v[kk * GP + g] = ae + ao;
         }
       }
       // reduce-scatter: lane l ends with the full sum of pair l
@@ -284,18 +293,24 @@ __global__ void __launch_bounds__(kThreads)
       const float pr = (x == -INFINITY) ? 0.f : ex2_approx(x - my_m);
       l_part = l_part * my_alpha + pr;
 #pragma unroll
-      for (int g = 0; g < GP; ++g)
+      for (int g = 0; g < GP; ++g) {
+        const uint64_t a2 = f2_pack(alpha[g], alpha[g]);
 #pragma unroll
-        for (int d = 0; d < DPL; ++d) acc[g][d] *= alpha[g];
+        for (int i = 0; i < DP2; ++i) acc2[g][i] = f2_mul(acc2[g][i], a2);
+      }
 #pragma unroll
       for (int kk = 0; kk < KG; ++kk) {
         float vr[DPL];
         load_row<DPL>(vs + row_off<D>(gi * KG + kk, lane), vr);
+        uint64_t v2[DP2];
+#pragma unroll
+        for (int i = 0; i < DP2; ++i) v2[i] = f2_pack(vr[2 * i], vr[2 * i + 1]);
 #pragma unroll
         for (int g = 0; g < GP; ++g) {
           const float pg = __shfl_sync(kFull, pr, kk * GP + g);
+          const uint64_t pg2 = f2_pack(pg, pg);
 #pragma unroll
-          for (int d = 0; d < DPL; ++d) acc[g][d] = fmaf(pg, vr[d], acc[g][d]);
+          for (int i = 0; i < DP2; ++i) acc2[g][i] = f2_fma(pg2, v2[i], acc2[g][i]);
         }
       }
     }
@@ -315,7 +330,12 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
   for (int g = 0; g < GP; ++g)
 #pragma unroll
-    for (int d = 0; d < DPL; ++d) sm[(warp * GP + g) * D + lane * DPL + d] = acc[g][d];
+    for (int i = 0; i < DP2; ++i) {
+      float x0, x1;
+      f2_unpack(acc2[g][i], x0, x1);
+      sm[(warp * GP + g) * D + lane * DPL + 2 * i] = x0;
+      sm[(warp * GP + g) * D + lane * DPL + 2 * i + 1] = x1;
+    }
   if (lane < GP) {
     float mm = m[0];
 #pragma unroll
