@@ -96,6 +96,9 @@ __global__ void __launch_bounds__(kThreads)
   constexpr int KG = 32 / GP;        // keys per warp step
   constexpr int NG = C::KT / KG;     // warp steps per tile
   extern __shared__ uint8_t smem_raw[];
+  // Per compute warp, the step's 32 probabilities (key kk, head g at
+  // kk * GP + g), read back by every lane as vectors instead of 32 shuffles.
+  __shared__ __align__(16) float pbuf[kNW][32];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ DBarriers sb;
 
@@ -298,6 +301,8 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
         for (int i = 0; i < DP2; ++i) acc2[g][i] = f2_mul(acc2[g][i], a2);
       }
+      pbuf[warp][lane] = pr;
+      __syncwarp();
 #pragma unroll
       for (int kk = 0; kk < KG; ++kk) {
         float vr[DPL];
@@ -307,12 +312,13 @@ __global__ void __launch_bounds__(kThreads)
         for (int i = 0; i < DP2; ++i) v2[i] = f2_pack(vr[2 * i], vr[2 * i + 1]);
 #pragma unroll
         for (int g = 0; g < GP; ++g) {
-          const float pg = __shfl_sync(kFull, pr, kk * GP + g);
+          const float pg = pbuf[warp][kk * GP + g];  // same address in every lane: broadcast
           const uint64_t pg2 = f2_pack(pg, pg);
 #pragma unroll
           for (int i = 0; i < DP2; ++i) acc2[g][i] = f2_fma(pg2, v2[i], acc2[g][i]);
         }
       }
+      __syncwarp();  // every lane has read pbuf before the next step writes it
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&sb.empty[s]);
