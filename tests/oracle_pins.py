@@ -401,3 +401,46 @@ def check_brute_force(attention_forward, fill, make_case, cases=120):
         assert np.allclose(out, ref_o, atol=1e-10), seed
         both_inf = np.isneginf(lse) & np.isneginf(ref_l)
         assert np.allclose(np.where(both_inf, 0, lse), np.where(both_inf, 0, ref_l), atol=1e-10), seed
+
+
+def check_context_lens(attention_forward, fill, make_case, cases=40, seed=17):
+    """An explicit context length defines the query positions (step14_4
+    tutorial, *Solution*: key j is masked iff j > start_pos + i).
+
+    * Passing ctx = k_len - q_len explicitly changes nothing.
+    * Any other ctx matches the element-by-element definition with p = ctx + i.
+    * Truncation: a causal row at position p never sees a key past p, so with
+      ctx' < k_len - q_len the result equals the same call on the request's
+      first ctx' + q_len keys with the context derived from them.
+    """
+    rng = np.random.default_rng(seed)
+    for c in range(cases):
+        w, q, k, v, sinks, table, cu_q, cu_k = make_case(c, fill)
+        derived = np.asarray(w.k_lens) - np.asarray(w.q_lens)
+        kw = dict(range_table=table, sinks=sinks, sink_mode=w.sink_mode)
+        o_none, l_none = attention_forward(q, k, v, cu_q, cu_k, w.causal, w.window_left, w.window_right, w.scale,
+                                           **kw)
+        o_exp, l_exp = attention_forward(q, k, v, cu_q, cu_k, w.causal, w.window_left, w.window_right, w.scale,
+                                         context_lens=derived, **kw)
+        assert np.array_equal(o_none, o_exp) and np.array_equal(l_none, l_exp, equal_nan=True), c
+        # shifted positions against the definition (table rows are taken as given)
+        ctx = np.array([int(rng.integers(0, d + 1)) for d in derived])
+        out, lse = attention_forward(q, k, v, cu_q, cu_k, w.causal, w.window_left, w.window_right, w.scale,
+                                     context_lens=ctx, **kw)
+        ref_o, ref_l = brute_force(q, k, v, list(cu_q), list(cu_k), w.causal, w.window_left, w.window_right,
+                                   w.scale, list(ctx), table, sinks, w.sink_mode)
+        assert np.allclose(out, ref_o, atol=1e-10), c
+        both_inf = np.isneginf(lse) & np.isneginf(ref_l)
+        assert np.allclose(np.where(both_inf, 0, lse), np.where(both_inf, 0, ref_l), atol=1e-10), c
+        # truncation invariant (causal, no range part)
+        keep = [np.arange(cu_k[b], cu_k[b] + ctx[b] + w.q_lens[b]) for b in range(w.num_reqs)]
+        idx = np.concatenate(keep) if keep else np.zeros(0, dtype=np.int64)
+        cu_t = np.zeros(w.num_reqs + 1, dtype=np.int64)
+        cu_t[1:] = np.cumsum(ctx + np.asarray(w.q_lens))
+        o_c, l_c = attention_forward(q, k, v, cu_q, cu_k, True, w.window_left, 0, w.scale, context_lens=ctx,
+                                     sinks=sinks, sink_mode=w.sink_mode)
+        o_t, l_t = attention_forward(q, k[idx], v[idx], cu_q, cu_t, True, w.window_left, 0, w.scale,
+                                     sinks=sinks, sink_mode=w.sink_mode)
+        assert np.allclose(o_c, o_t, atol=1e-12), c
+        both_inf = np.isneginf(l_c) & np.isneginf(l_t)
+        assert np.allclose(np.where(both_inf, 0, l_c), np.where(both_inf, 0, l_t), atol=1e-12, equal_nan=True), c

@@ -54,6 +54,12 @@ ATTENTION_MUTANTS = [
      lambda m: pins.check_causal_formula(m.visible_mask)),
     # context offset ignored (the packed-row reading)
     ("ctx_dropped", "p = ctx + i", "p = i", lambda m: pins.check_causal_formula(m.visible_mask)),
+    # an explicit context length ignored (always k_len - q_len)
+    ("explicit_ctx_ignored",
+     "ctx = (k_len - q_len) if context_lens is None else int(np.asarray(context_lens)[b])",
+     "ctx = k_len - q_len",
+     lambda m: pins.check_context_lens(m.attention_forward, real_range_table.fill_by_spans, make_tiny_case,
+                                       cases=10)),
     # range end treated as half-open
     ("range_half_open", "in_range = (start <= j) & (j <= end)", "in_range = (start <= j) & (j < end)",
      lambda m: pins.check_brute_force(m.attention_forward, real_range_table.fill_by_spans,

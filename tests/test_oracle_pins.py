@@ -70,6 +70,10 @@ def test_brute_force_tiny():
                            make_tiny_case, cases=150)
 
 
+def test_explicit_context_lens():
+    pins.check_context_lens(attention.attention_forward, range_table.fill_by_spans, make_tiny_case)
+
+
 def test_row_subset_equals_full():
     """Computing a subset of rows gives the same rows as the full batch."""
     w = workloads.scaled_workload("chunked_prefill_ranges")
