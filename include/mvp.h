@@ -23,11 +23,16 @@
  *     stream) and the call returns without synchronising.
  *   - Argument errors are detected on the host before anything is launched;
  *     nothing is written then.  Return values are mvp_status codes.
- *   - The library keeps one 4-byte device error word per device (allocated on
- *     the first call on that device).  Kernels that hit a bounded-wait
- *     timeout record a code there and unwind instead of hanging (so does a
- *     prefill kernel whose workspace queue another launch took over);
- *     mvp_get_last_device_error() reads and clears it.
+ *   - The library keeps one 4-byte device error word per device: a
+ *     __device__ variable of the library's own module, so nothing is
+ *     allocated for it; its device address is looked up on the first call on
+ *     that device.  Kernels that hit a bounded-wait timeout record a code
+ *     there and unwind instead of hanging (so does a prefill kernel whose
+ *     workspace queue another launch took over); mvp_get_last_device_error()
+ *     reads and clears it.
+ *   - Per-device state (that address, the SM count, kernel attributes) is
+ *     looked up once per process and device; a cudaDeviceReset() invalidates
+ *     it, so the library must not be used on a device after a reset.
  */
 #ifndef MVP_H_
 #define MVP_H_
@@ -171,6 +176,57 @@ int mvp_attn_fwd_varlen(const void* q, const void* k, const void* v, void* out, 
                         void* stream);
 
 /*
+ * Variants and testing options of one attention call (mvp_attn_fwd_varlen_ext).
+ *
+ * variant        MVP_VARIANT_DEFAULT, or MVP_VARIANT_D512_HEAD_SPLIT (head_dim
+ *                512 only, MVP_ERR_UNSUPPORTED otherwise): a 2-CTA cluster
+ *                splits the head dimension of each 128-row query tile, so
+ *                O of all 512 value columns stays in tensor memory and QK^T is
+ *                not recomputed; the two CTAs add their partial scores through
+ *                distributed shared memory every key tile.  Same results
+ *                within the tolerances, but slower on GB300 than the default
+ *                (which splits the value dimension over two work items, each
+ *                recomputing the scores).
+ * wait_limit_us  budget of one bounded device wait in microseconds; 0 means
+ *                the default of one second.  Every legitimate wait lasts
+ *                microseconds per key tile, but a wait can span a whole work
+ *                item (its rows times its keys), so a budget below a few
+ *                milliseconds risks reporting a timeout on a healthy call.
+ * fault          MVP_FAULT_NONE for every real call.  MVP_FAULT_WITHHOLD_PROBS
+ *                exists to test the timeout path: in every prefill CTA that
+ *                gets work (rank 0 of each CTA pair) one softmax warp never
+ *                signals that its first key tile's probabilities are ready,
+ *                so the MMA issuer's wait for them runs out; the kernel
+ *                records MVP_ERR_DEVICE_TIMEOUT (see
+ *                mvp_get_last_device_error), unwinds, frees its tensor memory
+ *                and returns, the prefill outputs of that call being
+ *                undefined.  Single-token rows (the decode kernel) are not
+ *                affected.
+ */
+typedef enum { MVP_VARIANT_DEFAULT = 0, MVP_VARIANT_D512_HEAD_SPLIT = 1 } mvp_variant;
+typedef enum { MVP_FAULT_NONE = 0, MVP_FAULT_WITHHOLD_PROBS = 1 } mvp_fault;
+typedef struct {
+  int variant;            /* mvp_variant */
+  unsigned wait_limit_us; /* 0: default (1 s) */
+  int fault;              /* mvp_fault */
+} mvp_attn_options;
+
+/*
+ * mvp_attn_fwd_varlen with options (NULL options: identical to
+ * mvp_attn_fwd_varlen).  Errors as mvp_attn_fwd_varlen, plus MVP_ERR_ARG for
+ * an unknown variant or fault and MVP_ERR_UNSUPPORTED for the D = 512 head
+ * split at another head_dim.
+ */
+int mvp_attn_fwd_varlen_ext(const void* q, const void* k, const void* v, void* out, float* lse,
+                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                            const int32_t* context_lens, int num_reqs, int total_q, int total_k,
+                            int max_q_len, int max_k_len, int num_decode_reqs, int num_heads_q,
+                            int num_heads_kv, int head_dim, const int32_t* range_table,
+                            const int32_t* range_covered, int causal, int window_left, int window_right,
+                            const float* sinks, int sink_mode, float scale, void* workspace,
+                            size_t workspace_bytes, void* stream, const mvp_attn_options* options);
+
+/*
  * The same attention over a paged K/V cache (the block-table layout of
  * vLLM's paged attention, which the FA4 pages run their masks on): the keys
  * and values of request b are not packed rows but seq_lens_k[b] positions
@@ -246,9 +302,14 @@ int mvp_attn_fwd_varlen_scan(const void* q, const void* k, const void* v, void* 
  * go to a fixed 16 MiB array in the library's own device memory
  * (mvp_static_scratch_bytes()), which every GPU that loads the library holds
  * until the process exits.  The call allocates nothing.
- *   - A batch whose partials would not fit (mvp_attn_workspace_size(decode
- *     requests, ...) > mvp_static_scratch_bytes()) is rejected with
- *     MVP_ERR_CAPACITY before anything is launched.
+ *   - Long decode rows are split over as many CTAs as the array holds
+ *     partials for (at most what mvp_attn_workspace_size would give), so a
+ *     large decode batch runs with fewer splits than with a full workspace.
+ *     The maximum: the array (less its 256-byte header) must hold one
+ *     split's partials of the call's decode rows, decode_requests x
+ *     num_heads_q x (head_dim + 2) x 4 bytes (decode_requests =
+ *     num_decode_reqs, or num_reqs when that is -1); a larger call is
+ *     rejected with MVP_ERR_CAPACITY before anything is launched.
  *   - The first call on a device looks up the array's device address (and the
  *     library's other per-device state); make that first call before any
  *     stream capture.
@@ -401,13 +462,15 @@ typedef struct {
  * Fills *out for an attention call with these HOST arrays: cu_seqlens_q
  * [num_reqs + 1], seq_lens_k [num_reqs], context_lens [num_reqs] or NULL,
  * range_table [total_q, 2] (as mvp_fill_query_ranges leaves it) or NULL, and
- * the call's heads, head_dim and mask scalars.
+ * the call's heads, head_dim and mask scalars; variant (mvp_variant) selects
+ * the prefill kernel whose executed work is counted.
  * Errors: MVP_ERR_ARG (NULL out or arrays, negative lengths, a query offset
- * array not starting at 0, bad mask scalars), MVP_ERR_UNSUPPORTED (head_dim).
+ * array not starting at 0, bad mask scalars, unknown variant),
+ * MVP_ERR_UNSUPPORTED (head_dim, or the D = 512 head split at another one).
  */
 int mvp_attn_accounting(const int32_t* cu_seqlens_q, const int32_t* seq_lens_k, const int32_t* context_lens,
                         const int32_t* range_table, int num_reqs, int num_heads_q, int num_heads_kv, int head_dim,
-                        int causal, int window_left, int window_right, mvp_attn_counts* out);
+                        int causal, int window_left, int window_right, int variant, mvp_attn_counts* out);
 
 /* Synchronises `stream`, returns MVP_ERR_DEVICE_TIMEOUT if a kernel recorded a
  * timeout since the last call (and clears it), MVP_ERR_CUDA on a CUDA error,

@@ -15,9 +15,14 @@ from ._lib import (  # noqa: F401
     MVP_ERR_DEVICE_TIMEOUT,
     MVP_ERR_UNSUPPORTED,
     MVP_OK,
+    FAULT_NONE,
+    FAULT_WITHHOLD_PROBS,
     SINK_KEY0_BIAS,
     SINK_NONE,
     SINK_NULL_LOGIT,
+    VARIANT_D512_HEAD_SPLIT,
+    VARIANT_DEFAULT,
+    AttnOptions,
     MvpError,
     StepMetadata,
     attn_accounting,

@@ -20,6 +20,11 @@ SINK_NONE = 0
 SINK_KEY0_BIAS = 1
 SINK_NULL_LOGIT = 2
 
+VARIANT_DEFAULT = 0
+VARIANT_D512_HEAD_SPLIT = 1
+FAULT_NONE = 0
+FAULT_WITHHOLD_PROBS = 1
+
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "lib", "libmvp.so")
 _lib = None
@@ -43,11 +48,19 @@ class AttnCounts(ctypes.Structure):
                 ("decode_read_bytes", ctypes.c_double), ("decode_cta_read_bytes", ctypes.c_double)]
 
 
+class AttnOptions(ctypes.Structure):
+    """``mvp_attn_options`` (include/mvp.h)."""
+
+    _fields_ = [("variant", ctypes.c_int), ("wait_limit_us", ctypes.c_uint), ("fault", ctypes.c_int)]
+
+
 _SIGNATURES = {
     "mvp_fill_query_ranges": (_i, [_vp, _i, _i, _vp, _vp, _i, _vp, _i, _vp, _vp]),
     "mvp_attn_workspace_size": (_sz, [_i, _i, _i, _i]),
     "mvp_attn_fwd_varlen": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i,
                                  _vp, _vp, _i, _i, _i, _vp, _i, _f, _vp, _sz, _vp]),
+    "mvp_attn_fwd_varlen_ext": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i,
+                                     _vp, _vp, _i, _i, _i, _vp, _i, _f, _vp, _sz, _vp, ctypes.POINTER(AttnOptions)]),
     "mvp_attn_fwd_paged": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _vp, _i, _i, _i, _i, _i, _i, _i,
                                 _i, _vp, _vp, _i, _i, _i, _vp, _i, _f, _vp, _sz, _vp]),
     "mvp_attn_fwd_varlen_static_ws": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
@@ -65,7 +78,7 @@ _SIGNATURES = {
     "mvp_meta_upload": (_i, [_vp, _vp]),
     "mvp_attn_fwd_varlen_scan": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i,
                                       _vp, _i, _i, _i, _i, _vp, _i, _f, _vp, _sz, _vp]),
-    "mvp_attn_accounting": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(AttnCounts)]),
+    "mvp_attn_accounting": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(AttnCounts)]),
 }
 
 
@@ -151,11 +164,14 @@ def attn_workspace_size(num_reqs, num_heads_q, head_dim, max_k_len) -> int:
 def attn_fwd_varlen(q, k, v, out, cu_seqlens_q, cu_seqlens_k, max_q_len, max_k_len, *, lse=None,
                     context_lens=None, range_table=None, range_covered=None, causal=True, window_left=-1,
                     window_right=-1, sinks=None, sink_mode=SINK_NONE, scale=None, workspace=None,
-                    num_decode_reqs=-1, stream=None):
+                    num_decode_reqs=-1, stream=None, variant=VARIANT_DEFAULT, wait_limit_us=0,
+                    fault=FAULT_NONE):
     """Masked varlen attention forward (see ``mvp_attn_fwd_varlen``).
 
     q [total_q, Hq, D], k/v [total_k, Hkv, D] bf16; out like q; lse fp32
     [Hq, total_q] or None; cu_seqlens int32 [B+1]; the rest as in the header.
+    ``variant`` / ``wait_limit_us`` / ``fault`` other than their defaults go
+    through ``mvp_attn_fwd_varlen_ext`` with those options.
     """
     lib = load_library()
     dev = q.device
@@ -178,14 +194,18 @@ def attn_fwd_varlen(q, k, v, out, cu_seqlens_q, cu_seqlens_k, max_q_len, max_k_l
     if scale is None:
         scale = d ** -0.5
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = lib.mvp_attn_fwd_varlen(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
-        _ptr(context_lens), num_reqs, total_q, total_k, int(max_q_len), int(max_k_len), int(num_decode_reqs),
-        hq, hkv, d,
-        _ptr(range_table), _ptr(range_covered), int(bool(causal)), int(window_left), int(window_right),
-        _ptr(sinks), int(sink_mode), float(scale), _ptr(workspace), ws_bytes, _stream(stream, dev))
+    args = [_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+            _ptr(context_lens), num_reqs, total_q, total_k, int(max_q_len), int(max_k_len), int(num_decode_reqs),
+            hq, hkv, d, _ptr(range_table), _ptr(range_covered), int(bool(causal)), int(window_left),
+            int(window_right), _ptr(sinks), int(sink_mode), float(scale), _ptr(workspace), ws_bytes,
+            _stream(stream, dev)]
+    if variant == VARIANT_DEFAULT and wait_limit_us == 0 and fault == FAULT_NONE:
+        name, st = "mvp_attn_fwd_varlen", lib.mvp_attn_fwd_varlen(*args)
+    else:
+        opts = AttnOptions(int(variant), int(wait_limit_us), int(fault))
+        name, st = "mvp_attn_fwd_varlen_ext", lib.mvp_attn_fwd_varlen_ext(*args, ctypes.byref(opts))
     if st != MVP_OK:
-        raise MvpError("mvp_attn_fwd_varlen", st)
+        raise MvpError(name, st)
 
 
 def attn_fwd_varlen_scan(q, k, v, out, cu_seqlens_q, cu_seqlens_k, max_q_len, max_k_len, ranges, *, lse=None,
@@ -454,7 +474,7 @@ class StepMetadata:
 
 
 def attn_accounting(cu_seqlens_q, seq_lens_k, num_heads_q, num_heads_kv, head_dim, *, context_lens=None,
-                    range_table=None, causal=True, window_left=-1, window_right=-1) -> dict:
+                    range_table=None, causal=True, window_left=-1, window_right=-1, variant=0) -> dict:
     """Work accounting of one attention call from host arrays
     (``mvp_attn_accounting``): the PR #55624 estimate, the exact mask and the
     kernels' executed work, as a dict.  No GPU needed."""
@@ -476,7 +496,8 @@ def attn_accounting(cu_seqlens_q, seq_lens_k, num_heads_q, num_heads_kv, head_di
     p_tb = arr(tbl, "range_table")
     out = AttnCounts()
     st = load_library().mvp_attn_accounting(p_cu, p_sk, p_cl, p_tb, n, num_heads_q, num_heads_kv, head_dim,
-                                            int(bool(causal)), window_left, window_right, ctypes.byref(out))
+                                            int(bool(causal)), window_left, window_right, int(variant),
+                                            ctypes.byref(out))
     del keep
     if st != MVP_OK:
         raise MvpError("mvp_attn_accounting", st)

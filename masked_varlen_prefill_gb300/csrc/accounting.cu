@@ -82,13 +82,15 @@ int pow2_divisor(int g, int cap) {
 extern "C" int mvp_attn_accounting(const int32_t* cu_seqlens_q, const int32_t* seq_lens_k,
                                    const int32_t* context_lens, const int32_t* range_table, int num_reqs,
                                    int num_heads_q, int num_heads_kv, int head_dim, int causal, int window_left,
-                                   int window_right, mvp_attn_counts* out) {
+                                   int window_right, int variant, mvp_attn_counts* out) {
   using namespace mvp;
   if (out == nullptr) return MVP_ERR_ARG;
   *out = mvp_attn_counts{};
   if (num_reqs < 0 || num_heads_q < 1 || num_heads_kv < 1 || num_heads_q % num_heads_kv != 0) return MVP_ERR_ARG;
   if (head_dim != 64 && head_dim != 128 && head_dim != 256 && head_dim != 512) return MVP_ERR_UNSUPPORTED;
   if ((causal != 0 && causal != 1) || window_left < -1 || window_right < -1) return MVP_ERR_ARG;
+  if (variant != MVP_VARIANT_DEFAULT && variant != MVP_VARIANT_D512_HEAD_SPLIT) return MVP_ERR_ARG;
+  if (variant == MVP_VARIANT_D512_HEAD_SPLIT && head_dim != 512) return MVP_ERR_UNSUPPORTED;
   if (num_reqs > 0 && (cu_seqlens_q == nullptr || seq_lens_k == nullptr)) return MVP_ERR_ARG;
   for (int b = 0; b < num_reqs; ++b) {
     const long long ql = static_cast<long long>(cu_seqlens_q[b + 1]) - cu_seqlens_q[b];
@@ -99,7 +101,7 @@ extern "C" int mvp_attn_accounting(const int32_t* cu_seqlens_q, const int32_t* s
 
   const double hq = num_heads_q, hkv = num_heads_kv, d = head_dim;
   const int group = num_heads_q / num_heads_kv;
-  const PrefillShape shape = prefill_tile_shape(head_dim);
+  const PrefillShape shape = prefill_tile_shape(head_dim, variant == MVP_VARIANT_D512_HEAD_SPLIT);
   const int gpack = pow2_divisor(group, 8);
   const int n_hgroups = group / gpack;
   const long long item_pos = shape.item_rows / gpack;  // query positions of an item

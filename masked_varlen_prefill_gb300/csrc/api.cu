@@ -11,6 +11,7 @@
 
 #include "../../include/mvp.h"
 #include "mvp_internal.cuh"
+#include "ptx.cuh"
 
 namespace mvp {
 namespace {
@@ -164,7 +165,8 @@ int attn_fwd_impl(const void* q, void* out, float* lse, const int32_t* cu_seqlen
                   int num_heads_kv, int head_dim, const int32_t* range_table, const int32_t* range_covered,
                   int causal, int window_left, int window_right, const float* sinks, int sink_mode, float scale,
                   void* workspace, size_t workspace_bytes, void* stream, const KVArgs& kv,
-                  const int32_t* scan_ranges = nullptr, int max_ranges = 0) {
+                  const int32_t* scan_ranges = nullptr, int max_ranges = 0,
+                  const mvp_attn_options* opts = nullptr) {
   const void* k = kv.k;
   const void* v = kv.v;
   const bool paged = kv.block_table != nullptr;
@@ -191,6 +193,12 @@ int attn_fwd_impl(const void* q, void* out, float* lse, const int32_t* cu_seqlen
   if (scan_ranges != nullptr && range_table != nullptr) return MVP_ERR_ARG;
   if (scan_ranges != nullptr && (reinterpret_cast<uintptr_t>(scan_ranges) & 7u) != 0) return MVP_ERR_UNSUPPORTED;
   if (static_cast<long long>(total_q) * num_heads_q * head_dim >= (1LL << 40)) return MVP_ERR_UNSUPPORTED;
+  if (opts != nullptr) {
+    if (opts->variant != MVP_VARIANT_DEFAULT && opts->variant != MVP_VARIANT_D512_HEAD_SPLIT) return MVP_ERR_ARG;
+    if (opts->variant == MVP_VARIANT_D512_HEAD_SPLIT && head_dim != 512) return MVP_ERR_UNSUPPORTED;
+    if (opts->fault != MVP_FAULT_NONE && opts->fault != MVP_FAULT_WITHHOLD_PROBS) return MVP_ERR_ARG;
+  }
+  const bool d512_split = opts != nullptr && opts->variant == MVP_VARIANT_D512_HEAD_SPLIT;
 
   // Paged: a TMA box never crosses a cache block.
   auto box_rows = [&](int rows) { return paged ? (rows < (1 << kv.block_shift) ? rows : (1 << kv.block_shift)) : rows; };
@@ -218,6 +226,8 @@ int attn_fwd_impl(const void* q, void* out, float* lse, const int32_t* cu_seqlen
   m.sink_mode = sink_mode;
   m.scale_log2 = scale * 1.4426950408889634f;
   m.scale = scale;
+  m.wait_limit_us = (opts != nullptr && opts->wait_limit_us != 0) ? opts->wait_limit_us : kDefaultWaitLimitUs;
+  m.fault = opts != nullptr ? opts->fault : kFaultNone;
 
   const int group = num_heads_q / num_heads_kv;
   int launches = 0;
@@ -239,7 +249,7 @@ int attn_fwd_impl(const void* q, void* out, float* lse, const int32_t* cu_seqlen
 
   // ------------------------------------------------------------ prefill rows
   if (max_q_len > 1 && prefill_first < num_reqs) {
-    const PrefillShape shape = prefill_tile_shape(head_dim);
+    const PrefillShape shape = prefill_tile_shape(head_dim, d512_split);
     const int gpack = largest_pow2_divisor(group, 8);
     const int bmp = 128 / gpack;
     PrefillParams pp;
@@ -271,7 +281,7 @@ int attn_fwd_impl(const void* q, void* out, float* lse, const int32_t* cu_seqlen
         !encode_3d(&mk, k, head_dim, num_heads_kv, total_k, 64, 1, box_rows(shape.k_box_keys), true) ||
         !encode_3d(&mv, v, head_dim, num_heads_kv, total_k, 64, 1, box_rows(shape.v_box_keys), true))
       return MVP_ERR_UNSUPPORTED;
-    if (launch_prefill(head_dim, pp, mq, mk, mv, st) != cudaSuccess) return MVP_ERR_CUDA;
+    if (launch_prefill(head_dim, d512_split, pp, mq, mk, mv, st) != cudaSuccess) return MVP_ERR_CUDA;
     ++launches;
   }
 
@@ -337,6 +347,21 @@ int mvp_attn_fwd_varlen(const void* q, const void* k, const void* v, void* out, 
   return attn_fwd_impl(q, out, lse, cu_seqlens_q, context_lens, num_reqs, total_q, max_q_len, max_k_len,
                        num_decode_reqs, num_heads_q, num_heads_kv, head_dim, range_table, range_covered, causal,
                        window_left, window_right, sinks, sink_mode, scale, workspace, workspace_bytes, stream, kv);
+}
+
+int mvp_attn_fwd_varlen_ext(const void* q, const void* k, const void* v, void* out, float* lse,
+                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, const int32_t* context_lens,
+                            int num_reqs, int total_q, int total_k, int max_q_len, int max_k_len,
+                            int num_decode_reqs, int num_heads_q, int num_heads_kv, int head_dim,
+                            const int32_t* range_table, const int32_t* range_covered, int causal, int window_left,
+                            int window_right, const float* sinks, int sink_mode, float scale, void* workspace,
+                            size_t workspace_bytes, void* stream, const mvp_attn_options* options) {
+  g_last_launches = 0;
+  KVArgs kv{k, v, total_k, cu_seqlens_k, nullptr, nullptr, 0, 0};
+  return attn_fwd_impl(q, out, lse, cu_seqlens_q, context_lens, num_reqs, total_q, max_q_len, max_k_len,
+                       num_decode_reqs, num_heads_q, num_heads_kv, head_dim, range_table, range_covered, causal,
+                       window_left, window_right, sinks, sink_mode, scale, workspace, workspace_bytes, stream, kv,
+                       nullptr, 0, options);
 }
 
 int mvp_attn_fwd_paged(const void* q, const void* k_cache, const void* v_cache, void* out, float* lse,

@@ -50,7 +50,7 @@ struct DCfg {
 struct __align__(8) DBarriers {
   uint64_t full[kStages];
   uint64_t empty[kStages];
-  int abort_flag;
+  WaitCtl wc;  // abort flag and wait budget of this CTA
 };
 
 template <int DPL>
@@ -153,7 +153,8 @@ __global__ void __launch_bounds__(kThreads)
       mbar_init(&sb.full[s], 1);
       mbar_init(&sb.empty[s], kNW);
     }
-    sb.abort_flag = 0;
+    sb.wc.abort = 0;
+    sb.wc.limit_us = p.m.wait_limit_us;
     mbar_fence_init();
   }
   __syncthreads();
@@ -169,7 +170,7 @@ __global__ void __launch_bounds__(kThreads)
       for (int t = 0; t < n_tiles; ++t) {
         const int s = t % kStages;
         if (t >= kStages &&
-            !mbar_wait(&sb.empty[s], ((t / kStages) - 1) & 1, &sb.abort_flag, p.err, kDevTimeoutLoad)) {
+            !mbar_wait(&sb.empty[s], ((t / kStages) - 1) & 1, &sb.wc, p.err, kDevTimeoutLoad)) {
           ok = false;
           break;
         }
@@ -187,8 +188,8 @@ __global__ void __launch_bounds__(kThreads)
         }
         ++issued;
       }
-      if (!ok) sb.abort_flag = 1;
-      volatile int own_flag = 0;
+      if (!ok) sb.wc.abort = 1;
+      WaitCtl own_flag = own_wait_ctl(&sb.wc);
       for (int s = 0; s < kStages && s < issued; ++s) {
         const int last = ((issued - 1 - s) / kStages) * kStages + s;
         mbar_wait(&sb.full[s], (last / kStages) & 1, &own_flag, nullptr, 0);
@@ -233,7 +234,7 @@ __global__ void __launch_bounds__(kThreads)
   bool ok = true;
   for (int t = 0; t < n_tiles && ok; ++t) {
     const int s = t % kStages;
-    if (!mbar_wait(&sb.full[s], (t / kStages) & 1, &sb.abort_flag, p.err, kDevTimeoutLoad)) {
+    if (!mbar_wait(&sb.full[s], (t / kStages) & 1, &sb.wc, p.err, kDevTimeoutLoad)) {
       ok = false;
       break;
     }

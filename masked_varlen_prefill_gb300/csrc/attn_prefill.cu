@@ -48,7 +48,7 @@
 // * Every mbarrier wait is bounded (ptx.cuh).
 #include <cuda_bf16.h>
 
-#include <cstdlib>
+#include <mutex>
 
 #include "mask.cuh"
 #include "mvp_internal.cuh"
@@ -209,7 +209,7 @@ struct __align__(8) Barriers {
   uint64_t x_empty[2];    // ... the peer has read what this CTA sent into its slot i
   uint64_t xchg[4][2];  // softmax column-half pairs (per TMEM lane quarter), by parity
   uint32_t tmem_base;
-  int abort_flag;
+  WaitCtl wc;  // abort flag and wait budget of this CTA
 };
 
 // Items are numbered q tile fastest (latest tile first), then head group,
@@ -370,7 +370,7 @@ __device__ __forceinline__ Plan plan_tiles(const Item& it, const PrefillParams& 
 // warp) and release its slot.
 __device__ __forceinline__ bool consume_plan(Barriers& sb, int n, int lane, PlanEntry& e, int* err) {
   const int slot = n % kPlanRing;
-  const bool ok = mbar_wait(&sb.plan_full[slot], (n / kPlanRing) & 1, &sb.abort_flag, err, kDevTimeoutOther);
+  const bool ok = mbar_wait(&sb.plan_full[slot], (n / kPlanRing) & 1, &sb.wc, err, kDevTimeoutOther);
   e = sb.plans[slot];
   __syncwarp();
   if (lane == 0) mbar_arrive(&sb.plan_empty[slot]);
@@ -382,7 +382,7 @@ __device__ __forceinline__ bool consume_plan(Barriers& sb, int n, int lane, Plan
 // overwrite slot k & 1 before this thread has passed exchange k + 1).  The
 // wait is bounded, so a failed partner cannot hang the pair.
 __device__ __forceinline__ bool pair_exchange(float2* slots, uint64_t* xb, int& k, int half, int row, float2 mine,
-                                              float2& theirs, volatile int* abort_flag, int* err) {
+                                              float2& theirs, volatile WaitCtl* abort_flag, int* err) {
   float2* slot = slots + (k & 1) * (2 * kBM);
   slot[half * kBM + row] = mine;
   mbar_arrive(&xb[k & 1]);
@@ -465,7 +465,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       mbar_init(&sb.xchg[i][0], 64);
       mbar_init(&sb.xchg[i][1], 64);
     }
-    sb.abort_flag = 0;
+    sb.wc.abort = 0;
+    sb.wc.limit_us = p.m.wait_limit_us;
     for (int i = 0; i < kPlanRing; ++i) mbar_init(&sb.plan_taken[i], 1);
     mbar_fence_init();
   }
@@ -612,9 +613,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           bool free;
           if constexpr (C::MERGED_RELEASE) {
             const int tl = kc - 1;  // the previous item's last tile
-            free = mbar_wait(&sb.s_full[tl & 1], (tl >> 1) & 1, &sb.abort_flag, p.err, kDevTimeoutMma);
+            free = mbar_wait(&sb.s_full[tl & 1], (tl >> 1) & 1, &sb.wc, p.err, kDevTimeoutMma);
           } else {
-            free = mbar_wait(&sb.q_empty, (qn - 1) & 1, &sb.abort_flag, p.err, kDevTimeoutMma);
+            free = mbar_wait(&sb.q_empty, (qn - 1) & 1, &sb.wc, p.err, kDevTimeoutMma);
           }
           if (!free) return false;
         }
@@ -630,8 +631,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (kc >= C::KST) {
           const int tp = kc - C::KST;  // the tile that used this stage before
           const bool free = C::MERGED_RELEASE
-                                ? mbar_wait(&sb.s_full[tp & 1], (tp >> 1) & 1, &sb.abort_flag, p.err, kDevTimeoutLoad)
-                                : mbar_wait(&sb.k_empty[s], (tp / C::KST) & 1, &sb.abort_flag, p.err, kDevTimeoutLoad);
+                                ? mbar_wait(&sb.s_full[tp & 1], (tp >> 1) & 1, &sb.wc, p.err, kDevTimeoutLoad)
+                                : mbar_wait(&sb.k_empty[s], (tp / C::KST) & 1, &sb.wc, p.err, kDevTimeoutLoad);
           if (!free) return false;
         }
         if (leader) mbar_arrive_expect_tx(&sb.k_full[s], C::MMA_CTAS * C::K_BYTES);
@@ -661,8 +662,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (vc >= C::VST) {
           const int tp = vc - C::VST;
           const bool free = C::MERGED_RELEASE
-                                ? mbar_wait(&sb.o_done[tp & 1], (tp >> 1) & 1, &sb.abort_flag, p.err, kDevTimeoutLoad)
-                                : mbar_wait(&sb.v_empty[s], (tp / C::VST) & 1, &sb.abort_flag, p.err, kDevTimeoutLoad);
+                                ? mbar_wait(&sb.o_done[tp & 1], (tp >> 1) & 1, &sb.wc, p.err, kDevTimeoutLoad)
+                                : mbar_wait(&sb.v_empty[s], (tp / C::VST) & 1, &sb.wc, p.err, kDevTimeoutLoad);
           if (!free) return false;
         }
         if (leader) mbar_arrive_expect_tx(&sb.v_full[s], C::MMA_CTAS * C::V_BYTES);
@@ -729,10 +730,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       // flag (issued copies always complete, and must before the CTA exits).
       // A pair's full barriers live in rank 0 and count both CTAs' copies;
       // rank 1 stays until rank 0 has drained (the final cluster barrier).
-      if (lane == 0 && !leader && !ok) sb.abort_flag = 1;
+      if (lane == 0 && !leader && !ok) sb.wc.abort = 1;
       if (lane == 0 && leader) {
-        if (!ok) sb.abort_flag = 1;
-        volatile int own_flag = 0;
+        if (!ok) sb.wc.abort = 1;
+        WaitCtl own_flag = own_wait_ctl(&sb.wc);
         if (qn > 0) mbar_wait(&sb.q_full, (qn - 1) & 1, &own_flag, nullptr, 0);
         for (int i = 0; i < 4; ++i) {
           // stage i was last armed by tile i + KST * m, m = (issued - 1 - i) / KST (phase parity m)
@@ -761,13 +762,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (!ok || e.last) break;
         const Plan& pl = e.pl;
         if (pl.n_tiles == 0) continue;
-        ok = mbar_wait_spin(&sb.q_full, qn & 1, &sb.abort_flag, p.err, kDevTimeoutLoad);
+        ok = mbar_wait_spin(&sb.q_full, qn & 1, &sb.wc, p.err, kDevTimeoutLoad);
         ++qn;
         for (int j = 0; ok && j <= pl.n_tiles; ++j) {
           if (j < pl.n_tiles) {
             const int t = T + j;
             const int s = t % C::KST;
-            if (!mbar_wait_spin(&sb.k_full[s], (t / C::KST) & 1, &sb.abort_flag, p.err, kDevTimeoutLoad)) {
+            if (!mbar_wait_spin(&sb.k_full[s], (t / C::KST) & 1, &sb.wc, p.err, kDevTimeoutLoad)) {
               ok = false;
               break;
             }
@@ -790,19 +791,19 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           }
           if (j >= 1) {
             const int t = T + j - 1;
-            if (!mbar_wait_spin(&sb.p_full[t & 1], (t >> 1) & 1, &sb.abort_flag, p.err, kDevTimeoutSoftmax)) {
+            if (!mbar_wait_spin(&sb.p_full[t & 1], (t >> 1) & 1, &sb.wc, p.err, kDevTimeoutSoftmax)) {
               ok = false;
               break;
             }
             // The item's first PV overwrites O: the epilogue warps must have
             // read the previous item's O out of TMEM (both CTAs of a pair).
             if (j == 1 && qn > 1 &&
-                !mbar_wait_spin(&sb.o_free, (qn - 2) & 1, &sb.abort_flag, p.err, kDevTimeoutSoftmax)) {
+                !mbar_wait_spin(&sb.o_free, (qn - 2) & 1, &sb.wc, p.err, kDevTimeoutSoftmax)) {
               ok = false;
               break;
             }
             const int s = t % C::VST;
-            if (!mbar_wait_spin(&sb.v_full[s], (t / C::VST) & 1, &sb.abort_flag, p.err, kDevTimeoutLoad)) {
+            if (!mbar_wait_spin(&sb.v_full[s], (t / C::VST) & 1, &sb.wc, p.err, kDevTimeoutLoad)) {
               ok = false;
               break;
             }
@@ -821,11 +822,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
         T += pl.n_tiles;
       }
-      if (!ok && lane == 0) sb.abort_flag = 1;
+      if (!ok && lane == 0) sb.wc.abort = 1;
       // All issued MMAs must finish before TMEM is released (and, in a pair,
       // before the peer's shared memory and TMEM go away).
       mma_commit_elect<C::MMA_CTAS>(&sb.final_mma);
-      volatile int own_flag = 0;
+      WaitCtl own_flag = own_wait_ctl(&sb.wc);
       mbar_wait(&sb.final_mma, 0, &own_flag, p.err, kDevTimeoutMma);
     } else if (warp == 1) {
       // A pair's rank 1: its TMEM is allocated by this warp; rank 0 issues the MMAs.
@@ -842,7 +843,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const int slot = n % kPlanRing;
         bool good = true;
         if (lane == 0 && n >= kPlanRing)
-          good = mbar_wait(&sb.plan_empty[slot], ((n / kPlanRing) - 1) & 1, &sb.abort_flag, p.err, kDevTimeoutOther);
+          good = mbar_wait(&sb.plan_empty[slot], ((n / kPlanRing) - 1) & 1, &sb.wc, p.err, kDevTimeoutOther);
         good = __shfl_sync(kFullMask, good, 0);
         if (good && lane == 0) {
           sb.plans[slot] = e;
@@ -903,7 +904,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             // entry c - 1 needed entry c - 5 consumed, so the slot's phase
             // parity is exact)
             if (lane == 0 && ct >= 0)
-              good = mbar_wait(&sb.plan_taken[ct % kPlanRing], (ct / kPlanRing) & 1, &sb.abort_flag, p.err,
+              good = mbar_wait(&sb.plan_taken[ct % kPlanRing], (ct / kPlanRing) & 1, &sb.wc, p.err,
                                kDevTimeoutOther);
             if (lane == 0 && good) item = claim(qc == 0);
             ok = __shfl_sync(kFullMask, good, 0);
@@ -925,7 +926,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             if constexpr (TWO) {
               if (lane == 0 && ok) {
                 if (qc >= kPlanRing)
-                  ok = mbar_wait_cluster(&sb.claim_empty[slot], ((qc / kPlanRing) - 1) & 1, &sb.abort_flag, p.err,
+                  ok = mbar_wait_cluster(&sb.claim_empty[slot], ((qc / kPlanRing) - 1) & 1, &sb.wc, p.err,
                                          kDevTimeoutOther);
                 if (ok) {
                   st_cluster_u32(mapa_shared(smem_u32(&sb.claims[slot]), 1), static_cast<uint32_t>(item));
@@ -936,7 +937,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             }
           } else {
             if (lane == 0) {
-              ok = mbar_wait_cluster(&sb.claim_full[slot], (qc / kPlanRing) & 1, &sb.abort_flag, p.err,
+              ok = mbar_wait_cluster(&sb.claim_full[slot], (qc / kPlanRing) & 1, &sb.wc, p.err,
                                      kDevTimeoutOther);
               if (ok) {
                 item = sb.claims[slot];
@@ -1045,7 +1046,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if constexpr (C::SPLITD) {
           if (js < pl.n_tiles) {
             const int ts = T + js;
-            if (!mbar_wait(&sb.s_full[ts & 1], (ts >> 1) & 1, &sb.abort_flag, p.err, kDevTimeoutMma)) {
+            if (!mbar_wait(&sb.s_full[ts & 1], (ts >> 1) & 1, &sb.wc, p.err, kDevTimeoutMma)) {
               ok = false;
               break;
             }
@@ -1060,7 +1061,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             // the slot's previous tile (two back) must have been read by the peer
             const int slot = xs & 1;
             if (xs >= 2 &&
-                !mbar_wait_cluster(&sb.x_empty[slot], ((xs - 2) >> 1) & 1, &sb.abort_flag, p.err, kDevTimeoutSoftmax)) {
+                !mbar_wait_cluster(&sb.x_empty[slot], ((xs - 2) >> 1) & 1, &sb.wc, p.err, kDevTimeoutSoftmax)) {
               ok = false;
               break;
             }
@@ -1078,7 +1079,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const int t = T + j;
         const int kb = pl.kb_lo + j;
         const uint32_t scol = tmem + lane_base + C::S_COL + (t & 1) * BN;
-        if (!C::SPLITD && !mbar_wait(&sb.s_full[t & 1], (t >> 1) & 1, &sb.abort_flag, p.err, kDevTimeoutMma)) {
+        if (!C::SPLITD && !mbar_wait(&sb.s_full[t & 1], (t >> 1) & 1, &sb.wc, p.err, kDevTimeoutMma)) {
           ok = false;
           break;
         }
@@ -1099,7 +1100,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           // side, so every warp-wide remote store and local load covers 512
           // contiguous bytes.
           const int slot = xr & 1;
-          if (!mbar_wait_cluster(&sb.x_full[slot], (xr >> 1) & 1, &sb.abort_flag, p.err, kDevTimeoutSoftmax)) {
+          if (!mbar_wait_cluster(&sb.x_full[slot], (xr >> 1) & 1, &sb.wc, p.err, kDevTimeoutSoftmax)) {
             ok = false;
             break;
           }
@@ -1145,7 +1146,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if constexpr (C::SPLIT > 1) {
           // the two halves of a row meet once per tile
           float2 other;
-          if (!pair_exchange(xslots, xb, xk, half, row, make_float2(mx_raw, 0.f), other, &sb.abort_flag, p.err)) {
+          if (!pair_exchange(xslots, xb, xk, half, row, make_float2(mx_raw, 0.f), other, &sb.wc, p.err)) {
             ok = false;
             break;
           }
@@ -1196,7 +1197,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         // tcgen05.ld/st are warp-collective); each half corrects its columns.
         if (j > 0 && __any_sync(kFullMask, need)) {
           const int tp = t - 1;  // the previous tile's PV must have landed in O
-          if (!mbar_wait(&sb.o_done[tp & 1], (tp >> 1) & 1, &sb.abort_flag, p.err, kDevTimeoutMma)) ok = false;
+          if (!mbar_wait(&sb.o_done[tp & 1], (tp >> 1) & 1, &sb.wc, p.err, kDevTimeoutMma)) ok = false;
           if (ok) {
             tc_fence_after();
             const uint32_t ocol = tmem + lane_base + C::O_COL + half * C::HDV;
@@ -1214,7 +1215,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
+        // (fault injection for the timeout tests: one warp withholds the first
+        // tile's arrival, so the MMA issuer's bounded wait runs out)
+        const bool withhold = p.m.fault == kFaultWithholdProbs && T == 0 && j == 0 &&
+                              warp == C::SOFTMAX_BEGIN && (C::NCTA == 1 || cluster_rank() == 0);
+        if (lane == 0 && !withhold) {
           if constexpr (C::PAIR) mbar_arrive_cluster(p_full_addr0 + (t & 1) * 8);
           else mbar_arrive(&sb.p_full[t & 1]);
         }
@@ -1226,7 +1231,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       if constexpr (C::SPLIT > 1) {
         // combine the halves' partial sums
         float2 other;
-        if (ok && pair_exchange(xslots, xb, xk, half, row, make_float2(l_sum, l_lse), other, &sb.abort_flag, p.err)) {
+        if (ok && pair_exchange(xslots, xb, xk, half, row, make_float2(l_sum, l_lse), other, &sb.wc, p.err)) {
           l_sum += other.x;
           l_lse += other.y;
         } else {
@@ -1239,7 +1244,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       if (half == 0) {
         const int slot = hk % C::EPI_SLOTS;
         if (hk >= C::EPI_SLOTS &&
-            !mbar_wait(&sb.epi_empty[slot], ((hk / C::EPI_SLOTS) - 1) & 1, &sb.abort_flag, p.err, kDevTimeoutStore))
+            !mbar_wait(&sb.epi_empty[slot], ((hk / C::EPI_SLOTS) - 1) & 1, &sb.wc, p.err, kDevTimeoutStore))
           ok = false;
         const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
         const float inv_l = (l_sum > 0.f) ? 1.f / l_sum : 0.f;
@@ -1278,7 +1283,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       const int qi = e.it.pos0 + pos_off + row / p.gpack;
       const bool valid = qi < e.it.q_len;
       const int slot = hk % C::EPI_SLOTS;
-      if (!mbar_wait(&sb.epi_full[slot], (hk / C::EPI_SLOTS) & 1, &sb.abort_flag, p.err, kDevTimeoutSoftmax)) {
+      if (!mbar_wait(&sb.epi_full[slot], (hk / C::EPI_SLOTS) & 1, &sb.wc, p.err, kDevTimeoutSoftmax)) {
         ok = false;
         break;
       }
@@ -1289,7 +1294,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       const bool has_tiles = e.pl.n_tiles > 0;
       if (has_tiles) {
         const int tl = T + e.pl.n_tiles - 1;  // the item's last PV
-        if (!mbar_wait(&sb.o_done[tl & 1], (tl >> 1) & 1, &sb.abort_flag, p.err, kDevTimeoutMma)) {
+        if (!mbar_wait(&sb.o_done[tl & 1], (tl >> 1) & 1, &sb.wc, p.err, kDevTimeoutMma)) {
           ok = false;
           break;
         }
@@ -1337,7 +1342,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         p.lse[static_cast<size_t>(head) * p.total_q + e.it.q0 + qi] = info.y;
       T += e.pl.n_tiles;
     }
-    if (!ok && lane == 0) sb.abort_flag = 1;
+    if (!ok && lane == 0) sb.wc.abort = 1;
   }
 
   tc_fence_before();
@@ -1365,22 +1370,33 @@ using Cfg256 = Cfg<256, 256, 128, 2, 2, 2>;
 // alternative keeps O resident by splitting the head dimension over a 2-CTA
 // cluster (no recomputation, partial scores exchanged every tile); it meets
 // the same tolerances but measured slower on GB300 (the exchange and its
-// cluster-scope release cost more per tile than the recomputed QK), so it is
-// opt-in (environment MVP_D512_HEAD_SPLIT=1).
+// cluster-scope release cost more per tile than the recomputed QK), so a
+// caller selects it explicitly (the head-split variant of
+// mvp_attn_fwd_varlen_ext).
 using Cfg512 = Cfg<512, 256, 64, 2, 2, 2>;
 using Cfg512S = Cfg<512, 512, 64, 2, 1, 2, 1>;
 
-bool d512_head_split() {
-  const char* v = getenv("MVP_D512_HEAD_SPLIT");
-  return v != nullptr && v[0] == '1';
-}
+// Per-device launch state of one kernel instantiation: its dynamic shared
+// memory attribute is set once, and the number of co-resident CTA pairs is
+// queried once (clusters must fit within a GPC).  Guarded by a mutex: two host
+// threads may make their first call on a device at the same time.
+struct LaunchState {
+  bool attr_set = false;
+  int active_pairs = 0;
+};
+std::mutex g_launch_mutex;
 
 template <class C>
 cudaError_t launch_cfg(const PrefillParams& p, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                        cudaStream_t stream) {
-  auto kern = p.m.block_table != nullptr ? attn_prefill_kernel<C, true> : attn_prefill_kernel<C, false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  const bool paged = p.m.block_table != nullptr;
+  auto kern = paged ? attn_prefill_kernel<C, true> : attn_prefill_kernel<C, false>;
+  static LaunchState state[2][64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  LaunchState& ls = state[paged ? 1 : 0][dev];
   const long long n_items =
       static_cast<long long>(p.n_qtiles) * (p.num_reqs - p.req_offset) * p.hkv * p.n_hgroups * C::DV_SPLIT;
   if (n_items <= 0) return cudaSuccess;
@@ -1398,24 +1414,24 @@ cudaError_t launch_cfg(const PrefillParams& p, const CUtensorMap& mq, const CUte
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;  // (the occupancy query below sees the cluster shape only)
-  // Persistent groups: as many CTAs (pairs) as can be resident at once (the
-  // pair count is queried once per device; clusters must fit within a GPC).
+  // Persistent groups: as many CTAs (pairs) as can be resident at once.
   int groups = p.n_ctas / C::NCTA;
-  if constexpr (C::NCTA > 1) {
-    static int active_pairs[64] = {};
-    int dev = 0;
-    e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (active_pairs[dev] == 0) {
+  {
+    std::lock_guard<std::mutex> lock(g_launch_mutex);
+    if (!ls.attr_set) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+      if (e != cudaSuccess) return e;
+      ls.attr_set = true;
+    }
+    if (C::NCTA > 1 && ls.active_pairs == 0) {
       cfg.gridDim = dim3(groups * C::NCTA);
       int active = 0;
       e = cudaOccupancyMaxActiveClusters(&active, kern, &cfg);
       if (e != cudaSuccess) return e;
-      active_pairs[dev] = active > 0 ? active : groups;
+      ls.active_pairs = active > 0 ? active : groups;
     }
-    if (active_pairs[dev] < groups) groups = active_pairs[dev];
   }
+  if (C::NCTA > 1 && ls.active_pairs < groups) groups = ls.active_pairs;
   if (n_items < groups) groups = static_cast<int>(n_items);
   cfg.gridDim = dim3(groups * C::NCTA);
   cfg.numAttrs = 2;
@@ -1436,24 +1452,24 @@ PrefillShape shape_of() {
           C::ITEM_ROWS};
 }
 
-PrefillShape prefill_tile_shape(int head_dim) {
+PrefillShape prefill_tile_shape(int head_dim, bool d512_head_split) {
   switch (head_dim) {
     case 64: return shape_of<Cfg64>();
     case 128: return shape_of<Cfg128>();
     case 256: return shape_of<Cfg256>();
-    case 512: return d512_head_split() ? shape_of<Cfg512S>() : shape_of<Cfg512>();
+    case 512: return d512_head_split ? shape_of<Cfg512S>() : shape_of<Cfg512>();
     default: return {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
   }
 }
 
-cudaError_t launch_prefill(int head_dim, const PrefillParams& p, const CUtensorMap& mq, const CUtensorMap& mk,
-                           const CUtensorMap& mv, cudaStream_t stream) {
+cudaError_t launch_prefill(int head_dim, bool d512_head_split, const PrefillParams& p, const CUtensorMap& mq,
+                           const CUtensorMap& mk, const CUtensorMap& mv, cudaStream_t stream) {
   switch (head_dim) {
     case 64: return launch_cfg<Cfg64>(p, mq, mk, mv, stream);
     case 128: return launch_cfg<Cfg128>(p, mq, mk, mv, stream);
     case 256: return launch_cfg<Cfg256>(p, mq, mk, mv, stream);
     case 512:
-      return d512_head_split() ? launch_cfg<Cfg512S>(p, mq, mk, mv, stream) : launch_cfg<Cfg512>(p, mq, mk, mv, stream);
+      return d512_head_split ? launch_cfg<Cfg512S>(p, mq, mk, mv, stream) : launch_cfg<Cfg512>(p, mq, mk, mv, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -21,6 +21,12 @@ struct FillParams {
 
 cudaError_t launch_fill(const FillParams& p, cudaStream_t stream);
 
+// Faults a caller can ask for to test the bounded-wait path (never set by
+// the plain entry points).  kFaultWithholdProbs: the first softmax warp of
+// every prefill CTA (rank 0 of each pair) does not signal that its first key
+// tile's probabilities are in TMEM, so the MMA issuer's wait for them runs out.
+enum FaultInjection : int { kFaultNone = 0, kFaultWithholdProbs = 1 };
+
 // ----------------------------------------------------------------- masks
 // Per-row visible set = base interval U range interval (closed, in key
 // coordinates of the request).  Shared by the prefill and decode kernels.
@@ -43,6 +49,8 @@ struct MaskParams {
   int sink_mode;
   float scale_log2;          // scale * log2(e)
   float scale;               // > 0
+  uint32_t wait_limit_us;    // budget of one bounded device wait
+  int fault;                 // FaultInjection: kFaultNone except in the timeout tests
 };
 
 // ----------------------------------------------------------------- prefill
@@ -83,9 +91,11 @@ struct PrefillShape {
   int oc;          // O columns one issuing CTA accumulates
   int mma_m;       // M of each MMA
 };
-PrefillShape prefill_tile_shape(int head_dim);
+// d512_head_split selects the head-dim-split form of D = 512 (TMEM-resident
+// O, no recomputed QK) instead of the default value split.
+PrefillShape prefill_tile_shape(int head_dim, bool d512_head_split);
 
-cudaError_t launch_prefill(int head_dim, const PrefillParams& p, const CUtensorMap& map_q,
+cudaError_t launch_prefill(int head_dim, bool d512_head_split, const PrefillParams& p, const CUtensorMap& map_q,
                            const CUtensorMap& map_k, const CUtensorMap& map_v, cudaStream_t stream);
 
 // ----------------------------------------------------------------- decode

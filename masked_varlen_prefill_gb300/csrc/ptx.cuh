@@ -24,10 +24,30 @@ enum DeviceError : int {
   kDevQueueConflict = 6,    // the prefill work queue was taken over by another launch
 };
 
-// Wall-clock budget of one barrier wait.  Legitimate waits in these kernels
-// last microseconds (one tile of loads or MMAs); one second means something
-// is broken.
-constexpr unsigned long long kWaitTimeoutNs = 1000000000ull;
+// Default wall-clock budget of one barrier wait.  Legitimate waits in these
+// kernels last microseconds (one tile of loads or MMAs); one second means
+// something is broken.  A launch may set a shorter budget (MaskParams::
+// wait_limit_us), which the tests use to make a withheld arrival time out
+// quickly.
+constexpr uint32_t kDefaultWaitLimitUs = 1000000u;
+
+// Per-CTA wait control, kept in shared memory: the abort flag every bounded
+// wait polls (raised by the first wait that gives up, so the others stop
+// early) and the budget of one wait in microseconds.
+struct WaitCtl {
+  int abort;
+  uint32_t limit_us;
+};
+
+// A local control for drain waits, which must not stop on the CTA's abort
+// flag (copies already issued always complete, and must before the CTA
+// exits) but keep the launch's budget.
+__device__ __forceinline__ WaitCtl own_wait_ctl(const volatile WaitCtl* ctl) {
+  WaitCtl w;
+  w.abort = 0;
+  w.limit_us = ctl->limit_us;
+  return w;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -70,19 +90,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait until the phase with parity `parity` of `bar` has completed.  Returns
-// false (after recording `code` in *err and raising *abort) when the wait
-// exceeds kWaitTimeoutNs, or as soon as another thread of the CTA aborted.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          int* err, int code) {
+// false (after recording `code` in *err and raising ctl->abort) when the wait
+// exceeds ctl->limit_us, or as soon as another thread of the CTA aborted.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile WaitCtl* ctl, int* err,
+                                          int code) {
   if (mbar_try_wait(bar, parity)) return true;
-  unsigned long long t0 = global_timer_ns();
+  const unsigned long long t0 = global_timer_ns();
+  const unsigned long long limit_ns = 1000ull * ctl->limit_us;
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 255u) == 0) {
-      if (*abort_flag) return false;
-      if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+      if (ctl->abort) return false;
+      if (global_timer_ns() - t0 > limit_ns) {
         if (err) atomicCAS(err, 0, code);
-        *abort_flag = 1;
+        ctl->abort = 1;
         return false;
       }
     }
@@ -104,17 +125,18 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
 // mbar_wait for a latency-critical single thread (the MMA issuer): polls with
 // the non-suspending test_wait, so the thread resumes the moment the phase
 // completes instead of after a suspend interval.  Same bound and abort rules.
-__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err,
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, volatile WaitCtl* ctl, int* err,
                                                int code) {
   if (mbar_test_wait(bar, parity)) return true;
-  unsigned long long t0 = global_timer_ns();
+  const unsigned long long t0 = global_timer_ns();
+  const unsigned long long limit_ns = 1000ull * ctl->limit_us;
   for (uint32_t it = 1;; ++it) {
     if (mbar_test_wait(bar, parity)) return true;
     if ((it & 1023u) == 0) {
-      if (*abort_flag) return false;
-      if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+      if (ctl->abort) return false;
+      if (global_timer_ns() - t0 > limit_ns) {
         if (err) atomicCAS(err, 0, code);
-        *abort_flag = 1;
+        ctl->abort = 1;
         return false;
       }
     }
@@ -341,17 +363,18 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
 }
 
 // mbar_wait with acquire at cluster scope (arrivals from the peer CTA).
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile WaitCtl* ctl,
                                                   int* err, int code) {
   if (mbar_try_wait_cluster(bar, parity)) return true;
-  unsigned long long t0 = global_timer_ns();
+  const unsigned long long t0 = global_timer_ns();
+  const unsigned long long limit_ns = 1000ull * ctl->limit_us;
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait_cluster(bar, parity)) return true;
     if ((it & 255u) == 0) {
-      if (*abort_flag) return false;
-      if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+      if (ctl->abort) return false;
+      if (global_timer_ns() - t0 > limit_ns) {
         if (err) atomicCAS(err, 0, code);
-        *abort_flag = 1;
+        ctl->abort = 1;
         return false;
       }
     }

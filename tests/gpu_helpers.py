@@ -44,8 +44,9 @@ def oracle_table(w):
     return table, n
 
 
-def run_gpu(w, q, k, v, sinks, use_workspace=True, with_lse=True, dev="cuda", num_decode_reqs=-1):
-    """Fill the range table (if any) and run attention on the GPU."""
+def run_gpu(w, q, k, v, sinks, use_workspace=True, with_lse=True, dev="cuda", num_decode_reqs=-1, **ext):
+    """Fill the range table (if any) and run attention on the GPU.  ``ext``:
+    further keywords of ``attn_fwd_varlen`` (variant, wait_limit_us)."""
     cu_q, cu_k = device_meta(w, dev)
     table = covered = None
     if w.ranges is not None:
@@ -65,7 +66,7 @@ def run_gpu(w, q, k, v, sinks, use_workspace=True, with_lse=True, dev="cuda", nu
     mvp.attn_fwd_varlen(q, k, v, out, cu_q, cu_k, max(max(w.q_lens), 1), max(max(w.k_lens), 1), lse=lse,
                         range_table=table, range_covered=covered, causal=w.causal,
                         window_left=w.window_left, window_right=w.window_right, sinks=sinks,
-                        sink_mode=w.sink_mode, scale=w.scale, workspace=ws, num_decode_reqs=num_decode_reqs)
+                        sink_mode=w.sink_mode, scale=w.scale, workspace=ws, num_decode_reqs=num_decode_reqs, **ext)
     torch.cuda.synchronize()
     assert mvp.get_last_device_error() == 0
     return out, lse, table, covered

@@ -37,11 +37,11 @@ HEAD_SPLIT_FLOPS = 2 * (2 * 128 * 64 * (256 + 256))
 KT = {64: 128, 128: 64, 256: 32, 512: 32}
 
 
-def _counts(w, table=None, context_lens=None):
+def _counts(w, table=None, context_lens=None, variant=0):
     cu_q, _ = w.cu_seqlens()
     return mvp.attn_accounting(cu_q, w.k_lens, w.num_heads_q, w.num_heads_kv, w.head_dim,
                                context_lens=context_lens, range_table=table, causal=w.causal,
-                               window_left=w.window_left, window_right=w.window_right)
+                               window_left=w.window_left, window_right=w.window_right, variant=variant)
 
 
 def _table(w):
@@ -113,11 +113,10 @@ def test_scaled_workloads_exact_and_executed(name):
     assert c["prefill_mma_flops"] == c["prefill_tiles"] * FLOPS_PER_TILE[d]
 
 
-def test_d512_head_split_accounting(monkeypatch):
+def test_d512_head_split_accounting():
     w = workloads.scaled_workload("global_causal_d512")
     base = _counts(w)
-    monkeypatch.setenv("MVP_D512_HEAD_SPLIT", "1")
-    split = _counts(w)
+    split = _counts(w, variant=mvp.VARIANT_D512_HEAD_SPLIT)
     # the same visible pairs; items of 128 rows with every value column (the
     # default's items are 256 rows with half of them); QK is not recomputed
     # per value half, so at most two thirds of the default's MMA work (less
@@ -190,5 +189,10 @@ def test_argument_errors():
         mvp.attn_accounting([0, 1], [3], 2, 1, 96)          # head_dim
     with pytest.raises(mvp.MvpError):
         mvp.attn_accounting([0, 1], [3], 2, 1, 64, window_left=-2)
+    with pytest.raises(mvp.MvpError):
+        mvp.attn_accounting([0, 1], [3], 2, 1, 64, variant=7)   # unknown variant
+    with pytest.raises(mvp.MvpError) as e:
+        mvp.attn_accounting([0, 1], [3], 2, 1, 256, variant=mvp.VARIANT_D512_HEAD_SPLIT)
+    assert e.value.status == mvp.MVP_ERR_UNSUPPORTED
     lib = mvp.load_library()
-    assert lib.mvp_attn_accounting(None, None, None, None, 0, 1, 1, 64, 1, -1, -1, None) == mvp.MVP_ERR_ARG
+    assert lib.mvp_attn_accounting(None, None, None, None, 0, 1, 1, 64, 1, -1, -1, 0, None) == mvp.MVP_ERR_ARG

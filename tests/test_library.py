@@ -75,6 +75,30 @@ def test_argument_errors_return_before_any_launch(lib):
     assert _attn(lib, total_q=0) == mvp.MVP_OK  # nothing to do
 
 
+def _attn_ext(lib, variant=0, wait_limit_us=0, fault=0, **over):
+    args = dict(q=1 << 20, k=1 << 20, v=1 << 20, out=1 << 20, lse=None, cu_q=1 << 20, cu_k=1 << 20, ctx=None,
+                num_reqs=1, total_q=4, total_k=4, max_q=4, max_k=4, ndec=-1, hq=4, hkv=2, d=128, table=None,
+                covered=None, causal=1, wl=-1, wr=-1, sinks=None, sink_mode=0, scale=0.1, ws=None, ws_bytes=0,
+                stream=None)
+    args.update(over)
+    opts = mvp.AttnOptions(variant, wait_limit_us, fault)
+    return lib.mvp_attn_fwd_varlen_ext(*[args[k] for k in (
+        "q", "k", "v", "out", "lse", "cu_q", "cu_k", "ctx", "num_reqs", "total_q", "total_k", "max_q", "max_k", "ndec",
+        "hq", "hkv", "d", "table", "covered", "causal", "wl", "wr", "sinks", "sink_mode", "scale", "ws",
+        "ws_bytes", "stream")], ctypes.byref(opts))
+
+
+def test_ext_option_errors_return_before_any_launch(lib):
+    assert _attn_ext(lib, variant=7) == mvp.MVP_ERR_ARG
+    assert _attn_ext(lib, variant=-1) == mvp.MVP_ERR_ARG
+    assert _attn_ext(lib, variant=mvp.VARIANT_D512_HEAD_SPLIT, d=128) == mvp.MVP_ERR_UNSUPPORTED
+    assert _attn_ext(lib, fault=9) == mvp.MVP_ERR_ARG
+    # the plain argument checks apply as well
+    assert _attn_ext(lib, d=96) == mvp.MVP_ERR_UNSUPPORTED
+    assert _attn_ext(lib, hq=3, hkv=2) == mvp.MVP_ERR_ARG
+    assert _attn_ext(lib, total_q=0) == mvp.MVP_OK
+
+
 def _paged(lib, **over):
     args = dict(q=1 << 20, kc=1 << 20, vc=1 << 20, out=1 << 20, lse=None, cu_q=1 << 20, seq_k=1 << 20,
                 bt=1 << 20, bs=16, max_blocks=4, num_blocks=8, ctx=None, num_reqs=1, total_q=4, max_q=4, max_k=64,
