@@ -27,6 +27,7 @@
 namespace {
 
 constexpr size_t kStaticScratchBytes = 16u << 20;  // 16 MiB
+constexpr size_t kHeaderBytes = 256;                 // work-queue header ahead of the partials
 
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
@@ -67,9 +68,13 @@ int mvp_attn_fwd_varlen_static_ws(const void* q, const void* k, const void* v, v
                                   const int32_t* range_covered, int causal, int window_left, int window_right,
                                   const float* sinks, int sink_mode, float scale, void* stream) {
   if (num_reqs < 1 || num_decode_reqs < -1 || num_decode_reqs > num_reqs) return MVP_ERR_ARG;
-  const int decode_reqs = num_decode_reqs < 0 ? num_reqs : num_decode_reqs;
-  const size_t need = mvp_attn_workspace_size(decode_reqs, num_heads_q, head_dim, max_k_len);
-  if (need > kStaticScratchBytes) return MVP_ERR_CAPACITY;  // batch too large for the fixed scratch
+  if (num_heads_q < 1 || head_dim < 1) return MVP_ERR_ARG;
+  // The attention call splits long decode rows over as many CTAs as the
+  // scratch holds partials for; the array must hold at least one split's
+  // partials of the decode rows (the stated maximum batch).
+  const size_t decode_reqs = static_cast<size_t>(num_decode_reqs < 0 ? num_reqs : num_decode_reqs);
+  const size_t one_split = decode_reqs * static_cast<size_t>(num_heads_q) * (static_cast<size_t>(head_dim) + 2) * 4;
+  if (kHeaderBytes + one_split > kStaticScratchBytes) return MVP_ERR_CAPACITY;  // batch too large for the array
   void* scratch = nullptr;
   if (scratch_address(&scratch) != cudaSuccess) return MVP_ERR_CUDA;
   return mvp_attn_fwd_varlen(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, context_lens, num_reqs, total_q,
