@@ -2,9 +2,10 @@
 
 Step = one pass of the whole path over one batch: the range-table fill
 (``fill_query_ranges``) and the attention forward (``attn_fwd_varlen``) on the
-mm_prefix sliding-layer workload (4 x 4096-token prefills, 16 q / 8 KV heads,
-D 256, causal 1024-token window OR-ed with 8 bidirectional 256-token ranges per
-request), inputs resident in HBM, L2 flushed (256 MiB write) between steps.
+chunked-prefill workload (8 requests, each a 2048-token chunk after a context
+of 0..30000 tokens, 16 q / 8 KV heads, D 256, causal 4096-token window OR-ed
+with 1..64 bidirectional ranges per request), inputs resident in HBM, L2
+flushed (256 MiB write) between steps.
 
 value  = effective TFLOP/s over unmasked score entries:
          4 * D * Hq * (exact number of visible (query, key) pairs) / step time.
@@ -13,8 +14,13 @@ e2e    = the same metric through the public API from pinned HOST tensors, the
          timed region.
 roofline: the attention kernel's algorithmic FLOPs per launch / its average
          CUDA-event duration, against the measured bf16 tensor peak.
+configs: every other workload of the benchmark set measured in the same run
+         (the mm_prefix sliding layer, the D 512 global layer, both mixed
+         serving batches with their decode and prefill sub-batches and the
+         mixed roofline, the tiny windowed batch) and the range fill at a
+         stress size against the HBM roofline.
 cpu_baseline: the float64 CPU oracle on a bounded sample of query rows of
-         the same workload, on this host's cores.
+         the headline workload, on this host's cores.
 
 ``--impl reference`` times that oracle (the only reference implementation
 that exists for this path) on the same metric.  Multi-GPU (torchrun): every
@@ -43,10 +49,29 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "unmasked-attention TFLOP/s (bf16) & % tensor peak; prefill tokens/s"
-WORKLOAD = "mm_prefix_sliding"
-WORKLOAD_DESC = ("mm_prefix sliding layer: 4 x 4096-token prefill, ctx 0, 16 q / 8 KV heads, D 256, bf16 "
-                 "N(0,1), causal 1024-token window OR 8 bidirectional 256-token ranges per request "
-                 "(range table filled on the GPU each step)")
+WORKLOAD = "chunked_prefill_ranges"
+WORKLOAD_DESCS = {
+    "tiny_window_sinks": ("tiny windowed attention: lengths 37 and 5, ctx 0, 4 q / 2 KV heads, D 64, bf16 N(0,1), "
+                          "non-causal symmetric window 8, key-0-bias sinks"),
+    "mm_prefix_sliding": ("mm_prefix sliding layer: 4 x 4096-token prefill, ctx 0, 16 q / 8 KV heads, D 256, bf16 "
+                          "N(0,1), causal 1024-token window OR 8 bidirectional 256-token ranges per request "
+                          "(range table filled on the GPU each step)"),
+    "global_causal_d512": ("global layer: 2 x 8192-token prefill, ctx 0, 8 q / 2 KV heads, D 512, bf16 N(0,1), "
+                           "pure causal, no ranges, no sinks"),
+    "chunked_prefill_ranges": ("chunked prefill with context offset: 8 requests x 2048-token chunk after a context "
+                               "U{0..30000}, 16 q / 8 KV heads, D 256, bf16 N(0,1), causal 4096-token window OR "
+                               "1-64 bidirectional ranges per request (64-320 tokens, some degenerate, some clipped "
+                               "at the chunk) (range table filled on the GPU each step)"),
+    "mixed_serving_a": ("mixed serving batch, full-causal layer: 256 decode rows (ctx U{1024..32768}) + 4 prefill "
+                        "chunks of 1024 after ctx U{0..16384}, 32 q / 8 KV heads, D 128, bf16 N(0,1), null-logit "
+                        "sinks"),
+    "mixed_serving_b": ("mixed serving batch, 4096-window layer: 256 decode rows (ctx U{1024..32768}) + 4 prefill "
+                        "chunks of 1024 after ctx U{0..16384}, 32 q / 8 KV heads, D 128, bf16 N(0,1), null-logit "
+                        "sinks"),
+}
+WORKLOAD_DESC = WORKLOAD_DESCS[WORKLOAD]
+CONFIG_NUMBER = {"tiny_window_sinks": "1", "mm_prefix_sliding": "2", "global_causal_d512": "3",
+                 "chunked_prefill_ranges": "4", "mixed_serving_a": "5a", "mixed_serving_b": "5b"}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
 
@@ -267,6 +292,20 @@ def time_oracle(w, counts, rows_per_req, pool, cores):
     return wall, flops, sum(len(r) for _, r in tasks), cpu_s
 
 
+def oracle_workers(w, cores):
+    """Workers for the oracle pool: one per core, fewer when the host's
+    available memory would not hold a float64 copy of the largest request's
+    q, K and V (with its temporaries) per worker within a quarter of it."""
+    per = 2 * 8 * (max(w.k_lens) * w.num_heads_kv * w.head_dim * 2 + max(w.q_lens) * w.num_heads_q * w.head_dim)
+    try:
+        avail = os.sysconf("SC_AVPHYS_PAGES") * os.sysconf("SC_PAGE_SIZE")
+    except (ValueError, OSError, AttributeError):
+        avail = 0
+    if avail <= 0:
+        return max(1, min(cores, 4))
+    return max(1, min(cores, int(0.25 * avail // max(per, 1))))
+
+
 def make_pool(cores, w_name):
     """Spawned process pool, one single-threaded-BLAS worker per core, each
     holding the workload's inputs; returns once every worker is ready."""
@@ -317,6 +356,8 @@ def aggregate(per_rank_flops, max_seconds):
     return per_rank_flops / max_seconds / 1e12
 
 
+
+
 # ----------------------------------------------------------------- main arms
 def run_reference(args, world, rank):
     from masked_varlen_prefill_gb300 import workloads
@@ -331,9 +372,9 @@ def run_reference(args, world, rank):
         table = np.full((w.total_q, 2), -1, dtype=np.int32)
         ort.fill_by_spans(table, ort.ranges_from_padded(w.ranges), cu_q, np.asarray(w.k_lens))
     counts = visible_counts_per_row(w, table)
-    cores = os.cpu_count() or 1
+    cores = oracle_workers(w, os.cpu_count() or 1)
     pool = make_pool(cores, args.workload)
-    rows_per_req = 64
+    rows_per_req = 64 if max(w.k_lens) <= 8192 else 32
     for _ in range(args.warmup):
         time_oracle(w, counts, rows_per_req, pool, cores)
     total_t, total_f, nrows = 0.0, 0.0, 0
@@ -350,8 +391,7 @@ def run_reference(args, world, rank):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": WORKLOAD_DESC if args.workload == WORKLOAD else args.workload,
-                       "parallelism": "replicas"},
+            "config": {"workload": WORKLOAD_DESCS.get(args.workload, args.workload), "parallelism": "replicas"},
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -364,6 +404,238 @@ def _leading_decode(w):
     while n < w.num_reqs and w.q_lens[n] == 1:
         n += 1
     return n
+
+
+class Batch:
+    """One workload's inputs resident on the device, and the library calls of
+    one step on them: the range-table fill (when the workload has ranges) and
+    the attention call, packed, paged or in scan mode.  Decode requests come
+    first in every workload, so the call passes their count."""
+
+    def __init__(self, w, dev, paged=0, scan=False):
+        import torch
+
+        import masked_varlen_prefill_gb300 as mvp
+        from masked_varlen_prefill_gb300 import workloads
+
+        self.mvp, self.torch = mvp, torch
+        self.w, self.dev, self.paged_bs, self.scan = w, dev, paged, scan
+        self.n_dec = _leading_decode(w)
+        self.q, self.k, self.v, self.sinks = workloads.make_tensors(w, device=dev)
+        self.cu_q_np, self.cu_k_np = w.cu_seqlens()
+        self.cu_q = torch.from_numpy(self.cu_q_np).to(dev)
+        self.cu_k = torch.from_numpy(self.cu_k_np).to(dev)
+        self.seq_lens = torch.tensor(w.k_lens, dtype=torch.int32, device=dev)
+        self.ranges = torch.from_numpy(w.ranges).to(dev) if w.ranges is not None else None
+        self.table = torch.empty((w.total_q, 2), dtype=torch.int32, device=dev) if self.ranges is not None else None
+        self.covered = torch.empty(1, dtype=torch.int32, device=dev) if self.ranges is not None else None
+        self.out = torch.empty_like(self.q)
+        self.max_q, self.max_k = max(w.q_lens), max(w.k_lens)
+        # workspace: the prefill work queue (header) and the decode split
+        # partials; uninitialised, as a serving engine would allocate it once
+        nbytes = mvp.attn_workspace_size(self.n_dec, w.num_heads_q, w.head_dim, self.max_k)
+        self.ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev) if nbytes else None
+        self.pg = None
+        if paged:
+            kc, vc, bt, sl = workloads.to_paged(self.k, self.v, w.k_lens, paged, seed=w.seed)
+            self.pg = dict(k_cache=kc, v_cache=vc, block_table=bt, seq_lens_k=sl)
+        self.kw = dict(causal=w.causal, window_left=w.window_left, window_right=w.window_right, sinks=self.sinks,
+                       sink_mode=w.sink_mode, scale=w.scale, workspace=self.ws)
+
+    def fill(self):
+        if self.ranges is None or self.scan:
+            return 0
+        self.mvp.fill_query_ranges(self.ranges, self.cu_q, self.seq_lens, self.table, num_tokens=self.w.total_q,
+                                   rows_written=self.covered)
+        return self.mvp.last_launch_count()
+
+    def attn(self, lo=0, hi=None):
+        """Attention over requests [lo, hi) of the batch (default: all)."""
+        mvp, w = self.mvp, self.w
+        hi = w.num_reqs if hi is None else hi
+        nd = max(0, min(self.n_dec, hi) - lo)
+        cq, ck = self.cu_q[lo:hi + 1], self.cu_k[lo:hi + 1]
+        mq, mk = max(w.q_lens[lo:hi]), max(w.k_lens[lo:hi])
+        if self.scan:
+            mvp.attn_fwd_varlen_scan(self.q, self.k, self.v, self.out, cq, ck, mq, mk,
+                                     None if self.ranges is None else self.ranges[lo:hi], num_decode_reqs=nd,
+                                     **self.kw)
+        elif self.pg is not None:
+            mvp.attn_fwd_paged(self.q, self.pg["k_cache"], self.pg["v_cache"], self.out, cq,
+                               self.pg["seq_lens_k"][lo:hi], self.pg["block_table"][lo:hi], self.paged_bs, mq, mk,
+                               range_table=self.table, range_covered=self.covered, num_decode_reqs=nd, **self.kw)
+        else:
+            mvp.attn_fwd_varlen(self.q, self.k, self.v, self.out, cq, ck, mq, mk, range_table=self.table,
+                                range_covered=self.covered, num_decode_reqs=nd, **self.kw)
+        return mvp.last_launch_count()
+
+    def step(self):
+        # nothing between the two calls: the attention kernel may start its
+        # setup while the fill kernel runs (programmatic dependent launch)
+        n = self.fill()
+        return n + self.attn()
+
+    def prepare(self):
+        """Fill the table once outside any timed region (scan mode has no fill
+        step; its exact visible count still comes from the table, which the
+        workloads' non-overlapping ranges make identical to the scan)."""
+        if self.ranges is not None:
+            self.mvp.fill_query_ranges(self.ranges, self.cu_q, self.seq_lens, self.table,
+                                       num_tokens=self.w.total_q, rows_written=self.covered)
+
+    def accounting(self):
+        """Exact visible pairs per row (from the GPU-filled table, which the
+        tests pin bit-exact) and the library's accounting of the call."""
+        w = self.w
+        table_np = None if self.table is None else self.table.cpu().numpy()
+        counts = visible_counts_per_row(w, table_np)
+        covered = self.covered is not None and int(self.covered.item()) != 0
+        acct = self.mvp.attn_accounting(self.cu_q_np, w.k_lens, w.num_heads_q, w.num_heads_kv, w.head_dim,
+                                        range_table=table_np if covered else None, causal=w.causal,
+                                        window_left=w.window_left, window_right=w.window_right)
+        flops = 4.0 * w.head_dim * w.num_heads_q * int(counts.sum())
+        if acct["exact_flops"] != flops:
+            raise RuntimeError("library accounting disagrees with the bench's visible count")
+        return counts, acct
+
+    def release(self):
+        for name in ("q", "k", "v", "sinks", "out", "ws", "pg", "table", "covered", "ranges"):
+            setattr(self, name, None)
+
+
+def time_calls(fn, reps, flush, stream):
+    """Mean seconds of ``fn`` over ``reps`` runs, each bracketed by CUDA events
+    on ``stream`` with an L2 flush before it (outside the events)."""
+    import torch
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for a, b in ev:
+        flush.zero_()
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in ev) / reps / 1e3
+
+
+def sub_batches(bt, counts, acct, peaks, flush, stream, reps):
+    """Decode-only and prefill-only sub-batches of a mixed batch, or the
+    attention call alone: kernel time, achieved rate and fraction of the
+    roofline of each side; returns (sub, dec_s, pre_s, dec_bytes, pre_flops)."""
+    w, n_dec = bt.w, bt.n_dec
+    peak_t = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    peak_b = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    cu_q_l = [int(x) for x in bt.cu_q_np]
+    visible = int(counts.sum())
+    dec_vis = int(counts[:cu_q_l[n_dec]].sum()) if n_dec else 0
+    pre_flops = 4.0 * w.head_dim * w.num_heads_q * (visible - dec_vis)
+    if 0 < n_dec < w.num_reqs:
+        for _ in range(2):
+            time_calls(lambda: bt.attn(0, n_dec), 1, flush, stream)
+            time_calls(lambda: bt.attn(n_dec, w.num_reqs), 1, flush, stream)
+        dec_s = time_calls(lambda: bt.attn(0, n_dec), reps, flush, stream)
+        pre_s = time_calls(lambda: bt.attn(n_dec, w.num_reqs), reps, flush, stream)
+    else:
+        time_calls(bt.attn, 1, flush, stream)
+        attn_s = time_calls(bt.attn, reps, flush, stream)
+        dec_s, pre_s = (attn_s, 0.0) if n_dec == w.num_reqs else (0.0, attn_s)
+    dec_bytes = dec_vis * w.num_heads_kv * w.head_dim * 2 * 2 + n_dec * w.num_heads_q * w.head_dim * 2 * 2
+    sub = {}
+    if n_dec:
+        sub["decode"] = {"ms": 1e3 * dec_s, "rows": n_dec, "algorithmic_bytes": dec_bytes,
+                         "GB_per_s": dec_bytes / dec_s / 1e9, "frac_hbm": dec_bytes / dec_s / 1e9 / peak_b}
+    if pre_s > 0:
+        sub["prefill"] = {"ms": 1e3 * pre_s, "TFLOP_per_s": pre_flops / pre_s / 1e12,
+                          "frac_tensor": pre_flops / pre_s / 1e12 / peak_t,
+                          "exact_over_executed_mma": (pre_flops / acct["prefill_mma_flops"]
+                                                      if acct["prefill_mma_flops"] else None)}
+    return sub, dec_s, pre_s, dec_bytes, pre_flops
+
+
+def mixed_roofline(step_s, flops, dec_bytes, acct, peaks):
+    """The step against max(algorithmic bytes / HBM peak, FLOPs / tensor peak):
+    bytes = the decode rows' K/V (once per KV head) and q / out plus the
+    prefill rows' compulsory bytes; FLOPs = every visible entry's 4 D Hq."""
+    peak_t = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    peak_b = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    nbytes = dec_bytes + acct["prefill_compulsory_bytes"]
+    bound = max(nbytes / (peak_b * 1e9), flops / (peak_t * 1e12))
+    return {"algorithmic_bytes": nbytes, "flops": flops, "bytes_bound_ms": 1e3 * nbytes / (peak_b * 1e9),
+            "flops_bound_ms": 1e3 * flops / (peak_t * 1e12), "bound_ms": 1e3 * bound, "step_ms": 1e3 * step_s,
+            "frac": bound / step_s}
+
+
+def measure_config(name, dev, peaks, flush, stream, reps):
+    """One workload of the benchmark set: the whole step (fill + attention)
+    timed over ``reps`` L2-flushed runs, its sub-batches, and for mixed
+    batches the mixed roofline."""
+    import torch
+
+    import masked_varlen_prefill_gb300 as mvp
+    from masked_varlen_prefill_gb300 import workloads
+
+    peak_t = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    w = workloads.workload(name)
+    bt = Batch(w, dev)
+    for _ in range(3):
+        flush.zero_()
+        bt.step()
+    torch.cuda.synchronize()
+    if mvp.get_last_device_error() != 0:
+        raise RuntimeError(f"device timeout during {name}")
+    counts, acct = bt.accounting()
+    visible = int(counts.sum())
+    flops = 4.0 * w.head_dim * w.num_heads_q * visible
+    step_s = time_calls(bt.step, reps, flush, stream)
+    sub, dec_s, pre_s, dec_bytes, pre_flops = sub_batches(bt, counts, acct, peaks, flush, stream, reps)
+    if mvp.get_last_device_error() != 0:
+        raise RuntimeError(f"device timeout during {name}")
+    res = {"config": CONFIG_NUMBER.get(name, name), "workload": WORKLOAD_DESCS.get(name, name),
+           "step_ms": 1e3 * step_s, "visible_entries": visible, "TFLOP_per_s": flops / step_s / 1e12,
+           "frac_tensor": flops / step_s / 1e12 / peak_t, "tokens_per_s": w.total_q / step_s,
+           "sub_batches": sub}
+    if 0 < bt.n_dec < w.num_reqs:
+        res["mixed_roofline"] = mixed_roofline(step_s, flops, dec_bytes, acct, peaks)
+    elif pre_s > 0:
+        res["kernel"] = {"ms": 1e3 * pre_s, "TFLOP_per_s": pre_flops / pre_s / 1e12,
+                         "frac_tensor": pre_flops / pre_s / 1e12 / peak_t}
+    bt.release()
+    del bt
+    torch.cuda.empty_cache()
+    return res
+
+
+def measure_fill_stress(dev, peaks, flush, stream, reps):
+    """The range fill at a stress size (4096 requests x 1024 rows, 64 ranges
+    each): algorithmic bytes 8 N (table rows written) + 4 (2 B + 1) (offsets
+    and lengths) + 8 B R (ranges read) against the HBM peak."""
+    import torch
+
+    import masked_varlen_prefill_gb300 as mvp
+    from masked_varlen_prefill_gb300 import workloads
+
+    peak_b = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    ranges_np, q_lens, seq = workloads.fill_stress_case()
+    nb, nr = ranges_np.shape[0], ranges_np.shape[1]
+    qsl = np.zeros(nb + 1, dtype=np.int32)
+    qsl[1:] = np.cumsum(q_lens)
+    n = int(qsl[-1])
+    ranges = torch.from_numpy(ranges_np).to(dev)
+    d_qsl = torch.from_numpy(qsl).to(dev)
+    d_seq = torch.tensor(seq, dtype=torch.int32, device=dev)
+    out = torch.empty((n, 2), dtype=torch.int32, device=dev)
+    covered = torch.empty(1, dtype=torch.int32, device=dev)
+
+    def fill():
+        mvp.fill_query_ranges(ranges, d_qsl, d_seq, out, num_tokens=n, rows_written=covered)
+
+    time_calls(fill, 3, flush, stream)
+    t = time_calls(fill, reps, flush, stream)
+    nbytes = 8 * n + 4 * (2 * nb + 1) + 8 * nb * nr
+    return {"requests": nb, "rows": n, "ranges_per_request": nr, "algorithmic_bytes": nbytes, "us": 1e6 * t,
+            "GB_per_s": nbytes / t / 1e9, "frac_hbm": nbytes / t / 1e9 / peak_b,
+            "timing": "CUDA events around the fill call (one kernel plus the 4-byte flag reset), L2 flushed "
+                      "between calls"}
 
 
 def graph_measure(args, w, q, k, v, sinks, flops, flush, stream, dev):
@@ -454,6 +726,120 @@ def graph_measure(args, w, q, k, v, sinks, flops, flush, stream, dev):
                       "staging to after a synchronize"}
 
 
+def e2e_measure(args, bt, flops, stream, world):
+    """Every step copies its inputs from pinned host memory and its output
+    back, inside the timed region.  Steps are pipelined the way a serving loop
+    would run them: two device buffer sets, host->device copies on one
+    stream, the fill and attention calls on another, device->host copies on a
+    third, so step i + 1's inputs travel while step i computes and step i - 1's
+    output returns.  The sequential form (copy, compute, copy on one stream)
+    is reported beside it."""
+    import torch
+
+    import masked_varlen_prefill_gb300 as mvp
+
+    w, dev, n_dec = bt.w, bt.dev, bt.n_dec
+    paged = bt.pg
+    max_q, max_k = bt.max_q, bt.max_k
+    kv_names = ["k", "v", "cu_k"] if paged is None else ["k_cache", "v_cache", "block_table", "seq_lens_k"]
+    kv_dev = [bt.k, bt.v, bt.cu_k] if paged is None else [paged[n] for n in kv_names]
+    names = ["q", "cu_q"] + kv_names + (["seq_lens", "ranges"] if bt.ranges is not None else []) + \
+        (["sinks"] if bt.sinks is not None else [])
+    dev_in = [bt.q, bt.cu_q] + kv_dev + ([bt.seq_lens, bt.ranges] if bt.ranges is not None else []) + \
+        ([bt.sinks] if bt.sinks is not None else [])
+    host_in = [t.cpu().pin_memory() for t in dev_in]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = bt.out.numel() * bt.out.element_size()
+    sets = []
+    for b in range(2):
+        d = dict(zip(names, dev_in if b == 0 else [torch.empty_like(t) for t in dev_in]))
+        d["out"] = bt.out if b == 0 else torch.empty_like(bt.out)
+        d["table"] = bt.table if (b == 0 or bt.table is None) else torch.empty_like(bt.table)
+        d["covered"] = bt.covered if (b == 0 or bt.covered is None) else torch.empty_like(bt.covered)
+        d["ws"] = bt.ws if (b == 0 or bt.ws is None) else torch.empty_like(bt.ws)
+        d["host_out"] = torch.empty(bt.out.shape, dtype=bt.out.dtype, pin_memory=True)
+        sets.append(d)
+
+    def compute(d, st):
+        kw2 = dict(bt.kw, sinks=d.get("sinks"), workspace=d["ws"])
+        if args.scan:
+            mvp.attn_fwd_varlen_scan(d["q"], d["k"], d["v"], d["out"], d["cu_q"], d["cu_k"], max_q, max_k,
+                                     d.get("ranges"), num_decode_reqs=n_dec, stream=st, **kw2)
+            return
+        if bt.ranges is not None:
+            mvp.fill_query_ranges(d["ranges"], d["cu_q"], d["seq_lens"], d["table"], num_tokens=w.total_q,
+                                  rows_written=d["covered"], stream=st)
+        if paged is not None:
+            mvp.attn_fwd_paged(d["q"], d["k_cache"], d["v_cache"], d["out"], d["cu_q"], d["seq_lens_k"],
+                               d["block_table"], args.paged, max_q, max_k, range_table=d["table"],
+                               range_covered=d["covered"], num_decode_reqs=n_dec, stream=st, **kw2)
+        else:
+            mvp.attn_fwd_varlen(d["q"], d["k"], d["v"], d["out"], d["cu_q"], d["cu_k"], max_q, max_k,
+                                range_table=d["table"], range_covered=d["covered"], num_decode_reqs=n_dec,
+                                stream=st, **kw2)
+
+    s_in, s_cmp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+
+    def pipelined(n_steps):
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        t0.record(s_in)
+        for i in range(n_steps):
+            b = i % 2
+            d = sets[b]
+            if i >= 2:
+                s_in.wait_event(ev_done[b])  # step i - 2 no longer reads these inputs
+            with torch.cuda.stream(s_in):
+                for n, h in zip(names, host_in):
+                    d[n].copy_(h, non_blocking=True)
+                ev_in[b].record(s_in)
+            s_cmp.wait_event(ev_in[b])
+            if i >= 2:
+                s_cmp.wait_event(ev_out[b])  # step i - 2's output has left this buffer
+            with torch.cuda.stream(s_cmp):
+                compute(d, s_cmp)
+                ev_done[b].record(s_cmp)
+            s_out.wait_event(ev_done[b])
+            with torch.cuda.stream(s_out):
+                d["host_out"].copy_(d["out"], non_blocking=True)
+                ev_out[b].record(s_out)
+        t1.record(s_out)
+        s_in.wait_event(ev_out[(n_steps - 1) % 2])
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1) / 1e3
+
+    def sequential(n_steps):
+        d = sets[0]
+        ts = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_steps)]
+        for a, z in ts:
+            a.record(stream)
+            for n, h in zip(names, host_in):
+                d[n].copy_(h, non_blocking=True)
+            compute(d, stream)
+            d["host_out"].copy_(d["out"], non_blocking=True)
+            z.record(stream)
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(z) for a, z in ts) / 1e3
+
+    pipelined(3)
+    sequential(2)
+    barrier(world)
+    e2e_s = reduce_max(pipelined(args.e2e_steps), world)
+    seq_s = reduce_max(sequential(args.e2e_steps), world)
+    if mvp.get_last_device_error() != 0:
+        raise RuntimeError("device timeout during the e2e steps")
+    return {"value": aggregate(flops * args.e2e_steps * world, e2e_s), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": args.e2e_steps,
+            "ms_per_step": 1e3 * e2e_s / args.e2e_steps,
+            "timing": "pinned host inputs -> device, fill + attention, output -> pinned host, every step; "
+                      "steps pipelined over two buffer sets and three streams",
+            "sequential": {"value": aggregate(flops * args.e2e_steps * world, seq_s), "unit": "TFLOP/s",
+                           "ms_per_step": 1e3 * seq_s / args.e2e_steps}}
+
+
 def run_gpu(args, world, rank, local):
     import torch
 
@@ -469,95 +855,28 @@ def run_gpu(args, world, rank, local):
     mvp.load_library()
     peaks, peak_src = load_peaks()
 
+    w = workloads.scaled_workload(args.workload) if args.scaled else workloads.workload(args.workload)
     # CPU baseline pool first (spawned, rank 0 only)
     pool = None
-    cores = os.cpu_count() or 1
+    cores = oracle_workers(w, os.cpu_count() or 1)
     if rank == 0 and not args.no_cpu_baseline:
         pool = make_pool(cores, args.workload)
 
-    w = workloads.scaled_workload(args.workload) if args.scaled else workloads.workload(args.workload)
-    n_dec = _leading_decode(w)
-    q, k, v, sinks = workloads.make_tensors(w, device=dev)
-    cu_q_np, cu_k_np = w.cu_seqlens()
-    cu_q = torch.from_numpy(cu_q_np).to(dev)
-    cu_k = torch.from_numpy(cu_k_np).to(dev)
-    seq_lens = torch.tensor(w.k_lens, dtype=torch.int32, device=dev)
-    ranges = torch.from_numpy(w.ranges).to(dev) if w.ranges is not None else None
-    table = torch.empty((w.total_q, 2), dtype=torch.int32, device=dev) if ranges is not None else None
-    covered = torch.empty(1, dtype=torch.int32, device=dev) if ranges is not None else None
-    out = torch.empty_like(q)
-    max_q, max_k = max(w.q_lens), max(w.k_lens)
-    # workspace: the prefill work queue (header) and the decode split partials;
-    # uninitialised, as a serving engine would allocate it once
-    nbytes = mvp.attn_workspace_size(n_dec, w.num_heads_q, w.head_dim, max_k)
-    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev) if nbytes else None
-    paged = None
-    if args.paged:
-        kc, vc, bt, sl = workloads.to_paged(k, v, w.k_lens, args.paged, seed=w.seed)
-        paged = dict(k_cache=kc, v_cache=vc, block_table=bt, seq_lens_k=sl)
+    bt = Batch(w, dev, paged=args.paged, scan=args.scan)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    kw = dict(causal=w.causal, window_left=w.window_left, window_right=w.window_right, sinks=sinks,
-              sink_mode=w.sink_mode, scale=w.scale, workspace=ws)
-
-    def fill():
-        if ranges is None or args.scan:
-            return 0
-        mvp.fill_query_ranges(ranges, cu_q, seq_lens, table, num_tokens=w.total_q, rows_written=covered)
-        return mvp.last_launch_count()
-
-    def attn(lo=0, hi=None):
-        """Attention over requests [lo, hi) of the batch (default: all)."""
-        hi = w.num_reqs if hi is None else hi
-        if args.scan:
-            nd = max(0, min(n_dec, hi) - lo)
-            mvp.attn_fwd_varlen_scan(q, k, v, out, cu_q[lo:hi + 1], cu_k[lo:hi + 1], max(w.q_lens[lo:hi]),
-                                     max(w.k_lens[lo:hi]), None if ranges is None else ranges[lo:hi],
-                                     num_decode_reqs=nd, **kw)
-        elif paged is not None:
-            nd = max(0, min(n_dec, hi) - lo)
-            mvp.attn_fwd_paged(q, paged["k_cache"], paged["v_cache"], out, cu_q[lo:hi + 1],
-                               paged["seq_lens_k"][lo:hi], paged["block_table"][lo:hi], args.paged,
-                               max(w.q_lens[lo:hi]), max(w.k_lens[lo:hi]), range_table=table,
-                               range_covered=covered, num_decode_reqs=nd, **kw)
-        elif lo == 0 and hi == w.num_reqs:
-            mvp.attn_fwd_varlen(q, k, v, out, cu_q, cu_k, max_q, max_k, range_table=table,
-                                range_covered=covered, num_decode_reqs=n_dec, **kw)
-        else:
-            nd = max(0, min(n_dec, hi) - lo)
-            mvp.attn_fwd_varlen(q, k, v, out, cu_q[lo:hi + 1], cu_k[lo:hi + 1], max(w.q_lens[lo:hi]),
-                                max(w.k_lens[lo:hi]), range_table=table, range_covered=covered,
-                                num_decode_reqs=nd, **kw)
-        return mvp.last_launch_count()
-
-    def step():
-        # nothing between the two calls: the attention kernel may start its
-        # setup while the fill kernel runs (programmatic dependent launch)
-        n = fill()
-        return n + attn()
-
-    if args.scan and ranges is not None:
-        # scan mode has no fill step; the table is filled once, outside the
-        # timed steps, for the exact visible count (the workloads' ranges do
-        # not overlap, so the scan and the table see the same keys)
-        mvp.fill_query_ranges(ranges, cu_q, seq_lens, table, num_tokens=w.total_q, rows_written=covered)
+    if args.scan:
+        bt.prepare()
     for _ in range(args.warmup):
         flush.zero_()
-        step()
+        bt.step()
     torch.cuda.synchronize()
     if mvp.get_last_device_error() != 0:
         raise RuntimeError("device timeout during warm-up")
 
-    # accounting (host), from the GPU-filled table, which the tests pin bit-exact
-    table_np = None if table is None else table.cpu().numpy()
-    counts = visible_counts_per_row(w, table_np)
+    counts, acct = bt.accounting()
     visible = int(counts.sum())
     flops = 4.0 * w.head_dim * w.num_heads_q * visible
-    acct = mvp.attn_accounting(cu_q_np, w.k_lens, w.num_heads_q, w.num_heads_kv, w.head_dim,
-                               range_table=table_np if (table_np is not None and int(covered.item())) else None,
-                               causal=w.causal, window_left=w.window_left, window_right=w.window_right)
-    if acct["exact_flops"] != flops:
-        raise RuntimeError("library accounting disagrees with the bench's visible count")
     est = acct["est_attn_qk_flops"] + acct["est_attn_av_flops"]
     accounting = {
         "estimate_flops_pr55624": est, "exact_flops": flops, "executed_mma_flops": acct["prefill_mma_flops"],
@@ -572,6 +891,7 @@ def run_gpu(args, world, rank, local):
         "decode_cta_read_bytes": acct["decode_cta_read_bytes"],
         "source": "mvp_attn_accounting (estimate: vLLM PR #55624 ExecutionContext with the window clamp)"}
 
+    # ------------------------------------------------------------- timed steps
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     sampler = ClockSampler(local)
@@ -583,7 +903,7 @@ def run_gpu(args, world, rank, local):
     for i in range(args.steps):
         flush.zero_()
         starts[i].record(stream)
-        launches += step()
+        launches += bt.step()
         ends[i].record(stream)
     torch.cuda.synchronize()
     sampler.mark("t1")
@@ -598,47 +918,17 @@ def run_gpu(args, world, rank, local):
     ms_per_step = 1e3 * max_s / args.steps
     tokens_per_s = w.total_q * args.steps * world / max_s
 
-    def time_sub(lo, hi, reps):
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
-        for a, b in ev:
-            flush.zero_()
-            a.record(stream)
-            attn(lo, hi)
-            b.record(stream)
-        torch.cuda.synchronize()
-        return sum(a.elapsed_time(b) for a, b in ev) / reps / 1e3
-
     # ------------------------------------------------------------- roofline
     peak_t = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     peak_b = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-    cu_q_l = [int(x) for x in cu_q_np]
-    dec_vis = int(counts[:cu_q_l[n_dec]].sum()) if n_dec else 0
-    pre_flops = 4.0 * w.head_dim * w.num_heads_q * (visible - dec_vis)
-    sub = {}
-    if 0 < n_dec < w.num_reqs:
-        for _ in range(2):
-            time_sub(0, n_dec, 1)
-            time_sub(n_dec, w.num_reqs, 1)
-        dec_s = time_sub(0, n_dec, max(3, args.steps // 4))
-        pre_s = time_sub(n_dec, w.num_reqs, max(3, args.steps // 4))
-    else:
-        # the attention call alone (the table from the last fill), same L2 flush
-        time_sub(0, w.num_reqs, 1)
-        attn_s = time_sub(0, w.num_reqs, max(3, args.steps // 4))
-        dec_s, pre_s = (attn_s, 0.0) if n_dec == w.num_reqs else (0.0, attn_s)
-    dec_bytes = (dec_vis * w.num_heads_kv * w.head_dim * 2 * 2 + n_dec * w.num_heads_q * w.head_dim * 2 * 2)
-    if n_dec:
-        sub["decode"] = {"ms": 1e3 * dec_s, "rows": n_dec, "algorithmic_bytes": dec_bytes,
-                         "GB_per_s": dec_bytes / dec_s / 1e9, "frac_hbm": dec_bytes / dec_s / 1e9 / peak_b}
-    if pre_s > 0:
-        sub["prefill"] = {"ms": 1e3 * pre_s, "TFLOP_per_s": pre_flops / pre_s / 1e12,
-                          "frac_tensor": pre_flops / pre_s / 1e12 / peak_t}
+    sub_reps = max(3, args.steps // 4)
+    sub, dec_s, pre_s, dec_bytes, pre_flops = sub_batches(bt, counts, acct, peaks, flush, stream, sub_reps)
     kernel_dir = os.path.join(ROOT, "masked_varlen_prefill_gb300", "csrc")
     if pre_s >= dec_s:
         achieved = pre_flops / pre_s / 1e12
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_t, "unit": "TFLOP/s",
                     "frac": achieved / peak_t,
-                    "traffic": (None if (paged is not None or args.scaled)
+                    "traffic": (None if (args.paged or args.scaled or args.scan)
                                 else load_traffic(os.path.join(kernel_dir, "attn_prefill.cu"), args.workload)),
                     "kernel": f"attn_prefill_kernel (D={w.head_dim})",
                     "peak_source": f"bf16_tflops (burst) of {peak_src}", "kernel_ms_per_launch": 1e3 * pre_s}
@@ -648,128 +938,18 @@ def run_gpu(args, world, rank, local):
                     "frac": achieved / peak_b, "traffic": None, "kernel": f"attn_decode_kernel (D={w.head_dim})",
                     "peak_source": f"hbm_gbs of {peak_src}", "kernel_ms_per_launch": 1e3 * dec_s}
     fill_ms = 0.0
-    if ranges is not None and not args.scan:
-        fe = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(10)]
-        for a, b in fe:
-            flush.zero_()
-            a.record(stream)
-            fill()
-            b.record(stream)
-        torch.cuda.synchronize()
-        fill_ms = sum(a.elapsed_time(b) for a, b in fe) / len(fe)
+    if bt.ranges is not None and not args.scan:
+        fill_ms = 1e3 * time_calls(bt.fill, 10, flush, stream)
     roofline["fill_ms_per_launch"] = fill_ms
+    mixed = mixed_roofline(max_s / args.steps, flops, dec_bytes, acct, peaks) if 0 < bt.n_dec < w.num_reqs else None
 
     # ------------------------------------------------------------- e2e (host buffers)
-    # Every step copies its inputs from pinned host memory and its output
-    # back, inside the timed region.  Steps are pipelined the way a serving
-    # loop would run them: two device buffer sets, host->device copies on one
-    # stream, the fill and attention calls on another, device->host copies on
-    # a third, so step i + 1's inputs travel while step i computes and step
-    # i - 1's output returns.  The sequential form (copy, compute, copy on one
-    # stream) is reported beside it.
-    e2e = None
-    if not args.no_e2e:
-        kv_names = ["k", "v", "cu_k"] if paged is None else ["k_cache", "v_cache", "block_table", "seq_lens_k"]
-        kv_dev = [k, v, cu_k] if paged is None else [paged[n] for n in kv_names]
-        names = ["q", "cu_q"] + kv_names + (["seq_lens", "ranges"] if ranges is not None else []) + \
-            (["sinks"] if sinks is not None else [])
-        dev_in = [q, cu_q] + kv_dev + ([seq_lens, ranges] if ranges is not None else []) + \
-            ([sinks] if sinks is not None else [])
-        host_in = [t.cpu().pin_memory() for t in dev_in]
-        h2d = sum(t.numel() * t.element_size() for t in host_in)
-        d2h = out.numel() * out.element_size()
-        sets = []
-        for b in range(2):
-            d = dict(zip(names, dev_in if b == 0 else [torch.empty_like(t) for t in dev_in]))
-            d["out"] = out if b == 0 else torch.empty_like(out)
-            d["table"] = table if (b == 0 or table is None) else torch.empty_like(table)
-            d["covered"] = covered if (b == 0 or covered is None) else torch.empty_like(covered)
-            d["host_out"] = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-            sets.append(d)
-
-        def compute(d, st):
-            kw2 = dict(kw, sinks=d.get("sinks"))
-            if args.scan:
-                mvp.attn_fwd_varlen_scan(d["q"], d["k"], d["v"], d["out"], d["cu_q"], d["cu_k"], max_q, max_k,
-                                         d.get("ranges"), num_decode_reqs=n_dec, stream=st, **kw2)
-                return
-            if ranges is not None:
-                mvp.fill_query_ranges(d["ranges"], d["cu_q"], d["seq_lens"], d["table"], num_tokens=w.total_q,
-                                      rows_written=d["covered"], stream=st)
-            if paged is not None:
-                mvp.attn_fwd_paged(d["q"], d["k_cache"], d["v_cache"], d["out"], d["cu_q"], d["seq_lens_k"],
-                                   d["block_table"], args.paged, max_q, max_k, range_table=d["table"],
-                                   range_covered=d["covered"], num_decode_reqs=n_dec, stream=st, **kw2)
-            else:
-                mvp.attn_fwd_varlen(d["q"], d["k"], d["v"], d["out"], d["cu_q"], d["cu_k"], max_q, max_k,
-                                    range_table=d["table"], range_covered=d["covered"], num_decode_reqs=n_dec,
-                                    stream=st, **kw2)
-
-        s_in, s_cmp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-        ev_in = [torch.cuda.Event() for _ in range(2)]
-        ev_done = [torch.cuda.Event() for _ in range(2)]
-        ev_out = [torch.cuda.Event() for _ in range(2)]
-
-        def pipelined(n_steps):
-            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            torch.cuda.synchronize()
-            t0.record(s_in)
-            for i in range(n_steps):
-                b = i % 2
-                d = sets[b]
-                if i >= 2:
-                    s_in.wait_event(ev_done[b])  # step i - 2 no longer reads these inputs
-                with torch.cuda.stream(s_in):
-                    for n, h in zip(names, host_in):
-                        d[n].copy_(h, non_blocking=True)
-                    ev_in[b].record(s_in)
-                s_cmp.wait_event(ev_in[b])
-                if i >= 2:
-                    s_cmp.wait_event(ev_out[b])  # step i - 2's output has left this buffer
-                with torch.cuda.stream(s_cmp):
-                    compute(d, s_cmp)
-                    ev_done[b].record(s_cmp)
-                s_out.wait_event(ev_done[b])
-                with torch.cuda.stream(s_out):
-                    d["host_out"].copy_(d["out"], non_blocking=True)
-                    ev_out[b].record(s_out)
-            t1.record(s_out)
-            s_in.wait_event(ev_out[(n_steps - 1) % 2])
-            torch.cuda.synchronize()
-            return t0.elapsed_time(t1) / 1e3
-
-        def sequential(n_steps):
-            d = sets[0]
-            ts = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_steps)]
-            for a, z in ts:
-                a.record(stream)
-                for n, h in zip(names, host_in):
-                    d[n].copy_(h, non_blocking=True)
-                compute(d, stream)
-                d["host_out"].copy_(d["out"], non_blocking=True)
-                z.record(stream)
-            torch.cuda.synchronize()
-            return sum(a.elapsed_time(z) for a, z in ts) / 1e3
-
-        pipelined(3)
-        sequential(2)
-        barrier(world)
-        e2e_s = reduce_max(pipelined(args.e2e_steps), world)
-        seq_s = reduce_max(sequential(args.e2e_steps), world)
-        if mvp.get_last_device_error() != 0:
-            raise RuntimeError("device timeout during the e2e steps")
-        e2e = {"value": aggregate(flops * args.e2e_steps * world, e2e_s), "unit": "TFLOP/s",
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": args.e2e_steps,
-               "ms_per_step": 1e3 * e2e_s / args.e2e_steps,
-               "timing": "pinned host inputs -> device, fill + attention, output -> pinned host, every step; "
-                         "steps pipelined over two buffer sets and three streams",
-               "sequential": {"value": aggregate(flops * args.e2e_steps * world, seq_s), "unit": "TFLOP/s",
-                              "ms_per_step": 1e3 * seq_s / args.e2e_steps}}
+    e2e = None if args.no_e2e else e2e_measure(args, bt, flops, stream, world)
 
     # ------------------------------------------------------------- graph replays
     graph = None
     if args.graph is not None:
-        graph = graph_measure(args, w, q, k, v, sinks, flops, flush, stream, dev)
+        graph = graph_measure(args, w, bt.q, bt.k, bt.v, bt.sinks, flops, flush, stream, dev)
 
     # ------------------------------------------------------------- CPU baseline
     cpu_baseline = None
@@ -781,12 +961,28 @@ def run_gpu(args, world, rank, local):
                                   f"the {args.workload} workload, float64 dense oracle, {cpu_s:.1f} core-seconds "
                                   f"over {cores} single-threaded workers"}
 
+    # ------------------------------------------------------------- the other configs
+    configs = None
+    plain = not (args.scaled or args.paged or args.scan or args.graph is not None)
+    if rank == 0 and plain and not args.no_configs:
+        bt.release()
+        del bt
+        torch.cuda.empty_cache()
+        reps = max(5, args.steps // 2)
+        configs = {}
+        for name in workloads.WORKLOADS:
+            if name != args.workload:
+                configs[name] = measure_config(name, dev, peaks, flush, stream, reps)
+        configs["fill_stress"] = measure_fill_stress(dev, peaks, flush, stream, reps)
+    barrier(world)
+
     if rank == 0:
-        desc = WORKLOAD_DESC if (args.workload == WORKLOAD and not args.scaled) else w.name
+        desc = WORKLOAD_DESCS.get(args.workload, args.workload) if not args.scaled else w.name
         line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-                "config": {"workload": desc, "global_batch": w.num_reqs * world, "seq_len": max_q,
+                "config": {"workload": desc, "config_number": CONFIG_NUMBER.get(args.workload),
+                           "global_batch": w.num_reqs * world, "seq_len": max(w.q_lens),
                            "kv_layout": (f"paged, {args.paged}-token blocks in a seeded random order"
                                          if args.paged else "packed"),
                            "ranges": ("scan mode: per-request range lists scanned in the kernels, no fill"
@@ -797,6 +993,10 @@ def run_gpu(args, world, rank, local):
                 "visible_entries_per_step": visible, "sub_batches": sub,
                 "roofline": roofline, "cpu_baseline": cpu_baseline, "e2e": e2e, "accounting": accounting,
                 "gpu_launches": launches, "clocks": sampler.summary()}
+        if mixed is not None:
+            line["mixed_roofline"] = mixed
+        if configs is not None:
+            line["configs"] = configs
         if graph is not None:
             line["graph"] = graph
         print(json.dumps(line))
@@ -814,11 +1014,13 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=WORKLOAD,
-                    help="workload name (default: the headline mm_prefix sliding layer)")
+                    help="workload name (default: the headline chunked-prefill workload)")
     ap.add_argument("--e2e-steps", type=int, default=10)
-    ap.add_argument("--cpu-rows-per-req", type=int, default=768)
+    ap.add_argument("--cpu-rows-per-req", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="do not measure the other workloads of the set (the 'configs' object)")
     ap.add_argument("--scan", action="store_true",
                     help="scan mode: pass the per-request range lists to the attention call instead of filling "
                          "the per-row table (mvp_attn_fwd_varlen_scan)")

@@ -199,6 +199,24 @@ WORKLOADS = ["tiny_window_sinks", "mm_prefix_sliding", "global_causal_d512",
              "chunked_prefill_ranges", "mixed_serving_a", "mixed_serving_b"]
 
 
+def fill_stress_case(seed: int = 99, num_reqs: int = 4096, rows: int = 1024, num_ranges: int = 64):
+    """Range-fill stress input: ``num_reqs`` requests of ``rows`` query rows
+    after a context drawn from 0..2047, each with ``num_ranges`` closed ranges
+    of 8..39 tokens separated by 1..9 free tokens from a start in 0..199 (so
+    about half the rows hold a range).  Returns (ranges int32 [B, R, 2],
+    q_lens, seq_lens) as lists / arrays.  Input drawing only."""
+    rng = np.random.default_rng(seed)
+    seq = rows + rng.integers(0, 2048, size=num_reqs)
+    start0 = rng.integers(0, 200, size=num_reqs)
+    length = rng.integers(8, 40, size=(num_reqs, num_ranges))
+    gap = rng.integers(1, 10, size=(num_reqs, num_ranges))
+    step = length + gap
+    starts = start0[:, None] + np.concatenate([np.zeros((num_reqs, 1), np.int64), np.cumsum(step, axis=1)[:, :-1]],
+                                              axis=1)
+    ranges = np.stack([starts, starts + length - 1], axis=2).astype(np.int32)
+    return ranges, [rows] * num_reqs, [int(x) for x in seq]
+
+
 def to_paged(k, v, k_lens, block_size: int, seed: int = 0, spare_blocks: int = 3, table_fill: int = -1):
     """Lay packed keys/values out in a paged cache (input generation only).
 

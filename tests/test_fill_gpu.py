@@ -120,20 +120,10 @@ def test_capacity_error_writes_nothing():
 
 
 def test_stress_size():
-    rng = np.random.default_rng(99)
-    nb = 4096
-    q_lens = [1024] * nb
-    seq = [1024 + int(c) for c in rng.integers(0, 2048, size=nb)]
-    per_req = []
-    for b in range(nb):
-        cur = int(rng.integers(0, 200))
-        rl = []
-        for _ in range(64):
-            length = int(rng.integers(8, 40))
-            rl.append((cur, cur + length - 1))
-            cur += length + int(rng.integers(1, 10))
-        per_req.append(rl)
-    ranges = workloads.pad_ranges(per_req)
+    """The benchmark's stress size: 4096 requests x 1024 rows, 64 ranges each."""
+    rng = np.random.default_rng(7)
+    ranges, q_lens, seq = workloads.fill_stress_case()
+    nb = len(q_lens)
     got, written, qsl = gpu_fill(ranges, q_lens, seq)
     # bit-exact on a sample of requests (the oracle is slow at this size)
     for b in rng.choice(nb, size=40, replace=False):
