@@ -921,7 +921,7 @@ def run_gpu(args, world, rank, local):
     # ------------------------------------------------------------- roofline
     peak_t = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     peak_b = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-    sub_reps = max(3, args.steps // 4)
+    sub_reps = max(10, args.steps // 2)
     sub, dec_s, pre_s, dec_bytes, pre_flops = sub_batches(bt, counts, acct, peaks, flush, stream, sub_reps)
     kernel_dir = os.path.join(ROOT, "masked_varlen_prefill_gb300", "csrc")
     if pre_s >= dec_s:
@@ -969,11 +969,13 @@ def run_gpu(args, world, rank, local):
         del bt
         torch.cuda.empty_cache()
         reps = max(5, args.steps // 2)
+        wanted = set(args.configs.split(",")) if args.configs else None
         configs = {}
         for name in workloads.WORKLOADS:
-            if name != args.workload:
+            if name != args.workload and (wanted is None or name in wanted):
                 configs[name] = measure_config(name, dev, peaks, flush, stream, reps)
-        configs["fill_stress"] = measure_fill_stress(dev, peaks, flush, stream, reps)
+        if wanted is None or "fill_stress" in wanted:
+            configs["fill_stress"] = measure_fill_stress(dev, peaks, flush, stream, reps)
     barrier(world)
 
     if rank == 0:
@@ -1021,6 +1023,9 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-configs", action="store_true",
                     help="do not measure the other workloads of the set (the 'configs' object)")
+    ap.add_argument("--configs", default=None, metavar="NAMES",
+                    help="comma-separated subset of the other workloads (and 'fill_stress') to measure in the "
+                         "'configs' object (default: all)")
     ap.add_argument("--scan", action="store_true",
                     help="scan mode: pass the per-request range lists to the attention call instead of filling "
                          "the per-row table (mvp_attn_fwd_varlen_scan)")
