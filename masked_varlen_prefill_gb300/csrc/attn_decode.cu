@@ -9,7 +9,7 @@
 // This path is HBM-bound (each key is 2 * D bf16 of K and V used by G query
 // heads), so it is SIMT, not tensor-core work:
 // * A CTA handles one (request, KV head, key split).  A producer warp streams
-//   KT-key tiles of K and V into a 3-stage shared-memory ring with TMA; four
+//   KT-key tiles of K and V into a 2- or 3-stage shared-memory ring with TMA; four
 //   compute warps read them back conflict-free (lane l owns D/32 consecutive
 //   dimensions of every key row).
 // * A warp takes KG = 32 / G keys at a time: each lane forms partial dot
@@ -31,10 +31,17 @@ namespace {
 
 constexpr int kNW = 4;                      // compute warps
 constexpr int kThreads = (kNW + 1) * 32;    // + producer warp
-constexpr int kStages = 3;
+constexpr int kMaxStages = 3;
 constexpr unsigned kFull = 0xffffffffu;
 
 __host__ __device__ constexpr int kt_for(int d) { return d == 64 ? 128 : (d == 128 ? 64 : 32); }
+// Stages of the K/V ring.  D = 128: two, so that three CTAs (12 compute warps)
+// fit an SM's shared memory; with three stages (two CTAs per SM) the decode
+// rows of the mixed serving batches ran at 87 / 82 % of the measured HBM
+// bandwidth against 98 / 90 % with two.  The other head dims keep three: their
+// CTAs are limited by registers, so fewer stages would only shrink the bytes
+// in flight.
+__host__ __device__ constexpr int stages_for(int d) { return d == 128 ? 2 : 3; }
 __host__ __device__ constexpr int box_for(int d) { return d > 256 ? 256 : d; }
 
 template <int D>
@@ -44,12 +51,13 @@ struct DCfg {
   static constexpr int BOX = box_for(D);
   static constexpr int NBOX = D / BOX;
   static constexpr int TILE = KT * D * 2;     // bytes of one K (or V) tile
-  static constexpr int SMEM = kStages * 2 * TILE + 1024;
+  static constexpr int STAGES = stages_for(D);
+  static constexpr int SMEM = STAGES * 2 * TILE + 1024;
 };
 
 struct __align__(8) DBarriers {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
   WaitCtl wc;  // abort flag and wait budget of this CTA
 };
 
@@ -149,7 +157,7 @@ __global__ void __launch_bounds__(kThreads)
   if (n_keys == 0 && sp > 0) return;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&sb.full[s], 1);
       mbar_init(&sb.empty[s], kNW);
     }
@@ -168,9 +176,9 @@ __global__ void __launch_bounds__(kThreads)
       int issued = 0;
       bool ok = true;
       for (int t = 0; t < n_tiles; ++t) {
-        const int s = t % kStages;
-        if (t >= kStages &&
-            !mbar_wait(&sb.empty[s], ((t / kStages) - 1) & 1, &sb.wc, p.err, kDevTimeoutLoad)) {
+        const int s = t % C::STAGES;
+        if (t >= C::STAGES &&
+            !mbar_wait(&sb.empty[s], ((t / C::STAGES) - 1) & 1, &sb.wc, p.err, kDevTimeoutLoad)) {
           ok = false;
           break;
         }
@@ -190,9 +198,9 @@ __global__ void __launch_bounds__(kThreads)
       }
       if (!ok) sb.wc.abort = 1;
       WaitCtl own_flag = own_wait_ctl(&sb.wc);
-      for (int s = 0; s < kStages && s < issued; ++s) {
-        const int last = ((issued - 1 - s) / kStages) * kStages + s;
-        mbar_wait(&sb.full[s], (last / kStages) & 1, &own_flag, nullptr, 0);
+      for (int s = 0; s < C::STAGES && s < issued; ++s) {
+        const int last = ((issued - 1 - s) / C::STAGES) * C::STAGES + s;
+        mbar_wait(&sb.full[s], (last / C::STAGES) & 1, &own_flag, nullptr, 0);
       }
     }
     return;
@@ -233,8 +241,8 @@ __global__ void __launch_bounds__(kThreads)
 
   bool ok = true;
   for (int t = 0; t < n_tiles && ok; ++t) {
-    const int s = t % kStages;
-    if (!mbar_wait(&sb.full[s], (t / kStages) & 1, &sb.wc, p.err, kDevTimeoutLoad)) {
+    const int s = t % C::STAGES;
+    if (!mbar_wait(&sb.full[s], (t / C::STAGES) & 1, &sb.wc, p.err, kDevTimeoutLoad)) {
       ok = false;
       break;
     }
