@@ -30,9 +30,12 @@
  *     there and unwind instead of hanging (so does a prefill kernel whose
  *     workspace queue another launch took over); mvp_get_last_device_error()
  *     reads and clears it.
- *   - Per-device state (that address, the SM count, kernel attributes) is
- *     looked up once per process and device; a cudaDeviceReset() invalidates
- *     it, so the library must not be used on a device after a reset.
+ *   - Per-device state (that address, the SM count, kernel attributes, a
+ *     second stream and two events for mixed batches) is set up on the first
+ *     attention call on a device -- make that call before any stream
+ *     capture -- and kept for the life of the process; a cudaDeviceReset()
+ *     invalidates it, so the library must not be used on a device after a
+ *     reset.
  */
 #ifndef MVP_H_
 #define MVP_H_
@@ -150,11 +153,15 @@ size_t mvp_attn_workspace_size(int num_reqs, int num_heads_q, int head_dim, int 
  *                 size the grid; rows beyond them are not computed).
  * num_decode_reqs -1: the batch may mix single-token (decode) requests and
  *                 longer ones anywhere; both kernels cover every request and
- *                 each skips the other's.  k >= 0: the caller guarantees that
- *                 requests [0, k) are exactly those with q_len == 1 (the
- *                 decode-first order vLLM's scheduler uses); then the decode
- *                 kernel covers only [0, k), the prefill kernel only
- *                 [k, num_reqs), and a side with no requests is not launched.
+ *                 each skips the other's, one after the other.  k >= 0: the
+ *                 caller guarantees that requests [0, k) are exactly those
+ *                 with q_len == 1 (the decode-first order vLLM's scheduler
+ *                 uses); then the decode kernel covers only [0, k), the
+ *                 prefill kernel only [k, num_reqs), a side with no requests
+ *                 is not launched, and when both are the decode kernel runs
+ *                 beside the prefill kernel on a second stream of the
+ *                 library's (forked from and joined back to `stream`; see
+ *                 mixed_prefill_sms of mvp_attn_options).
  * head_dim       64, 128, 256 or 512.  num_heads_q % num_heads_kv == 0.
  * range_table    int32 [total_q, 2] from mvp_fill_query_ranges, or NULL.
  * range_covered  int32 device scalar (rows_written of the fill) or NULL; when
@@ -192,6 +199,21 @@ int mvp_attn_fwd_varlen(const void* q, const void* k, const void* v, void* out, 
  *                microseconds per key tile, but a wait can span a whole work
  *                item (its rows times its keys), so a budget below a few
  *                milliseconds risks reporting a timeout on a healthy call.
+ * mixed_prefill_sms
+ *                batches with both single-token (decode) rows and longer
+ *                rows, given in decode-first order (num_decode_reqs >= 1
+ *                and rows after them), run the decode kernel beside the
+ *                prefill kernel: the prefill kernel's persistent CTAs take
+ *                this many SMs (0: the library's choice, three quarters of
+ *                the SMs when the decode side's estimated work is at least a
+ *                third of the prefill side's, else the two kernels run in
+ *                turn; > 0: that many, rounded to CTA pairs and at most the
+ *                SM count - 2) and the decode kernel runs on a second stream
+ *                of the library's (one per device), forked from and joined
+ *                back to `stream` with events, so all the call's work is
+ *                still ordered before later work on `stream`, also inside a
+ *                CUDA graph capture.  -1: the two kernels run one after the
+ *                other on `stream`.
  * fault          MVP_FAULT_NONE for every real call.  MVP_FAULT_WITHHOLD_PROBS
  *                exists to test the timeout path: in every prefill CTA that
  *                gets work (rank 0 of each CTA pair) one softmax warp never
@@ -209,6 +231,7 @@ typedef struct {
   int variant;            /* mvp_variant */
   unsigned wait_limit_us; /* 0: default (1 s) */
   int fault;              /* mvp_fault */
+  int mixed_prefill_sms;  /* 0: estimate; > 0: SMs of the prefill kernel; -1: no overlap */
 } mvp_attn_options;
 
 /*

@@ -51,7 +51,8 @@ class AttnCounts(ctypes.Structure):
 class AttnOptions(ctypes.Structure):
     """``mvp_attn_options`` (include/mvp.h)."""
 
-    _fields_ = [("variant", ctypes.c_int), ("wait_limit_us", ctypes.c_uint), ("fault", ctypes.c_int)]
+    _fields_ = [("variant", ctypes.c_int), ("wait_limit_us", ctypes.c_uint), ("fault", ctypes.c_int),
+                ("mixed_prefill_sms", ctypes.c_int)]
 
 
 _SIGNATURES = {
@@ -165,13 +166,14 @@ def attn_fwd_varlen(q, k, v, out, cu_seqlens_q, cu_seqlens_k, max_q_len, max_k_l
                     context_lens=None, range_table=None, range_covered=None, causal=True, window_left=-1,
                     window_right=-1, sinks=None, sink_mode=SINK_NONE, scale=None, workspace=None,
                     num_decode_reqs=-1, stream=None, variant=VARIANT_DEFAULT, wait_limit_us=0,
-                    fault=FAULT_NONE):
+                    fault=FAULT_NONE, mixed_prefill_sms=0):
     """Masked varlen attention forward (see ``mvp_attn_fwd_varlen``).
 
     q [total_q, Hq, D], k/v [total_k, Hkv, D] bf16; out like q; lse fp32
     [Hq, total_q] or None; cu_seqlens int32 [B+1]; the rest as in the header.
-    ``variant`` / ``wait_limit_us`` / ``fault`` other than their defaults go
-    through ``mvp_attn_fwd_varlen_ext`` with those options.
+    ``variant`` / ``wait_limit_us`` / ``fault`` / ``mixed_prefill_sms`` other
+    than their defaults go through ``mvp_attn_fwd_varlen_ext`` with those
+    options.
     """
     lib = load_library()
     dev = q.device
@@ -199,10 +201,10 @@ def attn_fwd_varlen(q, k, v, out, cu_seqlens_q, cu_seqlens_k, max_q_len, max_k_l
             hq, hkv, d, _ptr(range_table), _ptr(range_covered), int(bool(causal)), int(window_left),
             int(window_right), _ptr(sinks), int(sink_mode), float(scale), _ptr(workspace), ws_bytes,
             _stream(stream, dev)]
-    if variant == VARIANT_DEFAULT and wait_limit_us == 0 and fault == FAULT_NONE:
+    if variant == VARIANT_DEFAULT and wait_limit_us == 0 and fault == FAULT_NONE and mixed_prefill_sms == 0:
         name, st = "mvp_attn_fwd_varlen", lib.mvp_attn_fwd_varlen(*args)
     else:
-        opts = AttnOptions(int(variant), int(wait_limit_us), int(fault))
+        opts = AttnOptions(int(variant), int(wait_limit_us), int(fault), int(mixed_prefill_sms))
         name, st = "mvp_attn_fwd_varlen_ext", lib.mvp_attn_fwd_varlen_ext(*args, ctypes.byref(opts))
     if st != MVP_OK:
         raise MvpError(name, st)

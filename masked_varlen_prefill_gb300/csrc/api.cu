@@ -4,7 +4,9 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <climits>
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -27,7 +29,20 @@ int g_num_sms[kMaxDevices] = {};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 thread_local int g_last_launches = 0;
 
-cudaError_t device_state(int** err_ptr, int* num_sms = nullptr) {
+// The second stream of a device on which the decode kernel of a mixed batch
+// runs beside the prefill kernel, and the events that fork it from and join
+// it back to the caller's stream.  Created with the rest of the per-device
+// state on the first attention call on the device and kept for the life of
+// the process.
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr;
+  cudaEvent_t join = nullptr;
+  std::mutex mutex;  // one fork / launch / join sequence at a time
+};
+SideStream g_side[kMaxDevices];
+
+cudaError_t device_state(int** err_ptr, int* num_sms = nullptr, SideStream** side = nullptr) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -53,8 +68,20 @@ cudaError_t device_state(int** err_ptr, int* num_sms = nullptr) {
     if (e != cudaSuccess) return e;
     g_num_sms[dev] = n > 0 ? n : 1;
   }
+  SideStream& ss = g_side[dev];
+  if (ss.stream == nullptr) {
+    cudaStream_t st = nullptr;
+    cudaEvent_t f = nullptr, j = nullptr;
+    if ((e = cudaEventCreateWithFlags(&f, cudaEventDisableTiming)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&j, cudaEventDisableTiming)) != cudaSuccess) return e;
+    if ((e = cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    ss.fork = f;
+    ss.join = j;
+    ss.stream = st;
+  }
   *err_ptr = g_err_ptr[dev];
   if (num_sms) *num_sms = g_num_sms[dev];
+  if (side) *side = &ss;
   return cudaSuccess;
 }
 
@@ -160,6 +187,43 @@ struct KVArgs {
   int max_blocks;
 };
 
+// SMs for the prefill kernel of a mixed batch while the decode kernel runs
+// beside it, or 0 to run the two one after the other.  Both kernels' rates
+// grow with the SMs they hold (the decode kernel reaches the HBM peak only on
+// nearly all of them), so side by side they mostly save tails: the decode
+// CTAs fill the SMs the prefill kernel's last round leaves idle and the
+// prefill CTAs overlap the decode kernel's last wave.  Measured on the mixed
+// serving batches (152 SMs): 96 to 144 SMs for the prefill kernel all gave
+// 1-3 % over running the kernels in turn, 112 the best; a share sized by the
+// two sides' work (about 40 SMs for the prefill kernel) was slower than in
+// turn.  So the prefill kernel keeps three quarters of the SMs, and only
+// when the decode side has enough work to fill the other quarter for the
+// prefill kernel's duration: its estimated time (K/V bytes at the HBM rate)
+// at least a third of the prefill side's (FLOPs at the tensor rate).  The
+// key counts are device data, so the estimates use an average key run per
+// request (total_k / num_reqs packed, max_k_len paged) capped by the window.
+constexpr double kDecodeBytesPerS = 6.0e12;
+constexpr double kPrefillFlopsPerS = 1.1e15;
+
+int mixed_prefill_sms(int num_sms, int total_q, int total_k, bool paged, int num_reqs, int decode_rows,
+                      int max_q_len, int max_k_len, int causal, int window_left, int window_right, int hq, int hkv) {
+  const double avg_k = paged ? static_cast<double>(max_k_len) : static_cast<double>(total_k) / num_reqs;
+  double span = avg_k;  // keys one row sees
+  if (causal) {
+    if (window_left >= 0) span = std::min(span, window_left + 1.0);
+  } else if (window_left >= 0 && window_right >= 0) {
+    span = std::min(span, window_left + window_right + 1.0);
+  }
+  const double pre_rows = std::max(0, total_q - decode_rows);
+  const double pre_span = causal && window_left < 0 ? std::max(1.0, avg_k - 0.5 * max_q_len) : span;
+  const double t_dec = 4.0 * hkv * decode_rows * span / kDecodeBytesPerS;    // per unit of head_dim
+  const double t_pre = 4.0 * hq * pre_rows * pre_span / kPrefillFlopsPerS;  // per unit of head_dim
+  if (t_dec * 3.0 < t_pre) return 0;
+  int sms = (3 * num_sms) / 4;
+  sms -= sms & 1;  // whole CTA pairs
+  return sms;
+}
+
 int attn_fwd_impl(const void* q, void* out, float* lse, const int32_t* cu_seqlens_q, const int32_t* context_lens,
                   int num_reqs, int total_q, int max_q_len, int max_k_len, int num_decode_reqs, int num_heads_q,
                   int num_heads_kv, int head_dim, const int32_t* range_table, const int32_t* range_covered,
@@ -204,7 +268,8 @@ int attn_fwd_impl(const void* q, void* out, float* lse, const int32_t* cu_seqlen
   auto box_rows = [&](int rows) { return paged ? (rows < (1 << kv.block_shift) ? rows : (1 << kv.block_shift)) : rows; };
   int* err = nullptr;
   int num_sms = 1;
-  if (device_state(&err, &num_sms) != cudaSuccess) return MVP_ERR_CUDA;
+  SideStream* side = nullptr;
+  if (device_state(&err, &num_sms, &side) != cudaSuccess) return MVP_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   MaskParams m;
@@ -248,11 +313,13 @@ int attn_fwd_impl(const void* q, void* out, float* lse, const int32_t* cu_seqlen
   const int decode_count = num_decode_reqs < 0 ? num_reqs : num_decode_reqs;
 
   // ------------------------------------------------------------ prefill rows
-  if (max_q_len > 1 && prefill_first < num_reqs) {
+  const bool run_prefill = max_q_len > 1 && prefill_first < num_reqs;
+  PrefillParams pp{};
+  CUtensorMap pmq, pmk, pmv;
+  if (run_prefill) {
     const PrefillShape shape = prefill_tile_shape(head_dim, d512_split);
     const int gpack = largest_pow2_divisor(group, 8);
     const int bmp = 128 / gpack;
-    PrefillParams pp;
     pp.m = m;
     pp.out = out;
     pp.lse = lse;
@@ -275,19 +342,17 @@ int attn_fwd_impl(const void* q, void* out, float* lse, const int32_t* cu_seqlen
     // slower (mixed batch with a 4096 window: 51 vs 53 % of peak), so it is
     // used only without a window shorter than the longest key run.
     pp.queue = (window_left < 0 || window_left >= max_k_len) ? queue : nullptr;
-
-    CUtensorMap mq, mk, mv;
-    if (!encode_3d(&mq, q, head_dim, num_heads_q, total_q, 64, gpack, bmp, true) ||
-        !encode_3d(&mk, k, head_dim, num_heads_kv, total_k, 64, 1, box_rows(shape.k_box_keys), true) ||
-        !encode_3d(&mv, v, head_dim, num_heads_kv, total_k, 64, 1, box_rows(shape.v_box_keys), true))
+    if (!encode_3d(&pmq, q, head_dim, num_heads_q, total_q, 64, gpack, bmp, true) ||
+        !encode_3d(&pmk, k, head_dim, num_heads_kv, total_k, 64, 1, box_rows(shape.k_box_keys), true) ||
+        !encode_3d(&pmv, v, head_dim, num_heads_kv, total_k, 64, 1, box_rows(shape.v_box_keys), true))
       return MVP_ERR_UNSUPPORTED;
-    if (launch_prefill(head_dim, d512_split, pp, mq, mk, mv, st) != cudaSuccess) return MVP_ERR_CUDA;
-    ++launches;
   }
 
   // ------------------------------------------------------------ decode rows
-  if (decode_count > 0) {
-    DecodeParams dp;
+  const bool run_decode = decode_count > 0;
+  DecodeParams dp{};
+  CUtensorMap dmk, dmv;
+  if (run_decode) {
     dp.m = m;
     dp.q = q;
     dp.out = out;
@@ -319,12 +384,47 @@ int attn_fwd_impl(const void* q, void* out, float* lse, const int32_t* cu_seqlen
     dp.partial = splits > 1 ? static_cast<float*>(partials) : nullptr;
     const int per_cta = decode_heads_per_cta(head_dim, group);
     if (static_cast<long long>(num_heads_kv) * ((group + per_cta - 1) / per_cta) > 65535) return MVP_ERR_UNSUPPORTED;
-    CUtensorMap mk, mv;
     const int box = decode_box_inner(head_dim);
-    if (!encode_3d(&mk, k, head_dim, num_heads_kv, total_k, box, 1, box_rows(kt), false) ||
-        !encode_3d(&mv, v, head_dim, num_heads_kv, total_k, box, 1, box_rows(kt), false))
+    if (!encode_3d(&dmk, k, head_dim, num_heads_kv, total_k, box, 1, box_rows(kt), false) ||
+        !encode_3d(&dmv, v, head_dim, num_heads_kv, total_k, box, 1, box_rows(kt), false))
       return MVP_ERR_UNSUPPORTED;
-    if (launch_decode(head_dim, dp, mk, mv, st, &launches) != cudaSuccess) return MVP_ERR_CUDA;
+  }
+
+  // ------------------------------------------------------------ launches
+  // Both kernels: the decode kernel (HBM-bound) may run beside the prefill
+  // kernel (tensor-bound) instead of after it.  The prefill kernel's
+  // persistent CTAs then take a share of the SMs (mixed_prefill_sms) and the
+  // decode kernel goes to the device's side stream, forked from and joined
+  // back to the caller's stream with events (capturable in a CUDA graph).
+  // The decode-first order (num_decode_reqs >= 0) is required: it tells how
+  // many rows each side has.
+  const int share = (opts != nullptr) ? opts->mixed_prefill_sms : 0;
+  bool concurrent = run_prefill && run_decode && num_decode_reqs >= 0 && share >= 0 && num_sms >= 4;
+  int sms = 0;
+  if (concurrent) {
+    sms = share > 0 ? share
+                    : mixed_prefill_sms(num_sms, total_q, total_k, paged, num_reqs, decode_count, max_q_len,
+                                        max_k_len, causal, window_left, window_right, num_heads_q, num_heads_kv);
+    if (sms == 0) concurrent = false;               // too little decode work to overlap
+    if (sms > num_sms - 2) sms = num_sms - 2;       // leave the decode kernel at least two SMs
+    if (sms < 2) sms = 2;
+  }
+  if (!concurrent) {
+    if (run_prefill) {
+      if (launch_prefill(head_dim, d512_split, pp, pmq, pmk, pmv, st) != cudaSuccess) return MVP_ERR_CUDA;
+      ++launches;
+    }
+    if (run_decode && launch_decode(head_dim, dp, dmk, dmv, st, &launches) != cudaSuccess) return MVP_ERR_CUDA;
+  } else {
+    pp.n_ctas = sms;
+    std::lock_guard<std::mutex> lock(side->mutex);  // one fork / join at a time per device
+    if (cudaEventRecord(side->fork, st) != cudaSuccess || cudaStreamWaitEvent(side->stream, side->fork, 0) != cudaSuccess)
+      return MVP_ERR_CUDA;
+    if (launch_prefill(head_dim, d512_split, pp, pmq, pmk, pmv, st) != cudaSuccess) return MVP_ERR_CUDA;
+    ++launches;
+    if (launch_decode(head_dim, dp, dmk, dmv, side->stream, &launches) != cudaSuccess) return MVP_ERR_CUDA;
+    if (cudaEventRecord(side->join, side->stream) != cudaSuccess || cudaStreamWaitEvent(st, side->join, 0) != cudaSuccess)
+      return MVP_ERR_CUDA;
   }
   g_last_launches = launches;
   return MVP_OK;
