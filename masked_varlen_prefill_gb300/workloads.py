@@ -192,8 +192,27 @@ def workload(name: str) -> Workload:
         k_lens = [c + 1 for c in dec_ctx] + [c + 1024 for c in pre_ctx]
         wl = -1 if name.endswith("a") else 4095
         return Workload(name, 4, q_lens, k_lens, 32, 8, 128, True, wl, 0, SINK_NULL_LOGIT, None)
+    if name == "decode_profile":
+        # profiler-sized slice of the mixed serving batch: its first 32 decode
+        # rows (same context draw), 4096-token window, ~0.5 GB of K/V
+        rng = np.random.default_rng(4)
+        dec_ctx = [int(c) for c in rng.integers(1024, 32769, size=256)][:32]
+        return Workload(name, 4, [1] * 32, [c + 1 for c in dec_ctx], 32, 8, 128, True, 4095, 0, SINK_NULL_LOGIT,
+                        None)
+    if name == "prefill_d128_profile":
+        # profiler-sized slice of the mixed serving batch: its 4 prefill chunks
+        # of 1024 tokens (same context draw), 4096-token window
+        rng = np.random.default_rng(4)
+        rng.integers(1024, 32769, size=256)
+        pre_ctx = [int(c) for c in rng.integers(0, 16385, size=4)]
+        return Workload(name, 4, [1024] * 4, [c + 1024 for c in pre_ctx], 32, 8, 128, True, 4095, 0,
+                        SINK_NULL_LOGIT, None)
     raise KeyError(name)
 
+
+# Small slices of the mixed serving batch for profiler captures (a few hundred
+# MB on the device); not part of the benchmark set.
+PROFILE_WORKLOADS = ["decode_profile", "prefill_d128_profile"]
 
 WORKLOADS = ["tiny_window_sinks", "mm_prefix_sliding", "global_causal_d512",
              "chunked_prefill_ranges", "mixed_serving_a", "mixed_serving_b"]

@@ -30,14 +30,14 @@ pytestmark = pytest.mark.gpu
 HEADER = 256
 
 
-def _call(w, q, k, v, sinks, table, covered, ws, max_q=None, out=None, lse=None, cu=None):
+def _call(w, q, k, v, sinks, table, covered, ws, max_q=None, out=None, lse=None, cu=None, variant=0):
     cu_q, cu_k = gh.device_meta(w, q.device) if cu is None else cu
     out = torch.full_like(q, float("nan")) if out is None else out
     lse = torch.full((w.num_heads_q, w.total_q), float("nan"), device=q.device) if lse is None else lse
     mvp.attn_fwd_varlen(q, k, v, out, cu_q, cu_k, max_q or max(max(w.q_lens), 1), max(max(w.k_lens), 1), lse=lse,
                         range_table=table, range_covered=covered, causal=w.causal, window_left=w.window_left,
                         window_right=w.window_right, sinks=sinks, sink_mode=w.sink_mode, scale=w.scale,
-                        workspace=ws)
+                        workspace=ws, variant=variant)
     return out, lse
 
 
@@ -47,15 +47,15 @@ def _check_equal(a, b, what):
         f"{what}: lse differs from static"
 
 
-def _static_and_queue(w, ws_fill=None, max_q=None, repeats=1):
+def _static_and_queue(w, ws_fill=None, max_q=None, repeats=1, variant=0):
     q, k, v, sinks = gh.make_inputs(w)
     _, _, table, covered = gh.run_gpu(w, q, k, v, sinks, use_workspace=False)
-    ref = _call(w, q, k, v, sinks, table, covered, None, max_q=max_q)
+    ref = _call(w, q, k, v, sinks, table, covered, None, max_q=max_q, variant=variant)
     ws = torch.empty(HEADER, dtype=torch.uint8, device=q.device)
     if ws_fill is not None:
         ws.view(torch.int64)[:] = ws_fill
     for r in range(repeats):
-        got = _call(w, q, k, v, sinks, table, covered, ws, max_q=max_q)
+        got = _call(w, q, k, v, sinks, table, covered, ws, max_q=max_q, variant=variant)
         torch.cuda.synchronize()
         assert mvp.get_last_device_error() == 0
         _check_equal(got, ref, f"{w.name} call {r}")
@@ -124,9 +124,8 @@ def test_mostly_empty_item_space():
     _static_and_queue(w, max_q=8192, repeats=2)
 
 
-def test_head_split_cluster(monkeypatch):
-    monkeypatch.setenv("MVP_D512_HEAD_SPLIT", "1")
-    _static_and_queue(workloads.workload("global_causal_d512"), repeats=2)
+def test_head_split_cluster():
+    _static_and_queue(workloads.workload("global_causal_d512"), repeats=2, variant=mvp.VARIANT_D512_HEAD_SPLIT)
 
 
 def test_paged():
