@@ -62,7 +62,7 @@ constexpr int kBM = 128;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr unsigned kFullMask = 0xffffffffu;
 
-template <int D_, int DV_, int BN_, int KST_, int VST_, int NCTA_, int SPLITD_ = 0>
+template <int D_, int DV_, int BN_, int KST_, int VST_, int NCTA_, int SPLITD_ = 0, int NS_ = 2>
 struct Cfg {
   static constexpr int D = D_;
   static constexpr int DV = DV_;        // value columns handled by one item
@@ -135,10 +135,17 @@ struct Cfg {
   }
   static constexpr int IDS_CAP = ids_cap(2048);
   static constexpr int SMEM_BYTES = IDS_OFF + 2 * IDS_CAP * 4 + 1024;  // + alignment slack
+  // S buffers in TMEM.  The MMA issuer runs QK NS - 1 tiles ahead of PV:
+  // with two, S_{j+2} can only be computed once P_j (every softmax warp's)
+  // has been handed over and PV_j issued; with three (D = 128, where TMEM
+  // has room: 3 x 128 columns of S next to 128 of O), S_{j+2} is computed
+  // while the softmax warps still work on tile j.
+  static constexpr int NS = NS_;
   static constexpr int S_COL = 0;
-  static constexpr int O_COL = 2 * BN;
+  static constexpr int O_COL = NS * BN;
   static constexpr int TMEM_COLS = 512;
   static_assert(O_COL + OC <= TMEM_COLS, "TMEM budget");
+  static_assert(NS == 2 || NS == 3, "S buffers");
   static_assert(SMEM_BYTES <= 227 * 1024, "smem budget");
   static_assert(BN == 64 || BN == 128, "BN");
   static_assert(DV % 64 == 0 && OC <= 256 && DVC % 64 == 0, "DV");
@@ -152,6 +159,8 @@ struct Cfg {
   // The single MMA-issuing thread then commits twice per tile instead of
   // four or five times (its issue rate bounds the tensor pipe).
   static constexpr bool MERGED_RELEASE = KST == 2 && VST == 2;
+  static_assert(!MERGED_RELEASE || NS == 2, "merged release reads stage frees off the two S buffers");
+  static_assert(!SPLITD || NS == 2, "head-dim split: two S buffers");
 };
 
 // One work item: NCTA 128-row query tiles of one request and one KV head
@@ -198,8 +207,8 @@ struct __align__(8) Barriers {
   uint64_t k_empty[4];
   uint64_t v_full[4];
   uint64_t v_empty[4];
-  uint64_t s_full[2];
-  uint64_t p_full[2];
+  uint64_t s_full[3];  // tile t: buffer t % NS
+  uint64_t p_full[3];
   uint64_t o_done[2];
   uint64_t final_mma;
   uint64_t epi_full[2];   // an item's (1 / l, LSE) rows are written (half-0 softmax warps)
@@ -446,11 +455,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       mbar_init(&sb.v_full[i], 1);
       mbar_init(&sb.v_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::NS; ++i) {
       mbar_init(&sb.s_full[i], 1);
       mbar_init(&sb.p_full[i], 4 * C::SPLIT * C::MMA_CTAS);  // one arrival per softmax warp
-      mbar_init(&sb.o_done[i], 1);
     }
+    for (int i = 0; i < 2; ++i) mbar_init(&sb.o_done[i], 1);
     mbar_init(&sb.final_mma, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sb.epi_full[i], 4);
@@ -746,7 +755,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       // The whole warp runs this loop (converged, warp-uniform values); each
       // tcgen05.mma and commit is issued by one elected lane.  Descriptors are
       // computed once and each MMA only adds a compile-time offset.  Tile t is
-      // the CTA-wide tile index: S buffer t & 1, K stage t % KST, V stage
+      // the CTA-wide tile index: S buffer t % NS, K stage t % KST, V stage
       // t % VST.  In a pair, the same descriptors and TMEM addresses name the
       // operands in both CTAs.
       constexpr uint32_t idesc_qk = idesc_bf16_f32(C::ITEM_ROWS, C::BN, false, false);
@@ -764,7 +773,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (pl.n_tiles == 0) continue;
         ok = mbar_wait_spin(&sb.q_full, qn & 1, &sb.wc, p.err, kDevTimeoutLoad);
         ++qn;
-        for (int j = 0; ok && j <= pl.n_tiles; ++j) {
+        // Step j issues S_j = Q K_j^T, then O += P V of tile j - LEAD.
+        constexpr int LEAD = C::NS - 1;
+        for (int j = 0; ok && j < pl.n_tiles + LEAD; ++j) {
           if (j < pl.n_tiles) {
             const int t = T + j;
             const int s = t % C::KST;
@@ -772,7 +783,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
               ok = false;
               break;
             }
-            const uint32_t d = tmem + C::S_COL + (t & 1) * BN;
+            const uint32_t d = tmem + C::S_COL + (t % C::NS) * BN;
             const uint64_t dk = dk0 + static_cast<uint64_t>((s * C::K_BYTES) >> 4);
 #pragma unroll
             for (int c = 0; c < C::QCH; ++c) {
@@ -787,17 +798,17 @@ __global__ void __launch_bounds__(C::THREADS, 1)
               mma_commit_elect<C::MMA_CTAS>(&sb.k_empty[s]);
               if (j == pl.n_tiles - 1) mma_commit_elect<C::MMA_CTAS>(&sb.q_empty);  // Q free for the next item
             }
-            mma_commit_elect<C::MMA_CTAS>(&sb.s_full[t & 1]);
+            mma_commit_elect<C::MMA_CTAS>(&sb.s_full[t % C::NS]);
           }
-          if (j >= 1) {
-            const int t = T + j - 1;
-            if (!mbar_wait_spin(&sb.p_full[t & 1], (t >> 1) & 1, &sb.wc, p.err, kDevTimeoutSoftmax)) {
+          if (j >= LEAD) {
+            const int t = T + j - LEAD;
+            if (!mbar_wait_spin(&sb.p_full[t % C::NS], (t / C::NS) & 1, &sb.wc, p.err, kDevTimeoutSoftmax)) {
               ok = false;
               break;
             }
             // The item's first PV overwrites O: the epilogue warps must have
             // read the previous item's O out of TMEM (both CTAs of a pair).
-            if (j == 1 && qn > 1 &&
+            if (j == LEAD && qn > 1 &&
                 !mbar_wait_spin(&sb.o_free, (qn - 2) & 1, &sb.wc, p.err, kDevTimeoutSoftmax)) {
               ok = false;
               break;
@@ -808,9 +819,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
               break;
             }
             tc_fence_after();  // P (softmax warps) and the O read-out (epilogue warps) are ordered before
-            const uint32_t pcol = tmem + C::S_COL + (t & 1) * BN;
+            const uint32_t pcol = tmem + C::S_COL + (t % C::NS) * BN;
             const uint64_t dv = dv0 + static_cast<uint64_t>((s * C::V_BYTES) >> 4);
-            const uint32_t first = (j > 1) ? 1u : 0u;  // the item's first PV overwrites O
+            const uint32_t first = (j > LEAD) ? 1u : 0u;  // the item's first PV overwrites O
 #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk) {
               const uint64_t b = dv + static_cast<uint64_t>((kk * 16 * 128) >> 4);
@@ -1078,8 +1089,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const int j = C::SPLITD ? js - 1 : js;
         const int t = T + j;
         const int kb = pl.kb_lo + j;
-        const uint32_t scol = tmem + lane_base + C::S_COL + (t & 1) * BN;
-        if (!C::SPLITD && !mbar_wait(&sb.s_full[t & 1], (t >> 1) & 1, &sb.wc, p.err, kDevTimeoutMma)) {
+        const uint32_t scol = tmem + lane_base + C::S_COL + (t % C::NS) * BN;
+        if (!C::SPLITD && !mbar_wait(&sb.s_full[t % C::NS], (t / C::NS) & 1, &sb.wc, p.err, kDevTimeoutMma)) {
           ok = false;
           break;
         }
@@ -1220,8 +1231,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const bool withhold = p.m.fault == kFaultWithholdProbs && T == 0 && j == 0 &&
                               warp == C::SOFTMAX_BEGIN && (C::NCTA == 1 || cluster_rank() == 0);
         if (lane == 0 && !withhold) {
-          if constexpr (C::PAIR) mbar_arrive_cluster(p_full_addr0 + (t & 1) * 8);
-          else mbar_arrive(&sb.p_full[t & 1]);
+          if constexpr (C::PAIR) mbar_arrive_cluster(p_full_addr0 + (t % C::NS) * 8);
+          else mbar_arrive(&sb.p_full[t % C::NS]);
         }
         if (!ok) break;
       }
@@ -1363,7 +1374,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 }
 
 using Cfg64 = Cfg<64, 64, 128, 4, 4, 1>;
-using Cfg128 = Cfg<128, 128, 128, 4, 4, 2>;
+using Cfg128 = Cfg<128, 128, 128, 4, 4, 2, 0, 3>;
 using Cfg256 = Cfg<256, 256, 128, 2, 2, 2>;
 // D = 512: O of all 512 value columns does not fit TMEM next to S, so the
 // default splits the value dimension over two items (each recomputes S).  The
