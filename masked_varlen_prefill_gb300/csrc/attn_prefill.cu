@@ -141,6 +141,10 @@ struct Cfg {
   // has room: 3 x 128 columns of S next to 128 of O), S_{j+2} is computed
   // while the softmax warps still work on tile j.
   static constexpr int NS = NS_;
+  // S buffer of CTA-wide tile t (t >= 0) and the phase of its barriers; the
+  // unsigned forms keep NS = 2 at a mask and a shift.
+  static __device__ __forceinline__ uint32_t sbuf(int t) { return static_cast<uint32_t>(t) % NS; }
+  static __device__ __forceinline__ uint32_t sphase(int t) { return (static_cast<uint32_t>(t) / NS) & 1u; }
   static constexpr int S_COL = 0;
   static constexpr int O_COL = NS * BN;
   static constexpr int TMEM_COLS = 512;
@@ -783,7 +787,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
               ok = false;
               break;
             }
-            const uint32_t d = tmem + C::S_COL + (t % C::NS) * BN;
+            const uint32_t d = tmem + C::S_COL + C::sbuf(t) * BN;
             const uint64_t dk = dk0 + static_cast<uint64_t>((s * C::K_BYTES) >> 4);
 #pragma unroll
             for (int c = 0; c < C::QCH; ++c) {
@@ -798,11 +802,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
               mma_commit_elect<C::MMA_CTAS>(&sb.k_empty[s]);
               if (j == pl.n_tiles - 1) mma_commit_elect<C::MMA_CTAS>(&sb.q_empty);  // Q free for the next item
             }
-            mma_commit_elect<C::MMA_CTAS>(&sb.s_full[t % C::NS]);
+            mma_commit_elect<C::MMA_CTAS>(&sb.s_full[C::sbuf(t)]);
           }
           if (j >= LEAD) {
             const int t = T + j - LEAD;
-            if (!mbar_wait_spin(&sb.p_full[t % C::NS], (t / C::NS) & 1, &sb.wc, p.err, kDevTimeoutSoftmax)) {
+            if (!mbar_wait_spin(&sb.p_full[C::sbuf(t)], C::sphase(t), &sb.wc, p.err, kDevTimeoutSoftmax)) {
               ok = false;
               break;
             }
@@ -819,7 +823,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
               break;
             }
             tc_fence_after();  // P (softmax warps) and the O read-out (epilogue warps) are ordered before
-            const uint32_t pcol = tmem + C::S_COL + (t % C::NS) * BN;
+            const uint32_t pcol = tmem + C::S_COL + C::sbuf(t) * BN;
             const uint64_t dv = dv0 + static_cast<uint64_t>((s * C::V_BYTES) >> 4);
             const uint32_t first = (j > LEAD) ? 1u : 0u;  // the item's first PV overwrites O
 #pragma unroll
@@ -1089,8 +1093,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const int j = C::SPLITD ? js - 1 : js;
         const int t = T + j;
         const int kb = pl.kb_lo + j;
-        const uint32_t scol = tmem + lane_base + C::S_COL + (t % C::NS) * BN;
-        if (!C::SPLITD && !mbar_wait(&sb.s_full[t % C::NS], (t / C::NS) & 1, &sb.wc, p.err, kDevTimeoutMma)) {
+        const uint32_t scol = tmem + lane_base + C::S_COL + C::sbuf(t) * BN;
+        if (!C::SPLITD && !mbar_wait(&sb.s_full[C::sbuf(t)], C::sphase(t), &sb.wc, p.err, kDevTimeoutMma)) {
           ok = false;
           break;
         }
@@ -1231,8 +1235,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const bool withhold = p.m.fault == kFaultWithholdProbs && T == 0 && j == 0 &&
                               warp == C::SOFTMAX_BEGIN && (C::NCTA == 1 || cluster_rank() == 0);
         if (lane == 0 && !withhold) {
-          if constexpr (C::PAIR) mbar_arrive_cluster(p_full_addr0 + (t % C::NS) * 8);
-          else mbar_arrive(&sb.p_full[t % C::NS]);
+          if constexpr (C::PAIR) mbar_arrive_cluster(p_full_addr0 + C::sbuf(t) * 8);
+          else mbar_arrive(&sb.p_full[C::sbuf(t)]);
         }
         if (!ok) break;
       }
