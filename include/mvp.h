@@ -471,7 +471,9 @@ typedef struct {
   long long prefill_items;          /* work items with at least one key tile           */
   long long prefill_tiles;          /* key tiles visited, summed over items            */
   long long prefill_mma_instructions; /* tcgen05.mma issued: tiles x (D/16 + BN/16)   */
-  double prefill_mma_flops;         /* 2 M BN (D + DV) per tile (M = 128 x CTAs/MMA)   */
+  double prefill_mma_flops;         /* 2 M BN (D + DV) per tile (M = 128 x CTAs/MMA),
+                                       plus 2 M BN 32 per tile at D = 128 (row sums
+                                       carried by the PV MMA)                          */
   double prefill_compulsory_bytes;  /* q and out once, K and V of the visited tiles    */
                                     /* once (lse not included)                         */
   long long decode_keys_walked;     /* keys read per KV head (tiles start on multiples */

@@ -183,10 +183,11 @@ extern "C" int mvp_attn_accounting(const int32_t* cu_seqlens_q, const int32_t* s
   out->prefill_items = static_cast<long long>(items * heads_items);
   out->prefill_tiles = static_cast<long long>(tiles * heads_items);
   // per tile, each issuing CTA: qk_k / 16 QK MMAs (M x BN x 16) and BN / 16
-  // PV MMAs (M x oc x 16)
+  // PV MMAs (M x (oc + rowsum_n) x 16: where the tensor core sums the rows,
+  // the PV MMA carries rowsum_n more columns)
   out->prefill_mma_instructions = out->prefill_tiles * shape.issuers * (shape.qk_k / 16 + shape.bn / 16);
   out->prefill_mma_flops = static_cast<double>(out->prefill_tiles) * shape.issuers * 2.0 * shape.mma_m *
-                           static_cast<double>(bn) * (shape.qk_k + shape.oc);
+                           static_cast<double>(bn) * (shape.qk_k + shape.oc + shape.rowsum_n);
   out->prefill_compulsory_bytes = 2.0 * static_cast<double>(rows_pre) * hq * d * 2.0 +  // q in, out
                                   2.0 * static_cast<double>(touched_pre) * hkv * d * 2.0;  // k, v
   out->decode_keys_walked = keys_walked;

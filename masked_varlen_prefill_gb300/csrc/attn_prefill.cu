@@ -37,6 +37,10 @@
 // * TMEM (512 columns): S double buffer [0, BN) and [BN, 2 BN) in fp32; the
 //   bf16 probabilities P overwrite the first BN/2 columns of their S buffer and
 //   feed O += P V as the TMEM operand of tcgen05.mma; O at [2 BN, 2 BN + DV).
+//   At D = 128 the PV MMA also multiplies P by a block of ones that follows
+//   each V stage in shared memory, so that the row sums of P (what O is
+//   normalised by) accumulate in TMEM beside O instead of costing the softmax
+//   warps an unpack and an add per score pair.
 // * MMA order per step j: S_j = Q K_j^T, then O += P_{j-1} V_{j-1}, so the
 //   tensor core computes the next scores while the softmax warps work on the
 //   current ones.  MMA descriptors are computed once; loads are released per
@@ -62,7 +66,7 @@ constexpr int kBM = 128;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr unsigned kFullMask = 0xffffffffu;
 
-template <int D_, int DV_, int BN_, int KST_, int VST_, int NCTA_, int SPLITD_ = 0, int NS_ = 2>
+template <int D_, int DV_, int BN_, int KST_, int VST_, int NCTA_, int SPLITD_ = 0, int NS_ = 2, int ROWSUM_ = 0>
 struct Cfg {
   static constexpr int D = D_;
   static constexpr int DV = DV_;        // value columns handled by one item
@@ -112,11 +116,24 @@ struct Cfg {
                 "register split");
   static constexpr int Q_BYTES = kBM * DQ * 2;
   static constexpr int K_BYTES = KROWS * DQ * 2;  // per CTA
-  static constexpr int V_BYTES = BN * DVC * 2;    // per CTA
+  static constexpr int V_BYTES = BN * DVC * 2;    // per CTA, loaded per tile
   static constexpr int Q_OFF = 0;
   static constexpr int K_OFF = Q_BYTES;
   static constexpr int V_OFF = K_OFF + KST * K_BYTES;
-  static constexpr int TILE_BYTES = V_OFF + VST * V_BYTES;
+  // Row sums by the tensor core (ROWSUM): each V stage is followed by a
+  // constant 64-column block of bf16 ones, and the PV MMA takes ONES more
+  // columns of B from each CTA (its value columns, then ONES of the ones), so
+  // that the accumulator holds, after each CTA's part of O, ONES copies of
+  // every row's sum of the bf16 probabilities, accumulated and rescaled with
+  // O.  The softmax warps then add only the unrounded probabilities (for the
+  // LSE).  A V stage is VCH blocks of BN x 128 bytes (the loaded value
+  // columns) plus the ones block.
+  static constexpr bool ROWSUM = ROWSUM_ != 0;
+  static constexpr int ONES = ROWSUM ? 16 : 0;
+  static constexpr int V_STAGE = (VCH + (ROWSUM ? 1 : 0)) * BN * 128;  // stage stride
+  static constexpr int PART = DVC + ONES;                           // accumulator columns per CTA part
+  static constexpr int OCW = SPLITD ? OC : MMA_CTAS * PART;         // accumulator columns (PV N)
+  static constexpr int TILE_BYTES = V_OFF + VST * V_STAGE;
   // SPLITD: the peer's partial scores of two tiles, [2][128 rows][BN] fp32
   static constexpr int XS_OFF = TILE_BYTES;
   static constexpr int XS_BYTES = SPLITD ? 2 * kBM * BN * 4 : 0;
@@ -137,9 +154,11 @@ struct Cfg {
   static constexpr int SMEM_BYTES = IDS_OFF + 2 * IDS_CAP * 4 + 1024;  // + alignment slack
   // S buffers in TMEM.  The MMA issuer runs QK NS - 1 tiles ahead of PV:
   // with two, S_{j+2} can only be computed once P_j (every softmax warp's)
-  // has been handed over and PV_j issued; with three (D = 128, where TMEM
-  // has room: 3 x 128 columns of S next to 128 of O), S_{j+2} is computed
-  // while the softmax warps still work on tile j.
+  // has been handed over and PV_j issued; with three, S_{j+2} is computed
+  // while the softmax warps still work on tile j.  (Three fit next to O at
+  // D = 128 only, which gives those columns to the row sums instead: with
+  // the softmax warps' row-sum work gone, two buffers measured as fast as
+  // three.)
   static constexpr int NS = NS_;
   // S buffer of CTA-wide tile t (t >= 0) and the phase of its barriers; the
   // unsigned forms keep NS = 2 at a mask and a shift.
@@ -147,8 +166,14 @@ struct Cfg {
   static __device__ __forceinline__ uint32_t sphase(int t) { return (static_cast<uint32_t>(t) / NS) & 1u; }
   static constexpr int S_COL = 0;
   static constexpr int O_COL = NS * BN;
+  static constexpr int L_COL = O_COL + DVC;  // ROWSUM: the row sum (first ones column of part 0)
   static constexpr int TMEM_COLS = 512;
-  static_assert(O_COL + OC <= TMEM_COLS, "TMEM budget");
+  static_assert(O_COL + OCW <= TMEM_COLS, "TMEM budget");
+  // (each softmax half's O columns lie in one part; the ones block sits on a
+  // 64-column boundary of the stage, LBO = BN x 128 bytes away)
+  static_assert(!ROWSUM || (PAIR && HDV == DVC && DVC % 64 == 0 && OCW <= 256), "row sums in the PV MMA");
+  // Accumulator column of the item's value column `d` (0 .. OC - 1).
+  static __host__ __device__ constexpr int ocol(int d) { return (d / DVC) * PART + d % DVC; }
   static_assert(NS == 2 || NS == 3, "S buffers");
   static_assert(SMEM_BYTES <= 227 * 1024, "smem budget");
   static_assert(BN == 64 || BN == 128, "BN");
@@ -492,6 +517,15 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       tmem_relinquish();
     }
   }
+  if constexpr (C::ROWSUM) {
+    // the ones block after each V stage (bf16 1.0), made visible to the tensor core
+    constexpr int kWords = C::BN * 128 / 16;  // 16-byte words per block
+#pragma unroll 1
+    for (int i = threadIdx.x; i < C::VST * kWords; i += C::THREADS)
+      reinterpret_cast<uint4*>(smem + C::V_OFF + (i / kWords) * C::V_STAGE + C::VCH * C::BN * 128)[i % kWords] =
+          make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+    fence_proxy_async_smem();
+  }
   tc_fence_before();
   __syncthreads();
   if constexpr (C::NCTA == 2) cluster_sync_all();  // the peer's barriers are initialised
@@ -687,13 +721,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             const int vrow = row_of(e, buf, key0 + r);
 #pragma unroll
             for (int c = 0; c < C::VCH; ++c)
-              tma_load<C>(sV + s * C::V_BYTES + c * (BN * 128) + r * 128, &map_v, &sb.v_full[s],
+              tma_load<C>(sV + s * C::V_STAGE + c * (BN * 128) + r * 128, &map_v, &sb.v_full[s],
                           e.it.dv0 + rank * C::DVC + c * 64, e.it.hkv, vrow);
           }
         } else {
 #pragma unroll
           for (int c = 0; c < C::VCH; ++c)
-            tma_load<C>(sV + s * C::V_BYTES + c * (BN * 128), &map_v, &sb.v_full[s], e.it.dv0 + rank * C::DVC + c * 64,
+            tma_load<C>(sV + s * C::V_STAGE + c * (BN * 128), &map_v, &sb.v_full[s], e.it.dv0 + rank * C::DVC + c * 64,
                         e.it.hkv, e.it.k0 + key0);
         }
         ++vc;
@@ -763,7 +797,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       // t % VST.  In a pair, the same descriptors and TMEM addresses name the
       // operands in both CTAs.
       constexpr uint32_t idesc_qk = idesc_bf16_f32(C::ITEM_ROWS, C::BN, false, false);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(C::ITEM_ROWS, C::OC, false, true);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(C::ITEM_ROWS, C::OCW, false, true);
       const uint64_t dq = smem_desc_sw128(smem_u32(sQ), 16, 1024);
       const uint64_t dk0 = smem_desc_sw128(smem_u32(sK), 16, 1024);
       const uint64_t dv0 = smem_desc_sw128(smem_u32(sV), BN * 128, 1024);
@@ -824,7 +858,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             }
             tc_fence_after();  // P (softmax warps) and the O read-out (epilogue warps) are ordered before
             const uint32_t pcol = tmem + C::S_COL + C::sbuf(t) * BN;
-            const uint64_t dv = dv0 + static_cast<uint64_t>((s * C::V_BYTES) >> 4);
+            const uint64_t dv = dv0 + static_cast<uint64_t>((s * C::V_STAGE) >> 4);
             const uint32_t first = (j > LEAD) ? 1u : 0u;  // the item's first PV overwrites O
 #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk) {
@@ -1048,8 +1082,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       const float sink_raw = rc.sink / p.m.scale;            // units of the raw q.k score
       float m_ref = null_mode ? sink_l2 : -INFINITY;
       // Partial row sums of this thread's columns: the bf16-rounded
-      // probabilities (they normalise O, which the PV MMA builds from them)
-      // and the unrounded ones (they give the LSE).  The null logit counts once.
+      // probabilities (they normalise O, which the PV MMA builds from them;
+      // with ROWSUM the tensor core sums them and l_sum keeps only the null
+      // logit's share) and the unrounded ones (they give the LSE).  The null
+      // logit counts once.
       float l_sum = (null_mode && half == 0) ? 1.f : 0.f;
       float l_lse = l_sum;
 
@@ -1190,15 +1226,18 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           const float e0 = ex2_approx(t0);
           const float e1 = ex2_approx(t1);
           const uint32_t pk = pack_bf16x2(e0, e1);
-          acc_r[i & 3] = f2_add(acc_r[i & 3], f2_pack(__uint_as_float(pk << 16), __uint_as_float(pk & 0xffff0000u)));
+          if constexpr (!C::ROWSUM)  // (else the tensor core sums the rounded values)
+            acc_r[i & 3] = f2_add(acc_r[i & 3], f2_pack(__uint_as_float(pk << 16), __uint_as_float(pk & 0xffff0000u)));
           acc_e[i & 3] = f2_add(acc_e[i & 3], f2_pack(e0, e1));
           s[i] = pk;
         }
         {
           float a0, a1, b0, b1;
-          f2_unpack(f2_add(f2_add(acc_r[0], acc_r[1]), f2_add(acc_r[2], acc_r[3])), a0, a1);
+          if constexpr (!C::ROWSUM) {
+            f2_unpack(f2_add(f2_add(acc_r[0], acc_r[1]), f2_add(acc_r[2], acc_r[3])), a0, a1);
+            l_sum += a0 + a1;
+          }
           f2_unpack(f2_add(f2_add(acc_e[0], acc_e[1]), f2_add(acc_e[2], acc_e[3])), b0, b1);
-          l_sum += a0 + a1;
           l_lse += b0 + b1;
         }
         // P (bf16 pairs) over this half's scores.  Both halves have their
@@ -1215,7 +1254,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           if (!mbar_wait(&sb.o_done[tp & 1], (tp >> 1) & 1, &sb.wc, p.err, kDevTimeoutMma)) ok = false;
           if (ok) {
             tc_fence_after();
-            const uint32_t ocol = tmem + lane_base + C::O_COL + half * C::HDV;
+            const uint32_t ocol = tmem + lane_base + C::O_COL + C::ocol(half * C::HDV);
 #pragma unroll 1
             for (int c = 0; c < C::HDV / 32; ++c) {
               uint32_t o[32];
@@ -1224,6 +1263,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 #pragma unroll
               for (int u = 0; u < 32; ++u) o[u] = __float_as_uint(__uint_as_float(o[u]) * alpha);
               tmem_st_32x32b_x32(ocol + c * 32, o);
+            }
+            if constexpr (C::ROWSUM) {
+              if (half == 0) {  // the row sum (first of its equal columns) moves with O
+                const uint32_t lcol = tmem + lane_base + C::L_COL;
+                uint32_t lv = tmem_ld_32x32b_x1(lcol);
+                tmem_ld_wait1(lv);
+                tmem_st_32x32b_x1(lcol, __float_as_uint(__uint_as_float(lv) * alpha));
+              }
             }
           }
         }
@@ -1262,7 +1309,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             !mbar_wait(&sb.epi_empty[slot], ((hk / C::EPI_SLOTS) - 1) & 1, &sb.wc, p.err, kDevTimeoutStore))
           ok = false;
         const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-        const float inv_l = (l_sum > 0.f) ? 1.f / l_sum : 0.f;
+        // ROWSUM: the epilogue adds the tensor core's row sum to l_sum (then
+        // the null logit's share alone) and inverts it
+        const float inv_l = C::ROWSUM ? l_sum : ((l_sum > 0.f) ? 1.f / l_sum : 0.f);
         const float lse = (l_lse > 0.f) ? (m_use + lg2_approx(l_lse)) * 0.6931471805599453f : -INFINITY;
         rowinfo[slot * kBM + row] = make_float2(inv_l, lse);
         __syncwarp();
@@ -1307,6 +1356,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       if (lane == 0) mbar_arrive(&sb.epi_empty[slot]);
       ++hk;
       const bool has_tiles = e.pl.n_tiles > 0;
+      float inv_l = info.x;
       if (has_tiles) {
         const int tl = T + e.pl.n_tiles - 1;  // the item's last PV
         if (!mbar_wait(&sb.o_done[tl & 1], (tl >> 1) & 1, &sb.wc, p.err, kDevTimeoutMma)) {
@@ -1315,6 +1365,16 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
         tc_fence_after();
       }
+      if constexpr (C::ROWSUM) {
+        // the row's sum of bf16 probabilities (tensor core) + the null logit's share
+        float l = info.x;
+        if (has_tiles) {
+          uint32_t lv = tmem_ld_32x32b_x1(tmem + lane_base + C::L_COL);
+          tmem_ld_wait1(lv);
+          l += __uint_as_float(lv);
+        }
+        inv_l = (l > 0.f) ? 1.f / l : 0.f;
+      }
       __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.out) +
                             (static_cast<size_t>(e.it.q0 + qi) * p.hq + head) * C::D + e.it.dv0 + oc0;
       const uint32_t ocol = tmem + lane_base + C::O_COL;
@@ -1322,7 +1382,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       for (int c = 0; c < C::OC / 32; ++c) {
         uint32_t o[32];
         if (has_tiles) {
-          tmem_ld_32x32b_x32(ocol + c * 32, o);
+          tmem_ld_32x32b_x32(ocol + C::ocol(c * 32), o);
           tmem_ld_wait(o);
         } else {
 #pragma unroll
@@ -1341,7 +1401,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           uint32_t w[16];
 #pragma unroll
           for (int v = 0; v < 16; ++v)
-            w[v] = pack_bf16x2(__uint_as_float(o[2 * v]) * info.x, __uint_as_float(o[2 * v + 1]) * info.x);
+            w[v] = pack_bf16x2(__uint_as_float(o[2 * v]) * inv_l, __uint_as_float(o[2 * v + 1]) * inv_l);
           __nv_bfloat16* dst = orow + c * 32;
           if (out_v8) {
             st_global_v8(dst, w);
@@ -1378,7 +1438,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 }
 
 using Cfg64 = Cfg<64, 64, 128, 4, 4, 1>;
-using Cfg128 = Cfg<128, 128, 128, 4, 4, 2, 0, 3>;
+// D = 128: the softmax warps bound the tile, so the tensor core also sums
+// the rows (TMEM: 2 x 128 S + 160 accumulator columns; shared memory: two
+// K and two V stages, each V stage with its ones block).
+using Cfg128 = Cfg<128, 128, 128, 2, 2, 2, 0, 2, 1>;
 using Cfg256 = Cfg<256, 256, 128, 2, 2, 2>;
 // D = 512: O of all 512 value columns does not fit TMEM next to S, so the
 // default splits the value dimension over two items (each recomputes S).  The
@@ -1464,7 +1527,7 @@ cudaError_t launch_cfg(const PrefillParams& p, const CUtensorMap& mq, const CUte
 template <class C>
 PrefillShape shape_of() {
   return {C::BN, C::DV, C::DV_SPLIT, C::BN, C::KROWS, C::NCTA, C::ITEM_ROWS, C::SPLITD ? 2 : 1, C::DQ, C::OC,
-          C::ITEM_ROWS};
+          C::ITEM_ROWS, C::OCW - C::OC};
 }
 
 PrefillShape prefill_tile_shape(int head_dim, bool d512_head_split) {
@@ -1473,7 +1536,7 @@ PrefillShape prefill_tile_shape(int head_dim, bool d512_head_split) {
     case 128: return shape_of<Cfg128>();
     case 256: return shape_of<Cfg256>();
     case 512: return d512_head_split ? shape_of<Cfg512S>() : shape_of<Cfg512>();
-    default: return {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
+    default: return {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
   }
 }
 

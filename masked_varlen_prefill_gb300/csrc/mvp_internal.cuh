@@ -90,6 +90,7 @@ struct PrefillShape {
   int qk_k;        // head dims one issuing CTA multiplies in QK
   int oc;          // O columns one issuing CTA accumulates
   int mma_m;       // M of each MMA
+  int rowsum_n;    // PV MMA columns that sum the rows (P x ones), 0 when the softmax sums them
 };
 // d512_head_split selects the head-dim-split form of D = 512 (TMEM-resident
 // O, no recomputed QK) instead of the default value split.

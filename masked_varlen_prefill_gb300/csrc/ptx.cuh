@@ -291,6 +291,19 @@ __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_
 
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// One column: thread t of the warp reads / writes lane (taddr.lane + t).
+__device__ __forceinline__ uint32_t tmem_ld_32x32b_x1(uint32_t taddr) {
+  uint32_t r;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
+  return r;
+}
+__device__ __forceinline__ void tmem_ld_wait1(uint32_t& r) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(r) : : "memory");
+}
+__device__ __forceinline__ void tmem_st_32x32b_x1(uint32_t taddr, uint32_t r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(r) : "memory");
+}
+
 // ------------------------------------------------------------------ CTA pairs
 // A cluster of two CTAs shares each tcgen05.mma (.cta_group::2): the A rows
 // and the accumulator rows are split between the two CTAs (rank 0 holds rows

@@ -26,10 +26,11 @@ from oracle import range_table as ort
 # a CTA pair, M 256; D 512: a CTA pair, M 256, half the value columns per item);
 # keys per decode tile
 BN = {64: 128, 128: 128, 256: 128, 512: 64}
+# (D 128: the PV MMA also sums the rows, 2 x 16 more columns)
 INSTR_PER_TILE = {64: 64 // 16 + 128 // 16, 128: 128 // 16 + 128 // 16, 256: 256 // 16 + 128 // 16,
                   512: 512 // 16 + 64 // 16}
-FLOPS_PER_TILE = {64: 2 * 128 * 128 * (64 + 64), 128: 2 * 256 * 128 * (128 + 128), 256: 2 * 256 * 128 * (256 + 256),
-                  512: 2 * 256 * 64 * (512 + 256)}
+FLOPS_PER_TILE = {64: 2 * 128 * 128 * (64 + 64), 128: 2 * 256 * 128 * (128 + 128 + 32),
+                  256: 2 * 256 * 128 * (256 + 256), 512: 2 * 256 * 64 * (512 + 256)}
 # the opt-in D 512 head-dim split: two CTAs, each M 128 over half the head
 # dimension and half the value columns
 HEAD_SPLIT_INSTR = 2 * (256 // 16 + 64 // 16)
