@@ -57,6 +57,25 @@ def test_head_dims_and_groups(d, group):
     _parity_full(w)
 
 
+@pytest.mark.parametrize("d", [64, 128, 256, 512])
+@pytest.mark.parametrize("sink_mode", [workloads.SINK_NONE, workloads.SINK_NULL_LOGIT])
+def test_output_does_not_depend_on_the_lse_request(d, sink_mode):
+    """O does not depend on whether the caller asks for the LSE: bit for bit
+    the same output with and without an LSE buffer (a prefill request with
+    ranges, a decode row and a request of one tile's ragged tail), and the
+    oracle's output and LSE within tolerance."""
+    w = workloads.Workload(f"nolse_d{d}", 40 + d, [260, 1, 70], [700, 500, 70], 4, 2, d, True, 300, 0, sink_mode,
+                           workloads.pad_ranges([[(500, 560)], [], [(2, 30)]]))
+    q, k, v, sinks = gh.make_inputs(w)
+    out_l, lse, _, _ = gh.run_gpu(w, q, k, v, sinks, with_lse=True)
+    out_n, none, _, _ = gh.run_gpu(w, q, k, v, sinks, with_lse=False)
+    assert none is None
+    assert torch.equal(out_l.view(torch.int16), out_n.view(torch.int16))
+    ref_table, _ = gh.oracle_table(w)
+    ro, rl = gh.oracle_full(w, q, k, v, sinks, ref_table)
+    gh.compare(out_n, lse, ro, rl, what=w.name, strict=False)
+
+
 def test_key0_bias_with_key0_outside_window():
     # rows beyond the window never see key 0: the bias must not touch them
     w = workloads.Workload("k0", 3, [300], [300], 4, 2, 128, False, 20, 20, workloads.SINK_KEY0_BIAS, None)
