@@ -840,7 +840,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           }
           if (j >= LEAD) {
             const int t = T + j - LEAD;
-            if (!mbar_wait_spin(&sb.p_full[C::sbuf(t)], C::sphase(t), &sb.wc, p.err, kDevTimeoutSoftmax)) {
+            // (a suspending wait: this warp shares its SM sub-partition with
+            // the softmax warps of TMEM lane quarter 1, and polling for the
+            // softmax's hand-off took their issue slots, so that in a
+            // per-warp trace those warps arrived last on most tiles)
+            if (!mbar_wait(&sb.p_full[C::sbuf(t)], C::sphase(t), &sb.wc, p.err, kDevTimeoutSoftmax)) {
               ok = false;
               break;
             }

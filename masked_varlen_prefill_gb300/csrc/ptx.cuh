@@ -122,9 +122,11 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// mbar_wait for a latency-critical single thread (the MMA issuer): polls with
-// the non-suspending test_wait, so the thread resumes the moment the phase
-// completes instead of after a suspend interval.  Same bound and abort rules.
+// mbar_wait for a latency-critical single thread (the MMA issuer's short
+// waits on loads): polls with the non-suspending test_wait, so the thread
+// resumes the moment the phase completes instead of after a suspend
+// interval, at the price of issue slots on its sub-partition.  Same bound
+// and abort rules.
 __device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, volatile WaitCtl* ctl, int* err,
                                                int code) {
   if (mbar_test_wait(bar, parity)) return true;
