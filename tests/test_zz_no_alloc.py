@@ -6,7 +6,8 @@ pool, or a host framework owns the allocator), so they cannot hand the
 split-KV workspace to mvp_attn_fwd_varlen.  It keeps the partial results in a
 fixed array inside the library.  These tests check that it returns what the
 workspace-taking entry point returns, on two calls in a row (the second call
-finds the first call's partials and work-queue words still in the array):
+finds the first call's partials and work-queue words still in the array;
+the decode-heavy batch is also compared with the float64 oracle):
 a decode-heavy batch, the full mixed serving batch (256 long decode rows,
 which the array holds with fewer splits than a full workspace would give),
 and an unwindowed prefill batch large enough to use the work queue kept in
@@ -85,6 +86,9 @@ def test_static_scratch_matches_workspace_entry_point():
         torch.cuda.synchronize()
         assert mvp.get_last_device_error() == 0
         gh.compare(out, lse, ref_o, ref_l, what=f"static-scratch call {call}", strict=True)
+    # and directly against the float64 oracle
+    ro, rl = gh.oracle_full(w, q, k, v, sinks, None)
+    gh.compare(out, lse, ro, rl, what="static scratch vs oracle", strict=True)
 
 
 def _static_call(fn, w, q, k, v, sinks, cu_q, cu_k, n_dec, stream):
