@@ -53,8 +53,12 @@ typedef enum {
   MVP_ERR_CAPACITY = -2,     /* out_capacity < num_tokens (the page asserts)    */
   MVP_ERR_UNSUPPORTED = -3,  /* head_dim / head ratio / alignment not supported */
   MVP_ERR_CUDA = -4,         /* a CUDA runtime call or launch failed            */
-  MVP_ERR_DEVICE_TIMEOUT = -5 /* a kernel recorded a bounded-wait timeout (or a
-                                 work queue shared by overlapping calls)     */
+  MVP_ERR_DEVICE_TIMEOUT = -5, /* a kernel recorded a bounded-wait timeout (or a
+                                  work queue shared by overlapping calls)    */
+  MVP_ERR_DEVICE_BOUNDS = -6   /* bounds-checked build (libmvp_debug.so) only: a
+                                  kernel found an index derived from the
+                                  caller's offsets, range table or block table
+                                  outside its buffer and skipped the access   */
 } mvp_status;
 
 typedef enum {
@@ -498,8 +502,11 @@ int mvp_attn_accounting(const int32_t* cu_seqlens_q, const int32_t* seq_lens_k, 
                         int causal, int window_left, int window_right, int variant, mvp_attn_counts* out);
 
 /* Synchronises `stream`, returns MVP_ERR_DEVICE_TIMEOUT if a kernel recorded a
- * timeout since the last call (and clears it), MVP_ERR_CUDA on a CUDA error,
- * else MVP_OK. */
+ * timeout since the last call (and clears it), MVP_ERR_DEVICE_BOUNDS if a
+ * kernel of the bounds-checked build (libmvp_debug.so, compiled with
+ * MVP_DEBUG_BOUNDS; every entry point the same) found an index outside its
+ * buffer, MVP_ERR_CUDA on a CUDA error, else MVP_OK.  Each library has its
+ * own error word. */
 int mvp_get_last_device_error(void* stream);
 
 /* Static string for a status code. */

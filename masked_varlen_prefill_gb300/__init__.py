@@ -12,6 +12,7 @@ from ._lib import (  # noqa: F401
     MVP_ERR_ARG,
     MVP_ERR_CAPACITY,
     MVP_ERR_CUDA,
+    MVP_ERR_DEVICE_BOUNDS,
     MVP_ERR_DEVICE_TIMEOUT,
     MVP_ERR_UNSUPPORTED,
     MVP_OK,
@@ -32,6 +33,7 @@ from ._lib import (  # noqa: F401
     attn_fwd_varlen_scan,
     attn_fwd_varlen_static_ws,
     attn_workspace_size,
+    bounds_checked,
     fill_query_ranges,
     get_last_device_error,
     last_launch_count,

@@ -15,6 +15,7 @@ MVP_ERR_CAPACITY = -2
 MVP_ERR_UNSUPPORTED = -3
 MVP_ERR_CUDA = -4
 MVP_ERR_DEVICE_TIMEOUT = -5
+MVP_ERR_DEVICE_BOUNDS = -6
 
 SINK_NONE = 0
 SINK_KEY0_BIAS = 1
@@ -27,8 +28,13 @@ FAULT_WITHHOLD_PROBS = 1
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "lib", "libmvp.so")
+# The bounds-checked build of the same library (include/mvp.h,
+# MVP_ERR_DEVICE_BOUNDS): for tests, selected per thread by bounds_checked().
+_DEBUG_LIB_PATH = os.path.join(_HERE, "lib", "libmvp_debug.so")
 _lib = None
+_debug_lib = None
 _lock = threading.Lock()
+_local = threading.local()
 
 _vp = ctypes.c_void_p
 _i = ctypes.c_int
@@ -90,28 +96,57 @@ class MvpError(RuntimeError):
         super().__init__(f"{fn} failed: {msg} ({status})")
 
 
-def library_path() -> str:
-    return _LIB_PATH
+def library_path(debug_bounds: bool = False) -> str:
+    return _DEBUG_LIB_PATH if debug_bounds else _LIB_PATH
 
 
-def load_library():
-    """Load the C-ABI library; raise if it has not been built."""
-    global _lib
+def _open(path):
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is missing: build it with `python -m masked_varlen_prefill_gb300._build` "
+            "(there is no CPU fallback)")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+def load_library(debug_bounds: bool | None = None):
+    """Load the C-ABI library; raise if it has not been built.  debug_bounds:
+    the bounds-checked build instead (default: the one bounds_checked()
+    selected for this thread, else the product library)."""
+    global _lib, _debug_lib
+    if debug_bounds is None:
+        debug_bounds = getattr(_local, "debug_bounds", False)
+    if debug_bounds:
+        if _debug_lib is None:
+            with _lock:
+                if _debug_lib is None:
+                    _debug_lib = _open(_DEBUG_LIB_PATH)
+        return _debug_lib
     if _lib is not None:
         return _lib
     with _lock:
         if _lib is None:
-            if not os.path.exists(_LIB_PATH):
-                raise RuntimeError(
-                    f"{_LIB_PATH} is missing: build it with `python -m masked_varlen_prefill_gb300._build` "
-                    "(there is no CPU fallback)")
-            lib = ctypes.CDLL(_LIB_PATH)
-            for name, (res, args) in _SIGNATURES.items():
-                fn = getattr(lib, name)
-                fn.restype = res
-                fn.argtypes = args
-            _lib = lib
+            _lib = _open(_LIB_PATH)
     return _lib
+
+
+class bounds_checked:
+    """Context manager: every call of this binding made on this thread inside
+    it goes to the bounds-checked library (its own device error word; read
+    it with get_last_device_error() inside the block)."""
+
+    def __enter__(self):
+        self._prev = getattr(_local, "debug_bounds", False)
+        _local.debug_bounds = True
+        return load_library(True)
+
+    def __exit__(self, *exc):
+        _local.debug_bounds = self._prev
+        return False
 
 
 def _ptr(t):
@@ -447,25 +482,26 @@ class StepMetadata:
                                      _ptr(self.range_table), _ptr(self.range_covered), ctypes.byref(handle))
         if st != MVP_OK:
             raise MvpError("mvp_meta_create", st)
+        self._lib = lib  # the handle belongs to the library that made it
         self._handle = handle
 
     def stage(self, query_start_loc, seq_lens_k, seq_lens_bound=None, ranges=None):
         """Pack one batch (host arrays) into the staging block."""
         keep, (p_qsl, p_sk, p_sb, p_rg, n, nr) = _meta_args(query_start_loc, seq_lens_k, seq_lens_bound, ranges)
-        st = load_library().mvp_meta_stage(self._handle, p_qsl, p_sk, p_sb, p_rg, n, nr)
+        st = self._lib.mvp_meta_stage(self._handle, p_qsl, p_sk, p_sb, p_rg, n, nr)
         del keep
         if st != MVP_OK:
             raise MvpError("mvp_meta_stage", st)
 
     def upload(self, stream=None):
         """Copy the staged block to the device and fill the range table."""
-        st = load_library().mvp_meta_upload(self._handle, _stream(stream, self.device))
+        st = self._lib.mvp_meta_upload(self._handle, _stream(stream, self.device))
         if st != MVP_OK:
             raise MvpError("mvp_meta_upload", st)
 
     def close(self):
         if getattr(self, "_handle", None) is not None and self._handle.value is not None:
-            load_library().mvp_meta_destroy(self._handle)
+            self._lib.mvp_meta_destroy(self._handle)
             self._handle = None
 
     def __del__(self):

@@ -127,6 +127,7 @@ const char* mvp_status_str(int status) {
     case MVP_ERR_UNSUPPORTED: return "unsupported shape or alignment";
     case MVP_ERR_CUDA: return "CUDA error";
     case MVP_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    case MVP_ERR_DEVICE_BOUNDS: return "device-side index out of bounds (bounds-checked build)";
     default: return "unknown status";
   }
 }
@@ -293,6 +294,8 @@ int attn_fwd_impl(const void* q, void* out, float* lse, const int32_t* cu_seqlen
   m.scale = scale;
   m.wait_limit_us = (opts != nullptr && opts->wait_limit_us != 0) ? opts->wait_limit_us : kDefaultWaitLimitUs;
   m.fault = opts != nullptr ? opts->fault : kFaultNone;
+  m.total_q = total_q;
+  m.err = err;
 
   const int group = num_heads_q / num_heads_kv;
   int launches = 0;
@@ -514,7 +517,7 @@ int mvp_get_last_device_error(void* stream) {
   if (value != 0) {
     const int zero = 0;
     if (cudaMemcpy(err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return MVP_ERR_CUDA;
-    return MVP_ERR_DEVICE_TIMEOUT;
+    return value == kDevBounds ? MVP_ERR_DEVICE_BOUNDS : MVP_ERR_DEVICE_TIMEOUT;
   }
   return MVP_OK;
 }

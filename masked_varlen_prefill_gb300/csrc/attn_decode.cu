@@ -123,6 +123,7 @@ __global__ void __launch_bounds__(kThreads)
   const int q0 = __ldg(p.m.cu_q + b);
   const int q_len = __ldg(p.m.cu_q + b + 1) - q0;
   if (q_len != 1) return;
+  if (!in_bounds(q0, p.total_q, p.err)) return;  // (bounds-checked build; the whole CTA)
   int k0, k_len;
   if constexpr (PAGED) {
     k0 = 0;
@@ -414,6 +415,7 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams 
   const int h = warp_global % p.hq;
   const int q0 = __ldg(p.m.cu_q + b);
   if (__ldg(p.m.cu_q + b + 1) - q0 != 1) return;
+  if (!in_bounds(q0, p.total_q, p.err)) return;  // (bounds-checked build)
   const float* part = p.partial + (static_cast<size_t>(b) * p.hq + h) * p.n_splits * (D + 2);
   float M = -INFINITY;
   for (int s = 0; s < p.n_splits; ++s) M = fmaxf(M, part[s * (D + 2) + D]);

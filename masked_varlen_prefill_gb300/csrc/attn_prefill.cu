@@ -597,7 +597,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           const int last = e.it.k_len > 0 ? (e.it.k_len - 1) >> sh : 0;
           const int nb = min((((e.pl.kb_lo + e.pl.n_tiles) * BN - 1) >> sh) - fb + 1, C::IDS_CAP);
           const int32_t* row = p.m.block_table + static_cast<size_t>(e.it.b) * p.m.max_blocks;
-          for (int i = lane; i < nb; i += 32) cp_async_4(ids + buf * C::IDS_CAP + i, row + min(fb + i, last));
+          for (int i = lane; i < nb; i += 32)
+            if (in_bounds(min(fb + i, last), p.m.max_blocks, p.err)) cp_async_4(ids + buf * C::IDS_CAP + i, row + min(fb + i, last));
           cp_async_commit();
           if (wait) {
             cp_async_wait_all();
@@ -1349,7 +1350,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       if (!ok || e.last) break;
       const int head = e.it.h0 + (row % p.gpack);
       const int qi = e.it.pos0 + pos_off + row / p.gpack;
-      const bool valid = qi < e.it.q_len;
+      const bool valid = qi < e.it.q_len && in_bounds(e.it.q0 + qi, p.total_q, p.err);  // (checked build)
       const int slot = hk % C::EPI_SLOTS;
       if (!mbar_wait(&sb.epi_full[slot], (hk / C::EPI_SLOTS) & 1, &sb.wc, p.err, kDevTimeoutSoftmax)) {
         ok = false;

@@ -17,6 +17,7 @@
 #include <cstdint>
 
 #include "mvp_internal.cuh"
+#include "ptx.cuh"
 
 namespace mvp {
 
@@ -90,6 +91,7 @@ __device__ __forceinline__ int2 scan_ranges(const MaskParams& m, int b, int p) {
 // table row, or in scan mode the scan of its request's ranges.
 __device__ __forceinline__ int2 range_entry(const MaskParams& m, int row, int b, int p) {
   if (m.ranges != nullptr) return scan_ranges(m, b, p);
+  if (!in_bounds(row, m.total_q, m.err)) return make_int2(-1, -1);
   return __ldg(reinterpret_cast<const int2*>(m.table) + row);
 }
 
@@ -134,6 +136,7 @@ __device__ __forceinline__ RowVis row_visibility_from(const MaskParams& m, int p
 __device__ __forceinline__ int kv_row(const MaskParams& m, int b, int /*k0*/, int k_len, int l) {
   const int last = k_len > 0 ? ((k_len - 1) >> m.block_shift) : 0;
   const int blk = min(l >> m.block_shift, last);
+  if (!in_bounds(blk, m.max_blocks, m.err)) return 0;
   const int id = __ldg(m.block_table + static_cast<size_t>(b) * m.max_blocks + blk);
   // unsigned: a corrupt id wraps instead of overflowing; TMA bounds-checks the row
   return static_cast<int>((static_cast<unsigned>(id) << m.block_shift) +

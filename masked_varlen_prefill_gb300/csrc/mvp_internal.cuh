@@ -51,6 +51,9 @@ struct MaskParams {
   float scale;               // > 0
   uint32_t wait_limit_us;    // budget of one bounded device wait
   int fault;                 // FaultInjection: kFaultNone except in the timeout tests
+  // bounds-checked build: rows of q / out / table, and the error word
+  int total_q;
+  int* err;
 };
 
 // ----------------------------------------------------------------- prefill

@@ -22,7 +22,30 @@ enum DeviceError : int {
   kDevTimeoutOther = 4,
   kDevTimeoutStore = 5,     // the epilogue warps never released a hand-off slot
   kDevQueueConflict = 6,    // the prefill work queue was taken over by another launch
+  kDevBounds = 7,           // bounds-checked build: an index left its buffer (access skipped)
 };
+
+// Bounds-checked build (compiled with MVP_DEBUG_BOUNDS, a second library next
+// to the product one): every global access whose index comes from the
+// caller's device-side metadata (offsets, range table, block table) is
+// checked against its buffer; an index outside records kDevBounds in the
+// device error word and the access is skipped, where an unchecked access
+// would read or write out of bounds.  The product build compiles the checks
+// away.
+#ifdef MVP_DEBUG_BOUNDS
+constexpr bool kDebugBounds = true;
+#else
+constexpr bool kDebugBounds = false;
+#endif
+__device__ __forceinline__ bool in_bounds(long long i, long long n, int* err) {
+  if constexpr (!kDebugBounds) {
+    return true;
+  } else {
+    if (i >= 0 && i < n) return true;
+    if (err != nullptr) atomicCAS(err, 0, static_cast<int>(kDevBounds));
+    return false;
+  }
+}
 
 // Default wall-clock budget of one barrier wait.  Legitimate waits in these
 // kernels last microseconds (one tile of loads or MMAs); one second means

@@ -37,8 +37,21 @@ def test_exports_every_declared_symbol(lib):
         assert hasattr(lib, n), n
 
 
+def test_bounds_checked_build_exports_the_same_symbols(lib):
+    """libmvp_debug.so (MVP_DEBUG_BOUNDS) is the same library with device
+    bounds checks: every declared entry point, and its own status string."""
+    dbg = mvp.load_library(debug_bounds=True)
+    assert dbg is not lib
+    for n in _declared():
+        assert hasattr(dbg, n), n
+    assert dbg.mvp_status_str(mvp.MVP_ERR_DEVICE_BOUNDS).decode() != "unknown status"
+    with mvp.bounds_checked() as d:
+        assert d is dbg and mvp.load_library() is dbg
+    assert mvp.load_library() is lib
+
+
 def test_status_strings(lib):
-    for code in (0, -1, -2, -3, -4, -5):
+    for code in (0, -1, -2, -3, -4, -5, -6):
         assert lib.mvp_status_str(code).decode() != "unknown status"
     assert lib.mvp_status_str(99).decode() == "unknown status"
 
