@@ -151,7 +151,12 @@ size_t mvp_attn_workspace_size(int num_reqs, int num_heads_q, int head_dim, int 
  * k, v   bf16 [total_k, num_heads_kv, head_dim], contiguous, 16-byte aligned.
  * out    bf16 [total_q, num_heads_q, head_dim] (written for every row).
  * lse    fp32 [num_heads_q, total_q] or NULL.
- * cu_seqlens_q, cu_seqlens_k  int32 [num_reqs + 1] packed offsets.
+ * cu_seqlens_q, cu_seqlens_k  int32 [num_reqs + 1] packed offsets, within
+ *                 total_q / total_k, with 0 <= q_len <= k_len per request.
+ *                 The product library trusts them (reading them on the host
+ *                 would synchronise); the bounds-checked build
+ *                 (libmvp_debug.so) reports a request with q_len > k_len, or
+ *                 a row outside total_q, as MVP_ERR_DEVICE_BOUNDS.
  * context_lens int32 [num_reqs] or NULL (NULL: k_len - q_len).
  * max_q_len, max_k_len  host upper bounds of the per-request lengths (used to
  *                 size the grid; rows beyond them are not computed).

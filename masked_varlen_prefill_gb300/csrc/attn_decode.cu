@@ -132,6 +132,7 @@ __global__ void __launch_bounds__(kThreads)
     k0 = __ldg(p.m.cu_k + b);
     k_len = __ldg(p.m.cu_k + b + 1) - k0;
   }
+  (void)in_bounds(0, k_len, p.err);  // a decode row needs a key: q_len <= k_len (checked build)
   const int pos = p.m.ctx_lens ? __ldg(p.m.ctx_lens + b) : (k_len - 1);
   const RowVis vis = row_visibility(p.m, pos, k_len, table_active(p.m), q0, b);
   int lo, hi;

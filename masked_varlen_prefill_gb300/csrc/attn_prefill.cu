@@ -276,6 +276,7 @@ __device__ __forceinline__ Item item_geometry(int item, const PrefillParams& p) 
     it.k_len = __ldg(p.m.cu_k + it.b + 1) - it.k0;
   }
   it.ctx = p.m.ctx_lens ? __ldg(p.m.ctx_lens + it.b) : (it.k_len - it.q_len);
+  if (it.q_len > 0) (void)in_bounds(it.q_len - 1, it.k_len, p.err);  // q_len <= k_len (checked build)
   it.pos0 = (p.n_qtiles - 1 - x) * (C::ITEM_ROWS / p.gpack);
   it.valid = it.pos0 < it.q_len && !(p.skip_decode && it.q_len == 1);
   return it;
