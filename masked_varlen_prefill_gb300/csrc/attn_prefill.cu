@@ -282,16 +282,16 @@ __device__ __forceinline__ Item item_geometry(int item, const PrefillParams& p) 
   return it;
 }
 
-// The scheduler's next item index after an invalid item `item` (geometry
-// `it`), in its static-stride class (item mod stride): the first item of
-// this (request, head) block whose q tile has rows, or, when the request has
-// no prefill rows at all, the first item of the next request that has (32
-// requests tested per step by the warp).  Item spaces sized for a capacity
-// (upper-bound q lengths, padding requests) then cost O(requests) per CTA,
-// not O(items).  Warp-collective; returns INT_MAX past the last item.
+// The first item after an invalid item `item` (geometry `it`) that can have
+// rows: the first item of this (request, head) block whose q tile has rows,
+// or, when the request has no prefill rows at all, the first item of the
+// next request that has (32 requests tested per step by the warp); the
+// scheduler then takes the first item of its own sequence at or after it.
+// Item spaces sized for a capacity (upper-bound q lengths, padding requests)
+// then cost O(requests) per CTA, not O(items).  Warp-collective; LLONG_MAX
+// past the last request.
 template <class C>
-__device__ __forceinline__ int next_candidate(int item, const Item& it, const PrefillParams& p, int stride,
-                                              int lane) {
+__device__ __forceinline__ long long candidate_target(int item, const Item& it, const PrefillParams& p, int lane) {
   const int nz = p.hkv * p.n_hgroups * C::DV_SPLIT;
   const long long per_req = static_cast<long long>(nz) * p.n_qtiles;
   const int prows = C::ITEM_ROWS / p.gpack;  // query positions per item
@@ -303,7 +303,7 @@ __device__ __forceinline__ int next_candidate(int item, const Item& it, const Pr
   } else {
     int b = it.b + 1;
     for (;;) {
-      if (b >= p.num_reqs) return INT_MAX;
+      if (b >= p.num_reqs) return LLONG_MAX;
       const int c = b + lane;
       bool good = false;
       if (c < p.num_reqs) {
@@ -319,8 +319,7 @@ __device__ __forceinline__ int next_candidate(int item, const Item& it, const Pr
     }
     target = (b - p.req_offset) * per_req;
   }
-  const long long next = item + ((target - item + stride - 1) / stride) * stride;
-  return next > INT_MAX ? INT_MAX : static_cast<int>(next);
+  return target;
 }
 
 // Work-queue words (the prefill scheduler's, in the caller's workspace):
@@ -938,16 +937,38 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         return idx >= 0 && idx < n_items - n_static ? n_static + static_cast<int>(idx) : INT_MAX;
       };
       int item = -1;
+      int round = -1;  // static rounds walked
       int qc = 0;  // claims made (rank 0) / received (rank 1)
       for (int c = 0; ok; ++c) {  // c: plan entries
         PlanEntry e;
         if (!dyn || item < n_static) {  // static phase
-          const int first = blockIdx.x / C::NCTA;
-          item = item < 0 ? first : (item >= n_items - n_groups ? INT_MAX : item + n_groups);
+          // Round rr of the static rounds gives this CTA (group g) item
+          // rr * n_groups + g.  When every item is static (no work queue),
+          // odd rounds run backwards (rr * n_groups + n_groups - 1 - g): the
+          // groups that take the first items of one round take the last of
+          // the next, which evens out the items' costs across groups (they
+          // fall with the position inside a (request, head) block).  Measured
+          // on the windowed mixed batch's prefill rows: 0.588 vs 0.565 of the
+          // bf16 peak; ahead of a queued last round it cost 1-5 %.
+          const int g = blockIdx.x / C::NCTA;
+          auto item_of = [&](long long rr) -> int {
+            const long long it_ = rr * n_groups + ((!dyn && (rr & 1)) ? n_groups - 1 - g : g);
+            return it_ >= n_items ? INT_MAX : static_cast<int>(it_);
+          };
+          ++round;
+          item = item_of(round);
           while (item < n_static) {  // skip items without rows
             e.it = item_geometry<C, PAGED>(item, p);
             if (e.it.valid) break;
-            item = next_candidate<C>(item, e.it, p, n_groups, lane);
+            const long long target = candidate_target<C>(item, e.it, p, lane);
+            if (target >= n_items) {
+              item = INT_MAX;
+              break;
+            }
+            long long rr = target / n_groups;  // the first round whose item is at or after target
+            if (static_cast<long long>(item_of(rr)) < target) ++rr;
+            round = static_cast<int>(rr);
+            item = item_of(round);
           }
         }
         if (dyn && item >= n_static) {  // queue phase
@@ -967,7 +988,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             while (ok && item < n_items) {  // skip items without rows
               e.it = item_geometry<C, PAGED>(item, p);
               if (e.it.valid) break;
-              const int target = next_candidate<C>(item, e.it, p, 1, lane);
+              const long long target = candidate_target<C>(item, e.it, p, lane);
               if (target >= n_items) {
                 item = INT_MAX;
               } else {
