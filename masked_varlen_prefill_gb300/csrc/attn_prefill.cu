@@ -597,8 +597,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           const int last = e.it.k_len > 0 ? (e.it.k_len - 1) >> sh : 0;
           const int nb = min((((e.pl.kb_lo + e.pl.n_tiles) * BN - 1) >> sh) - fb + 1, C::IDS_CAP);
           const int32_t* row = p.m.block_table + static_cast<size_t>(e.it.b) * p.m.max_blocks;
-          for (int i = lane; i < nb; i += 32)
-            if (in_bounds(min(fb + i, last), p.m.max_blocks, p.err)) cp_async_4(ids + buf * C::IDS_CAP + i, row + min(fb + i, last));
+          for (int i = lane; i < nb; i += 32) {
+            const int blk = min(fb + i, last);
+            if (in_bounds(blk, p.m.max_blocks, p.err)) cp_async_4(ids + buf * C::IDS_CAP + i, row + blk);
+          }
           cp_async_commit();
           if (wait) {
             cp_async_wait_all();
