@@ -76,6 +76,29 @@ def test_output_does_not_depend_on_the_lse_request(d, sink_mode):
     gh.compare(out_n, lse, ro, rl, what=w.name, strict=False)
 
 
+@pytest.mark.parametrize("d", [64, 128, 256, 512])
+@pytest.mark.parametrize("sink_mode", [workloads.SINK_NONE, workloads.SINK_NULL_LOGIT])
+def test_running_max_moves_on_every_tile(d, sink_mode):
+    """Scores that rise along the keys by ~12 (log2 units) per 128 keys move
+    every row's running max past the lazy-rescale threshold tile after tile,
+    so O (and, at D = 128, the row sums the PV MMA accumulates beside it) is
+    rescaled on every tile; N(0, 1) inputs almost never do that after the
+    first tile.  Full (non-causal) attention over ragged lengths."""
+    w = workloads.Workload(f"rising_d{d}", 500 + d, [200, 130], [1200, 700], 4, 2, d, False, -1, -1, sink_mode,
+                           None)
+    q, k, v, sinks = gh.make_inputs(w)
+    slope = 12.0 / (1.4426950408889634 * w.scale * 128)
+    _, cu_k = w.cu_seqlens()
+    for b in range(w.num_reqs):
+        n = int(cu_k[b + 1] - cu_k[b])
+        ramp = slope * torch.arange(n, device=k.device, dtype=torch.float32)
+        k[cu_k[b]:cu_k[b + 1], :, 0] = ramp[:, None].to(torch.bfloat16)
+    q[:, :, 0] = 1.0
+    out, lse, _, _ = gh.run_gpu(w, q, k, v, sinks)
+    ro, rl = gh.oracle_full(w, q, k, v, sinks, None)
+    gh.compare(out, lse, ro, rl, what=w.name, strict=False)
+
+
 def test_key0_bias_with_key0_outside_window():
     # rows beyond the window never see key 0: the bias must not touch them
     w = workloads.Workload("k0", 3, [300], [300], 4, 2, 128, False, 20, 20, workloads.SINK_KEY0_BIAS, None)
