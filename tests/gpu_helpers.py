@@ -17,12 +17,16 @@ from oracle import range_table as ort
 
 OUT_ATOL = 1e-2
 LSE_RTOL = 1e-3
-# bf16 keeps 8 significant bits: a correctly rounded bf16 output can differ
-# from the exact value by half an ulp, i.e. up to 2^-9 |x|, and the bf16
-# probabilities of the P.V product add about as much again.  For |out| above
-# 2.56 that exceeds 1e-2 no matter how the kernel computes, so shapes that
-# produce such outputs (a few visible keys per row) use max(1e-2, 2^-8 |ref|).
-BF16_REL = 2.0 ** -8
+# bf16 keeps 8 significant bits (unit roundoff u = 2^-8): a correctly
+# rounded bf16 output can differ from the exact value by half an ulp, up to
+# u |x| (just above a power of two), and rounding the probabilities to bf16
+# for the P.V product perturbs each weight by up to u as well, which can move
+# the output by about as much again (a row with a few visible keys and a
+# null-logit sink has no cancellation).  Together 2u |x| = 2^-7 |x|: for
+# |out| above 1.28 that exceeds 1e-2 however the kernel computes, so shapes
+# that produce such outputs (a few visible keys per row) use
+# max(1e-2, 2^-7 |ref|).
+BF16_REL = 2.0 ** -7
 
 
 def device_meta(w, dev):
@@ -118,7 +122,7 @@ def compare(out_gpu, lse_gpu, out_ref, lse_ref, rows=None, what="", strict=True)
     """Assert the tolerances; returns (max_abs_out, max_rel_lse).
 
     strict: out max-abs <= 1e-2 everywhere (the workload shapes).  Otherwise
-    each element may also use the bf16 bound 2^-8 |ref| when that is larger."""
+    each element may also use the bf16 bound 2^-7 |ref| when that is larger."""
     og = out_gpu.float().cpu().numpy()
     lg = None if lse_gpu is None else lse_gpu.cpu().numpy()
     where = ""
@@ -156,7 +160,7 @@ def compare(out_gpu, lse_gpu, out_ref, lse_ref, rows=None, what="", strict=True)
                 f = np.isfinite(ref)
                 if f.any():
                     err_l = max(err_l, float((np.abs(got[f] - ref[f]) / np.maximum(np.abs(ref[f]), 1.0)).max()))
-    kind = "max-abs" if strict else "scaled error (1e-2 or 2^-8|ref|)"
+    kind = "max-abs" if strict else "scaled error (1e-2 or 2^-7|ref|)"
     assert err_o <= OUT_ATOL, f"{what}: out {kind} {err_o:.3e} > {OUT_ATOL}{where}"
     assert err_l <= LSE_RTOL, f"{what}: lse rel {err_l:.3e} > {LSE_RTOL}"
     return err_o, err_l
