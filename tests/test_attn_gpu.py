@@ -11,6 +11,8 @@ import numpy as np
 import pytest
 import torch
 
+import masked_varlen_prefill_gb300 as mvp
+
 from masked_varlen_prefill_gb300 import workloads
 
 from . import gpu_helpers as gh
@@ -106,6 +108,39 @@ def test_running_max_moves_on_every_tile(d, sink_mode):
     out, lse, _, _ = gh.run_gpu(w, q, k, v, sinks)
     ro, rl = gh.oracle_full(w, q, k, v, sinks, None)
     gh.compare(out, lse, ro, rl, what=w.name, strict=False)
+
+
+@pytest.mark.parametrize("d", [128, 256])
+def test_upper_bound_item_space_with_the_alternating_static_order(d):
+    """A windowed batch without ranges runs every item statically, odd rounds
+    walking the pairs backwards.  Sized by an upper bound of the query
+    lengths (4x), most items have no rows and the scheduler jumps over them
+    (to the block's first q tile with rows, or the next request with any);
+    zero-row requests sit between the others.  Every item computes the same
+    arithmetic whichever pair takes it: the bits must equal the call sized by
+    the exact maximum, and both the oracle."""
+    q_lens = [300, 0, 700, 1, 0, 520, 64, 0, 900]
+    k_lens = [800, 0, 700, 1500, 3, 2000, 64, 9, 4000]
+    w = workloads.Workload(f"ubound_d{d}", 70 + d, q_lens, k_lens, 8, 2, d, True, 511, 0,
+                           workloads.SINK_NULL_LOGIT, None)
+    q, k, v, sinks = gh.make_inputs(w)
+    cu_q, cu_k = gh.device_meta(w, q.device)
+
+    def call(max_q):
+        out = torch.full_like(q, float("nan"))
+        lse = torch.full((w.num_heads_q, w.total_q), float("nan"), device=q.device)
+        mvp.attn_fwd_varlen(q, k, v, out, cu_q, cu_k, max_q, max(k_lens), lse=lse, causal=True,
+                            window_left=w.window_left, sinks=sinks, sink_mode=w.sink_mode, scale=w.scale)
+        torch.cuda.synchronize()
+        assert mvp.get_last_device_error() == 0
+        return out, lse
+
+    out_e, lse_e = call(max(q_lens))
+    out_u, lse_u = call(4 * max(q_lens))
+    assert torch.equal(out_e.view(torch.int16), out_u.view(torch.int16))
+    assert torch.equal(lse_e, lse_u)
+    ro, rl = gh.oracle_full(w, q, k, v, sinks, None)
+    gh.compare(out_u, lse_u, ro, rl, what=w.name, strict=False)
 
 
 def test_key0_bias_with_key0_outside_window():
