@@ -12,7 +12,6 @@ import pytest
 import torch
 
 import masked_varlen_prefill_gb300 as mvp
-
 from masked_varlen_prefill_gb300 import workloads
 
 from . import gpu_helpers as gh
