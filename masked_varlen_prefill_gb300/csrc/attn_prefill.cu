@@ -129,6 +129,11 @@ struct Cfg {
   // LSE).  A V stage is VCH blocks of BN x 128 bytes (the loaded value
   // columns) plus the ones block.
   static constexpr bool ROWSUM = ROWSUM_ != 0;
+  // Otherwise the softmax warps sum the rounded probabilities: at D = 512 by
+  // mixed-precision adds (add.rn.f32.bf16 on each bf16 half, no unpack;
+  // same bits), measured 58.5 vs 57.6 % of the bf16 peak there, while at
+  // D = 256 the shift / mask / packed add measured 0.5-1 % faster.
+  static constexpr bool MIXED_SUM = !ROWSUM && D_ == 512;
   static constexpr int ONES = ROWSUM ? 16 : 0;
   static constexpr int V_STAGE = (VCH + (ROWSUM ? 1 : 0)) * BN * 128;  // stage stride
   static constexpr int PART = DVC + ONES;                           // accumulator columns per CTA part
@@ -1246,8 +1251,12 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const uint64_t sc2 = f2_pack(sc, sc);
         const uint64_t nm2 = f2_pack(-m_use, -m_use);
         uint64_t acc_r[4], acc_e[4];
+        float acc_lo[4], acc_hi[4];  // (MIXED_SUM: rounded probabilities of the even, odd columns)
 #pragma unroll
-        for (int k = 0; k < 4; ++k) acc_r[k] = acc_e[k] = 0ull;
+        for (int k = 0; k < 4; ++k) {
+          acc_r[k] = acc_e[k] = 0ull;
+          acc_lo[k] = acc_hi[k] = 0.f;
+        }
 #pragma unroll
         for (int i = 0; i < HC / 2; ++i) {
           float t0, t1;
@@ -1255,14 +1264,20 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           const float e0 = ex2_approx(t0);
           const float e1 = ex2_approx(t1);
           const uint32_t pk = pack_bf16x2(e0, e1);
-          if constexpr (!C::ROWSUM)  // (else the tensor core sums the rounded values)
+          if constexpr (C::MIXED_SUM)
+            add_bf16x2_halves(pk, acc_lo[i & 3], acc_hi[i & 3]);
+          else if constexpr (!C::ROWSUM)  // (else the tensor core sums the rounded values)
             acc_r[i & 3] = f2_add(acc_r[i & 3], f2_pack(__uint_as_float(pk << 16), __uint_as_float(pk & 0xffff0000u)));
           acc_e[i & 3] = f2_add(acc_e[i & 3], f2_pack(e0, e1));
           s[i] = pk;
         }
         {
           float a0, a1, b0, b1;
-          if constexpr (!C::ROWSUM) {
+          if constexpr (C::MIXED_SUM) {
+            a0 = (acc_lo[0] + acc_lo[1]) + (acc_lo[2] + acc_lo[3]);
+            a1 = (acc_hi[0] + acc_hi[1]) + (acc_hi[2] + acc_hi[3]);
+            l_sum += a0 + a1;
+          } else if constexpr (!C::ROWSUM) {
             f2_unpack(f2_add(f2_add(acc_r[0], acc_r[1]), f2_add(acc_r[2], acc_r[3])), a0, a1);
             l_sum += a0 + a1;
           }

@@ -607,6 +607,16 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
   return d;
 }
 
+// Mixed-precision adds (sm_100+): each bf16 half of `pk` is added to an fp32
+// accumulator as its exact fp32 value, rounded to nearest (the same result as
+// widening the half by a shift or mask and adding in fp32).
+__device__ __forceinline__ void add_bf16x2_halves(uint32_t pk, float& lo_acc, float& hi_acc) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "add.rn.f32.bf16 %0, l, %0;\n\tadd.rn.f32.bf16 %1, h, %1;\n\t}"
+      : "+f"(lo_acc), "+f"(hi_acc)
+      : "r"(pk));
+}
+
 // Named barrier over `count` threads (ids 1..15; 0 is __syncthreads).
 __device__ __forceinline__ void named_barrier(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
