@@ -33,6 +33,7 @@ constexpr int kNW = 4;                      // compute warps
 constexpr int kThreads = (kNW + 1) * 32;    // + producer warp
 constexpr int kMaxStages = 3;
 constexpr unsigned kFull = 0xffffffffu;
+constexpr float kRescaleThreshold = 8.0f;   // log2 units
 
 __host__ __device__ constexpr int kt_for(int d) { return d == 64 ? 128 : (d == 128 ? 64 : 32); }
 // Stages of the K/V ring.  D = 128: two, so that three CTAs (12 compute warps)
@@ -105,8 +106,9 @@ __global__ void __launch_bounds__(kThreads)
   constexpr int NG = C::KT / KG;     // warp steps per tile
   extern __shared__ uint8_t smem_raw[];
   // Per compute warp, the step's 32 probabilities (key kk, head g at
-  // kk * GP + g), read back by every lane as vectors instead of 32 shuffles.
-  __shared__ __align__(16) float pbuf[kNW][32];
+  // kk * GP + g) as (p, p) pairs, read back by every lane as broadcasts
+  // instead of 32 shuffles.
+  __shared__ __align__(16) float pbuf[kNW][64];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ DBarriers sb;
 
@@ -209,37 +211,71 @@ __global__ void __launch_bounds__(kThreads)
   }
 
   // ------------------------------------------------------------------ compute
-  // q for this lane's dims, every head of the CTA, pre-scaled to log2 units;
-  // kept as (even, odd) dim pairs for the packed fp32x2 FMAs below.
-  constexpr int DP2 = DPL / 2;
-  uint64_t q2[GP][DP2];
+  // Scores: DS lanes share one key's dot product, each over QDL dims (two or
+  // one 16-byte chunks of the K row: chunk ds + j * DS, so the eight lanes of
+  // a quarter-warp read 128 consecutive bytes), for all GP heads at once; a
+  // reduce-scatter over those DS lanes leaves each lane the full score of one
+  // (key, head) pair, held by DUP lanes alike.  A warp step of KG keys runs
+  // NSUB such sub-steps of KS keys, so that every lane owns the probability
+  // of one of the step's 32 (key, head) pairs.
+  constexpr int QDL = (GP == 8) ? 8 : 16;  // dims per lane in the score step (q registers: QDL * GP)
+  constexpr int DS = D / QDL;              // lanes per key
+  constexpr int KS = 32 / DS;              // keys per sub-step
+  constexpr int DUP = DS / GP;             // lanes holding the same score
+  constexpr int NSUB = DUP;                // sub-steps per warp step
+  constexpr int QCH = QDL / 8;             // 16-byte chunks of a K row per lane
+  static_assert(DS >= GP && DS <= 32 && KS * NSUB == KG, "score layout");
+  const int ds = lane % DS;   // dim slice
+  const int ks = lane / DS;   // key of the sub-step
+  const int hh = ds / DUP;    // head of this lane's scores
+  const int rr = ds % DUP;    // the sub-step whose score this lane keeps
+
+  // q for this lane's dim chunks, every head of the CTA, pre-scaled to log2
+  // units, as (even, odd) dim pairs for the packed fp32x2 FMAs.
+  uint64_t q2[GP][QDL / 2];
 #pragma unroll
   for (int g = 0; g < GP; ++g) {
-    float tmp[DPL];
 #pragma unroll
-    for (int d = 0; d < DPL; ++d) tmp[d] = 0.f;
-    if (g < heads_here) {
-      const uint8_t* src = reinterpret_cast<const uint8_t*>(p.q) +
-                           ((static_cast<size_t>(q0) * p.hq + hq0 + g) * D + lane * DPL) * 2;
-      load_row<DPL>(src, tmp);
+    for (int j = 0; j < QCH; ++j) {
+      float tmp[8];
+#pragma unroll
+      for (int d = 0; d < 8; ++d) tmp[d] = 0.f;
+      if (g < heads_here) {
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(p.q) +
+                             ((static_cast<size_t>(q0) * p.hq + hq0 + g) * D + 8 * (ds + j * DS)) * 2;
+        load_row<8>(src, tmp);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        q2[g][4 * j + i] = f2_pack(tmp[2 * i] * p.m.scale_log2, tmp[2 * i + 1] * p.m.scale_log2);
     }
-#pragma unroll
-    for (int i = 0; i < DP2; ++i) q2[g][i] = f2_pack(tmp[2 * i] * p.m.scale_log2, tmp[2 * i + 1] * p.m.scale_log2);
   }
-  const int my_g = lane % GP;
   const bool key0_mode = p.m.sink_mode == 1 && p.m.sinks != nullptr;
   float my_sink = 0.f;
-  if (key0_mode && my_g < heads_here) my_sink = __ldg(p.m.sinks + hq0 + my_g) * 1.4426950408889634f;
+  if (key0_mode && hh < heads_here) my_sink = __ldg(p.m.sinks + hq0 + hh) * 1.4426950408889634f;
+  // Keys every lane may take without a mask test: inside the split and in
+  // the interval the row sees whole (key 0 excluded when it carries a sink).
+  int core_lo, core_hi;
+  vis.core(core_lo, core_hi);
+  core_hi = min(core_hi, c_hi);
+  if (key0_mode) core_lo = max(core_lo, 1);
 
-  float m[GP];
-  uint64_t acc2[GP][DP2];  // O partial sums, (even, odd) dim pairs
-  float l_part = 0.f;
+  // Per-step probabilities as (p, p) pairs, [key of the step][head], read
+  // back by every lane as broadcasts.
+  uint64_t* pb = reinterpret_cast<uint64_t*>(pbuf[warp]);
+
+  // O partial sums: lane l owns dims [l * DPL, (l + 1) * DPL) of every head.
+  constexpr int DP2 = DPL / 2;
+  uint64_t acc2[GP][DP2];
 #pragma unroll
-  for (int g = 0; g < GP; ++g) {
-    m[g] = -INFINITY;
+  for (int g = 0; g < GP; ++g)
 #pragma unroll
     for (int i = 0; i < DP2; ++i) acc2[g][i] = 0ull;  // (+0.f, +0.f)
-  }
+  // Running max of head hh in log2 units, raised only when a step's max
+  // exceeds it by more than kRescaleThreshold (probabilities stay <= 2^8),
+  // and this lane's share of that head's sum.
+  float m_h = -INFINITY;
+  float l_part = 0.f;
 
   bool ok = true;
   for (int t = 0; t < n_tiles && ok; ++t) {
@@ -248,83 +284,97 @@ __global__ void __launch_bounds__(kThreads)
       ok = false;
       break;
     }
-    const uint8_t* ks = smem + s * 2 * C::TILE;
-    const uint8_t* vs = ks + C::TILE;
+    const uint8_t* ks_tile = smem + s * 2 * C::TILE;
+    const uint8_t* vs_tile = ks_tile + C::TILE;
+    const int t0 = c_lo + t * C::KT;
+    const bool interior = t0 >= core_lo && t0 + C::KT - 1 <= core_hi;
     for (int gi = warp; gi < NG; gi += kNW) {
-      float v[32];
+      float x[NSUB];
 #pragma unroll
-      for (int kk = 0; kk < KG; ++kk) {
-        float kr[DPL];
-        load_row<DPL>(ks + row_off<D>(gi * KG + kk, lane), kr);
-        uint64_t k2[DP2];
+      for (int a = 0; a < NSUB; ++a) {
+        const int kk = gi * KG + a * KS + ks;  // key of the tile
+        uint64_t a2[GP];
 #pragma unroll
-        for (int i = 0; i < DP2; ++i) k2[i] = f2_pack(kr[2 * i], kr[2 * i + 1]);
+        for (int j = 0; j < QCH; ++j) {
+          const int dim0 = 8 * (ds + j * DS);
+          float kr[8];
+          load_row<8>(ks_tile + (dim0 / C::BOX) * (C::KT * C::BOX * 2) + kk * (C::BOX * 2) + (dim0 % C::BOX) * 2,
+                      kr);
+          uint64_t k2[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) k2[i] = f2_pack(kr[2 * i], kr[2 * i + 1]);
+#pragma unroll
+          for (int g = 0; g < GP; ++g)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              a2[g] = (j == 0 && i == 0) ? f2_mul(q2[g][0], k2[0]) : f2_fma(q2[g][4 * j + i], k2[i], a2[g]);
+        }
+        float v[GP];
 #pragma unroll
         for (int g = 0; g < GP; ++g) {
-          // even and odd dims summed separately, then added
-          uint64_t a2 = f2_mul(q2[g][0], k2[0]);
-#pragma unroll
-          for (int i = 1; i < DP2; ++i) a2 = f2_fma(q2[g][i], k2[i], a2);
           float ae, ao;
-          f2_unpack(a2, ae, ao);
-          v[kk * GP + g] = ae + ao;
+          f2_unpack(a2[g], ae, ao);
+          v[g] = ae + ao;
+        }
+        // reduce-scatter over the DS lanes of the key: while more than one
+        // head is left, the upper lanes keep the upper half; then plain sums
+#pragma unroll
+        for (int o = DS / 2, n = GP / 2; o >= 1; o >>= 1, n >>= 1) {
+          if (n >= 1) {
+            const bool upper = (lane & o) != 0;
+#pragma unroll
+            for (int i = 0; i < n; ++i) {
+              const float send = upper ? v[i] : v[i + n];
+              const float keep = upper ? v[i + n] : v[i];
+              v[i] = keep + __shfl_xor_sync(kFull, send, o);
+            }
+          } else {
+            v[0] += __shfl_xor_sync(kFull, v[0], o);
+          }
+        }
+        x[a] = v[0];
+        if (!interior) {
+          const int key = t0 + kk;
+          if (key0_mode && key == 0) x[a] += my_sink;
+          if (!(key <= c_hi && vis.visible(key))) x[a] = -INFINITY;
         }
       }
-      // reduce-scatter: lane l ends with the full sum of pair l
+      // max of head hh over the step's keys: this lane's NSUB, then the KS keys
+      float mx = x[0];
 #pragma unroll
-      for (int o = 16, n = 16; o >= 1; o >>= 1, n >>= 1) {
-        const bool upper = (lane & o) != 0;
+      for (int a = 1; a < NSUB; ++a) mx = fmaxf(mx, x[a]);
 #pragma unroll
-        for (int i = 0; i < n; ++i) {
-          const float send = upper ? v[i] : v[i + n];
-          const float keep = upper ? v[i + n] : v[i];
-          v[i] = keep + __shfl_xor_sync(kFull, send, o);
+      for (int o = DS; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+      const bool need = mx > m_h + kRescaleThreshold;
+      if (__any_sync(kFull, need)) {
+        const float alpha = need ? ex2_approx(m_h - mx) : 1.f;  // 0 while m_h is -inf
+        if (need) m_h = mx;
+        l_part *= alpha;
+#pragma unroll
+        for (int g = 0; g < GP; ++g) {
+          const float ag = __shfl_sync(kFull, alpha, g * DUP);
+          const uint64_t a2 = f2_pack(ag, ag);
+#pragma unroll
+          for (int i = 0; i < DP2; ++i) acc2[g][i] = f2_mul(acc2[g][i], a2);
         }
       }
-      const int key = c_lo + t * C::KT + gi * KG + lane / GP;
-      float x = v[0];
-      if (key0_mode && key == 0) x += my_sink;
-      const bool visible = key <= c_hi && vis.visible(key);
-      x = visible ? x : -INFINITY;
-      // per-head max over this step's keys
-      float mx = x;
+      float xr = x[0];
 #pragma unroll
-      for (int o = GP; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
-      float alpha[GP];
-#pragma unroll
-      for (int g = 0; g < GP; ++g) {
-        const float gm = __shfl_sync(kFull, mx, g);
-        const float mn = fmaxf(m[g], gm);
-        alpha[g] = (mn == -INFINITY) ? 1.f : ex2_approx(m[g] - mn);
-        m[g] = mn;
-      }
-      float my_m = m[0];
-#pragma unroll
-      for (int g = 1; g < GP; ++g) my_m = (my_g == g) ? m[g] : my_m;
-      float my_alpha = alpha[0];
-#pragma unroll
-      for (int g = 1; g < GP; ++g) my_alpha = (my_g == g) ? alpha[g] : my_alpha;
-      const float pr = (x == -INFINITY) ? 0.f : ex2_approx(x - my_m);
-      l_part = l_part * my_alpha + pr;
-#pragma unroll
-      for (int g = 0; g < GP; ++g) {
-        const uint64_t a2 = f2_pack(alpha[g], alpha[g]);
-#pragma unroll
-        for (int i = 0; i < DP2; ++i) acc2[g][i] = f2_mul(acc2[g][i], a2);
-      }
-      pbuf[warp][lane] = pr;
+      for (int a = 1; a < NSUB; ++a) xr = (rr == a) ? x[a] : xr;
+      const float pr = (xr == -INFINITY) ? 0.f : ex2_approx(xr - m_h);
+      l_part += pr;
+      pb[(rr * KS + ks) * GP + hh] = f2_pack(pr, pr);
       __syncwarp();
 #pragma unroll
       for (int kk = 0; kk < KG; ++kk) {
         float vr[DPL];
-        load_row<DPL>(vs + row_off<D>(gi * KG + kk, lane), vr);
+        load_row<DPL>(vs_tile + row_off<D>(gi * KG + kk, lane), vr);
         uint64_t v2[DP2];
 #pragma unroll
         for (int i = 0; i < DP2; ++i) v2[i] = f2_pack(vr[2 * i], vr[2 * i + 1]);
 #pragma unroll
         for (int g = 0; g < GP; ++g) {
-          const float pg = pbuf[warp][kk * GP + g];  // same address in every lane: broadcast
-          const uint64_t pg2 = f2_pack(pg, pg);
+          const uint64_t pg2 = pb[kk * GP + g];  // same address in every lane: broadcast
 #pragma unroll
           for (int i = 0; i < DP2; ++i) acc2[g][i] = f2_fma(pg2, v2[i], acc2[g][i]);
         }
@@ -335,9 +385,11 @@ __global__ void __launch_bounds__(kThreads)
     if (lane == 0) mbar_arrive(&sb.empty[s]);
   }
 
-  // per-head sums: lanes holding the same head
+  // per-head sums: the lanes holding head hh (every key, every duplicate)
 #pragma unroll
-  for (int o = GP; o < 32; o <<= 1) l_part += __shfl_xor_sync(kFull, l_part, o);
+  for (int o = 1; o < DUP; o <<= 1) l_part += __shfl_xor_sync(kFull, l_part, o);
+#pragma unroll
+  for (int o = DS; o < 32; o <<= 1) l_part += __shfl_xor_sync(kFull, l_part, o);
 
   // ------------------------------------------------------------------ merge warps
   // Stage buffers are free once every tile was consumed by every warp.
@@ -353,15 +405,11 @@ __global__ void __launch_bounds__(kThreads)
       sm[(warp * GP + g) * D + lane * DPL + 2 * i] = x0;
       sm[(warp * GP + g) * D + lane * DPL + 2 * i + 1] = x1;
     }
-  if (lane < GP) {
-    float mm = m[0];
-#pragma unroll
-    for (int g = 1; g < GP; ++g) mm = (lane == g) ? m[g] : mm;
-    sml[(warp * GP + lane) * 2 + 0] = mm;
-    sml[(warp * GP + lane) * 2 + 1] = l_part;  // lane g holds head g's sum
+  if (ks == 0 && rr == 0) {  // lane hh * DUP: head hh's max and sum
+    sml[(warp * GP + hh) * 2 + 0] = m_h;
+    sml[(warp * GP + hh) * 2 + 1] = l_part;
   }
   asm volatile("bar.sync 1, %0;" ::"r"(kNW * 32) : "memory");
-
   const bool null_mode = p.m.sink_mode == 2 && p.m.sinks != nullptr;
   for (int idx = threadIdx.x; idx < heads_here * D; idx += kNW * 32) {
     const int g = idx / D, d = idx % D;
