@@ -213,11 +213,13 @@ int mvp_attn_fwd_varlen(const void* q, const void* k, const void* v, void* out, 
  *                rows, given in decode-first order (num_decode_reqs >= 1
  *                and rows after them), run the decode kernel beside the
  *                prefill kernel: the prefill kernel's persistent CTAs take
- *                this many SMs (0: the library's choice, three quarters of
- *                the SMs when the decode side's estimated work is at least a
- *                third of the prefill side's, else the two kernels run in
- *                turn; > 0: that many, rounded to CTA pairs and at most the
- *                SM count - 2) and the decode kernel runs on a second stream
+ *                this many SMs (0: the library's choice, 1.2 times the
+ *                prefill side's part of the two sides' estimated work, at
+ *                most three quarters of the SMs, when the decode side's
+ *                estimated work is at least a third of the prefill side's,
+ *                else the two kernels run in turn; > 0: that many, rounded
+ *                to CTA pairs and at most the SM count - 2) and the decode
+ *                kernel runs on a second stream
  *                of the library's (one per device), forked from and joined
  *                back to `stream` with events, so all the call's work is
  *                still ordered before later work on `stream`, also inside a

@@ -189,20 +189,21 @@ struct KVArgs {
 };
 
 // SMs for the prefill kernel of a mixed batch while the decode kernel runs
-// beside it, or 0 to run the two one after the other.  Both kernels' rates
-// grow with the SMs they hold (the decode kernel reaches the HBM peak only on
-// nearly all of them), so side by side they mostly save tails: the decode
-// CTAs fill the SMs the prefill kernel's last round leaves idle and the
-// prefill CTAs overlap the decode kernel's last wave.  Measured on the mixed
-// serving batches (152 SMs): 96 to 144 SMs for the prefill kernel all gave
-// 1-3 % over running the kernels in turn, 112 the best; a share sized by the
-// two sides' work (about 40 SMs for the prefill kernel) was slower than in
-// turn.  So the prefill kernel keeps three quarters of the SMs, and only
-// when the decode side has enough work to fill the other quarter for the
-// prefill kernel's duration: its estimated time (K/V bytes at the HBM rate)
-// at least a third of the prefill side's (FLOPs at the tensor rate).  The
-// key counts are device data, so the estimates use an average key run per
-// request (total_k / num_reqs packed, max_k_len paged) capped by the window.
+// beside it, or 0 to run the two one after the other.  The decode kernel's
+// rate grows with its SMs up to the HBM peak (measured on the decode rows of
+// the mixed serving batches: ~53 GB/s per SM, 5.5 TB/s on 104 SMs), and its
+// CTAs spread over the prefill kernel's SMs once that finishes; the prefill
+// kernel's persistent grid is fixed at launch, so a share too small makes the
+// prefill side the long pole (5b: 0.98 ms at 32 SMs against 0.78 at 48),
+// while a share too large only delays the decode rows a little (0.83 ms at
+// 96).  The share is the prefill side's part of the two sides' estimated
+// work, 1.2 times over (the measured optimum: 24 and 48 SMs for the two
+// serving batches, whose prefill sides are 13 and 26 % of the work), at
+// most three quarters of the SMs; it overlaps only when the decode side's
+// estimated time (K/V bytes at the HBM rate) is at least a third of the
+// prefill side's (FLOPs at the tensor rate).  The key counts are device
+// data, so the estimates use an average key run per request (total_k /
+// num_reqs packed, max_k_len paged) capped by the window.
 constexpr double kDecodeBytesPerS = 6.0e12;
 constexpr double kPrefillFlopsPerS = 1.1e15;
 
@@ -220,8 +221,9 @@ int mixed_prefill_sms(int num_sms, int total_q, int total_k, bool paged, int num
   const double t_dec = 4.0 * hkv * decode_rows * span / kDecodeBytesPerS;    // per unit of head_dim
   const double t_pre = 4.0 * hq * pre_rows * pre_span / kPrefillFlopsPerS;  // per unit of head_dim
   if (t_dec * 3.0 < t_pre) return 0;
-  int sms = (3 * num_sms) / 4;
-  sms -= sms & 1;  // whole CTA pairs
+  const int cap = (3 * num_sms) / 4;
+  int sms = static_cast<int>(std::ceil(1.2 * num_sms * t_pre / (t_pre + t_dec)));
+  sms = std::max(2, std::min(sms + (sms & 1), cap - (cap & 1)));  // whole CTA pairs
   return sms;
 }
 

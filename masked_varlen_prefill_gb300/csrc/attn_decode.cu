@@ -29,8 +29,6 @@ namespace mvp {
 
 namespace {
 
-constexpr int kNW = 4;                      // compute warps
-constexpr int kThreads = (kNW + 1) * 32;    // + producer warp
 constexpr int kMaxStages = 3;
 constexpr unsigned kFull = 0xffffffffu;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
@@ -44,6 +42,12 @@ __host__ __device__ constexpr int kt_for(int d) { return d == 64 ? 128 : (d == 1
 // in flight.
 __host__ __device__ constexpr int stages_for(int d) { return d == 128 ? 2 : 3; }
 __host__ __device__ constexpr int box_for(int d) { return d > 256 ? 256 : d; }
+// Compute warps per CTA (a producer warp comes on top).
+__host__ __device__ constexpr int nw_for(int) { return 4; }
+// Dims of q and K per lane in the score step (q registers: QDL * GP).
+__host__ __device__ constexpr int qdl_for(int, int gp) { return gp == 8 ? 8 : 16; }
+// (key, head) probabilities each lane owns per warp step.
+__host__ __device__ constexpr int pairs_for(int d, int gp) { return (d == 128 && gp >= 4) ? 2 : 1; }
 
 template <int D>
 struct DCfg {
@@ -54,6 +58,8 @@ struct DCfg {
   static constexpr int TILE = KT * D * 2;     // bytes of one K (or V) tile
   static constexpr int STAGES = stages_for(D);
   static constexpr int SMEM = STAGES * 2 * TILE + 1024;
+  static constexpr int NW = nw_for(D);          // compute warps
+  static constexpr int THREADS = (NW + 1) * 32;  // + the producer warp
 };
 
 struct __align__(8) DBarriers {
@@ -97,18 +103,21 @@ __device__ __forceinline__ int row_off(int kk, int lane) {
 // PAGED: K/V rows come through a block table (compile-time, so the packed
 // kernel carries none of the paged addressing).
 template <int D, int GP, bool PAGED>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(DCfg<D>::THREADS)
     attn_decode_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                        const DecodeParams p) {
   using C = DCfg<D>;
   constexpr int DPL = C::DPL;
-  constexpr int KG = 32 / GP;        // keys per warp step
+  constexpr int PPL = pairs_for(D, GP);  // probabilities per lane and step
+  constexpr int KG = 32 * PPL / GP;      // keys per warp step
   constexpr int NG = C::KT / KG;     // warp steps per tile
+  static_assert(C::NW * GP * (D + 2) * 4 <= C::STAGES * 2 * C::TILE, "merge buffers fit the stages");
+  static_assert(C::KT % KG == 0, "whole steps per tile");
   extern __shared__ uint8_t smem_raw[];
   // Per compute warp, the step's 32 probabilities (key kk, head g at
   // kk * GP + g) as (p, p) pairs, read back by every lane as broadcasts
   // instead of 32 shuffles.
-  __shared__ __align__(16) float pbuf[kNW][64];
+  __shared__ __align__(16) float pbuf[C::NW][64 * pairs_for(D, GP)];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ DBarriers sb;
 
@@ -163,7 +172,7 @@ __global__ void __launch_bounds__(kThreads)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&sb.full[s], 1);
-      mbar_init(&sb.empty[s], kNW);
+      mbar_init(&sb.empty[s], C::NW);
     }
     sb.wc.abort = 0;
     sb.wc.limit_us = p.m.wait_limit_us;
@@ -171,7 +180,7 @@ __global__ void __launch_bounds__(kThreads)
   }
   __syncthreads();
 
-  if (warp == kNW) {
+  if (warp == C::NW) {
     // ---------------------------------------------------------------- producer
     if (lane == 0 && n_tiles > 0) {
       tma_prefetch_desc(&map_k);
@@ -216,13 +225,13 @@ __global__ void __launch_bounds__(kThreads)
   // a quarter-warp read 128 consecutive bytes), for all GP heads at once; a
   // reduce-scatter over those DS lanes leaves each lane the full score of one
   // (key, head) pair, held by DUP lanes alike.  A warp step of KG keys runs
-  // NSUB such sub-steps of KS keys, so that every lane owns the probability
-  // of one of the step's 32 (key, head) pairs.
-  constexpr int QDL = (GP == 8) ? 8 : 16;  // dims per lane in the score step (q registers: QDL * GP)
+  // NSUB such sub-steps of KS keys, so that every lane owns the probabilities
+  // of PPL of the step's 32 * PPL (key, head) pairs.
+  constexpr int QDL = qdl_for(D, GP);     // dims per lane in the score step
   constexpr int DS = D / QDL;              // lanes per key
   constexpr int KS = 32 / DS;              // keys per sub-step
   constexpr int DUP = DS / GP;             // lanes holding the same score
-  constexpr int NSUB = DUP;                // sub-steps per warp step
+  constexpr int NSUB = DUP * PPL;          // sub-steps per warp step
   constexpr int QCH = QDL / 8;             // 16-byte chunks of a K row per lane
   static_assert(DS >= GP && DS <= 32 && KS * NSUB == KG, "score layout");
   const int ds = lane % DS;   // dim slice
@@ -288,7 +297,7 @@ __global__ void __launch_bounds__(kThreads)
     const uint8_t* vs_tile = ks_tile + C::TILE;
     const int t0 = c_lo + t * C::KT;
     const bool interior = t0 >= core_lo && t0 + C::KT - 1 <= core_hi;
-    for (int gi = warp; gi < NG; gi += kNW) {
+    for (int gi = warp; gi < NG; gi += C::NW) {
       float x[NSUB];
 #pragma unroll
       for (int a = 0; a < NSUB; ++a) {
@@ -358,12 +367,15 @@ __global__ void __launch_bounds__(kThreads)
           for (int i = 0; i < DP2; ++i) acc2[g][i] = f2_mul(acc2[g][i], a2);
         }
       }
-      float xr = x[0];
 #pragma unroll
-      for (int a = 1; a < NSUB; ++a) xr = (rr == a) ? x[a] : xr;
-      const float pr = (xr == -INFINITY) ? 0.f : ex2_approx(xr - m_h);
-      l_part += pr;
-      pb[(rr * KS + ks) * GP + hh] = f2_pack(pr, pr);
+      for (int r = 0; r < PPL; ++r) {  // this lane's pairs: sub-steps rr + r * DUP
+        float xr = x[r * DUP];
+#pragma unroll
+        for (int a = 1; a < DUP; ++a) xr = (rr == a) ? x[r * DUP + a] : xr;
+        const float pr = (xr == -INFINITY) ? 0.f : ex2_approx(xr - m_h);
+        l_part += pr;
+        pb[((r * DUP + rr) * KS + ks) * GP + hh] = f2_pack(pr, pr);
+      }
       __syncwarp();
 #pragma unroll
       for (int kk = 0; kk < KG; ++kk) {
@@ -393,9 +405,9 @@ __global__ void __launch_bounds__(kThreads)
 
   // ------------------------------------------------------------------ merge warps
   // Stage buffers are free once every tile was consumed by every warp.
-  asm volatile("bar.sync 1, %0;" ::"r"(kNW * 32) : "memory");
-  float* sm = reinterpret_cast<float*>(smem);                 // [kNW][GP][D]
-  float* sml = sm + kNW * GP * D;                              // [kNW][GP][2]
+  asm volatile("bar.sync 1, %0;" ::"r"(C::NW * 32) : "memory");
+  float* sm = reinterpret_cast<float*>(smem);                 // [NW][GP][D]
+  float* sml = sm + C::NW * GP * D;                            // [NW][GP][2]
 #pragma unroll
   for (int g = 0; g < GP; ++g)
 #pragma unroll
@@ -409,16 +421,17 @@ __global__ void __launch_bounds__(kThreads)
     sml[(warp * GP + hh) * 2 + 0] = m_h;
     sml[(warp * GP + hh) * 2 + 1] = l_part;
   }
-  asm volatile("bar.sync 1, %0;" ::"r"(kNW * 32) : "memory");
+  asm volatile("bar.sync 1, %0;" ::"r"(C::NW * 32) : "memory");
+
   const bool null_mode = p.m.sink_mode == 2 && p.m.sinks != nullptr;
-  for (int idx = threadIdx.x; idx < heads_here * D; idx += kNW * 32) {
+  for (int idx = threadIdx.x; idx < heads_here * D; idx += C::NW * 32) {
     const int g = idx / D, d = idx % D;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kNW; ++w) M = fmaxf(M, sml[(w * GP + g) * 2]);
+    for (int w = 0; w < C::NW; ++w) M = fmaxf(M, sml[(w * GP + g) * 2]);
     float a = 0.f, L = 0.f;
 #pragma unroll
-    for (int w = 0; w < kNW; ++w) {
+    for (int w = 0; w < C::NW; ++w) {
       const float mw = sml[(w * GP + g) * 2];
       const float f = (mw == -INFINITY) ? 0.f : ex2_approx(mw - M);
       a += f * sm[(w * GP + g) * D + d];
@@ -503,7 +516,7 @@ cudaError_t launch_dg(const DecodeParams& p, const CUtensorMap& mk, const CUtens
   if (e != cudaSuccess) return e;
   const int n_sub = (p.group + GP - 1) / GP;
   dim3 grid(p.n_splits, p.num_reqs, p.hkv * n_sub);
-  kern<<<grid, kThreads, DCfg<D>::SMEM, stream>>>(mk, mv, p);
+  kern<<<grid, DCfg<D>::THREADS, DCfg<D>::SMEM, stream>>>(mk, mv, p);
   return cudaGetLastError();
 }
 
