@@ -109,6 +109,32 @@ def test_running_max_moves_on_every_tile(d, sink_mode):
     gh.compare(out, lse, ro, rl, what=w.name, strict=False)
 
 
+@pytest.mark.parametrize("d,group", [(64, 4), (128, 4), (128, 8), (128, 2), (256, 4)])
+@pytest.mark.parametrize("use_workspace", [True, False])
+def test_decode_running_max_rises_along_the_keys(d, group, use_workspace):
+    """Single-token rows whose scores rise by ~12 (log2 units) per 128 keys:
+    a warp's running max passes the lazy-rescale threshold every few steps
+    and lags the step maximum by up to the threshold in between, so both the
+    rescale and the stale-max paths of the decode kernel run (N(0, 1) scores
+    settle after the first tile).  Rows of up to 5000 keys: split over two
+    key chunks with the workspace (plus the combine), one without; the
+    1-key row has only key 0; the null-logit sink adds one more term."""
+    k_lens = [5000, 3000, 700, 4500, 1]
+    w = workloads.Workload(f"dec_rising_d{d}_g{group}", 900 + d + group, [1] * len(k_lens), k_lens, 2 * group, 2,
+                           d, True, -1, 0, workloads.SINK_NULL_LOGIT, None)
+    q, k, v, sinks = gh.make_inputs(w)
+    slope = 12.0 / (1.4426950408889634 * w.scale * 128)
+    _, cu_k = w.cu_seqlens()
+    for b in range(w.num_reqs):
+        n = int(cu_k[b + 1] - cu_k[b])
+        ramp = slope * torch.arange(n, device=k.device, dtype=torch.float32)
+        k[cu_k[b]:cu_k[b + 1], :, 0] = ramp[:, None].to(torch.bfloat16)
+    q[:, :, 0] = 1.0
+    out, lse, _, _ = gh.run_gpu(w, q, k, v, sinks, use_workspace=use_workspace, num_decode_reqs=w.num_reqs)
+    ro, rl = gh.oracle_full(w, q, k, v, sinks, None)
+    gh.compare(out, lse, ro, rl, what=w.name, strict=False)
+
+
 @pytest.mark.parametrize("d", [128, 256])
 def test_upper_bound_item_space_with_the_alternating_static_order(d):
     """A windowed batch without ranges runs every item statically, odd rounds
