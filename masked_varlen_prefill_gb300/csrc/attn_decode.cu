@@ -21,6 +21,8 @@
 //   is a single split and the CTA writes the final output itself.
 #include <cuda_bf16.h>
 
+#include <mutex>
+
 #include "mask.cuh"
 #include "mvp_internal.cuh"
 #include "ptx.cuh"
@@ -509,11 +511,28 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams 
   }
 }
 
+// The dynamic shared memory attribute of each instantiation is set once per
+// device (under a mutex: two host threads may make their first call on a
+// device at the same time).
+std::mutex g_decode_attr_mutex;
+
 template <int D, int GP>
 cudaError_t launch_dg(const DecodeParams& p, const CUtensorMap& mk, const CUtensorMap& mv, cudaStream_t stream) {
-  auto kern = p.m.block_table != nullptr ? attn_decode_kernel<D, GP, true> : attn_decode_kernel<D, GP, false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DCfg<D>::SMEM);
+  const bool paged = p.m.block_table != nullptr;
+  auto kern = paged ? attn_decode_kernel<D, GP, true> : attn_decode_kernel<D, GP, false>;
+  static bool attr_set[2][64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  {
+    std::lock_guard<std::mutex> lock(g_decode_attr_mutex);
+    if (!attr_set[paged ? 1 : 0][dev]) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DCfg<D>::SMEM);
+      if (e != cudaSuccess) return e;
+      attr_set[paged ? 1 : 0][dev] = true;
+    }
+  }
   const int n_sub = (p.group + GP - 1) / GP;
   dim3 grid(p.n_splits, p.num_reqs, p.hkv * n_sub);
   kern<<<grid, DCfg<D>::THREADS, DCfg<D>::SMEM, stream>>>(mk, mv, p);
