@@ -9,13 +9,14 @@
 // This path is HBM-bound (each key is 2 * D bf16 of K and V used by G query
 // heads), so it is SIMT, not tensor-core work:
 // * A CTA handles one (request, KV head, key split).  A producer warp streams
-//   KT-key tiles of K and V into a 2- or 3-stage shared-memory ring with TMA; four
-//   compute warps read them back conflict-free (lane l owns D/32 consecutive
-//   dimensions of every key row).
-// * A warp takes KG = 32 / G keys at a time: each lane forms partial dot
-//   products for every (key, head) pair over its dimensions, and a shuffle
-//   reduce-scatter leaves lane l with the full score of pair l.  The online
-//   base-2 softmax and the p * V accumulation follow.
+//   KT-key tiles of K and V into a 2- or 3-stage shared-memory ring with TMA;
+//   four compute warps read them back conflict-free.
+// * A warp takes a step of KG keys at a time.  Scores: the DS lanes that
+//   share one key each form partial dot products over their slice of the
+//   head dimension for every q head of the CTA, and a shuffle reduce-scatter
+//   over those DS lanes leaves each lane the full score of one (key, head)
+//   pair.  The online base-2 softmax (lazy rescale) follows, and the p * V
+//   accumulation with lane l owning D/32 dimensions of every head.
 // * Long rows are split across CTAs (split-KV); partial (acc, max, sum)
 //   triples are merged by decode_combine_kernel.  Without workspace every row
 //   is a single split and the CTA writes the final output itself.
