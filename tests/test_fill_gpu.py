@@ -88,6 +88,27 @@ def test_random(seed):
     check(workloads.pad_ranges(per_req), q_lens, seq)
 
 
+@pytest.mark.parametrize("nb,nr", [(1024, 2), (1025, 2), (1000, 3), (600, 3), (64, 32)])
+def test_many_short_requests(nb, nr):
+    """Batches of many 1- to 9-row requests: up to 1024 requests with at most
+    2048 range entries between them are read from shared-memory copies, the
+    others from global memory (1025 requests; 3000 entries); CTAs span many
+    requests, and a request's rows are split between two CTAs."""
+    rng = np.random.default_rng(nb * 7 + nr)
+    q_lens = [int(rng.integers(1, 10)) for _ in range(nb)]
+    seq = [q + int(rng.integers(0, 40)) for q in q_lens]
+    per_req = []
+    for b in range(nb):
+        rl = []
+        for _ in range(int(rng.integers(0, nr + 1))):
+            s0 = int(rng.integers(0, seq[b] + 2))
+            rl.append((s0, s0 + int(rng.integers(-1, 12))))
+        per_req.append(rl)
+    ranges = workloads.pad_ranges(per_req, min_width=nr)
+    assert ranges.shape == (nb, nr, 2)
+    check(ranges, q_lens, seq)
+
+
 def test_no_ranges_and_degenerate_only():
     check(None, [5, 3], [9, 3])
     check(workloads.pad_ranges([[(3, 3), (7, 2)], []]), [5, 3], [9, 3])
