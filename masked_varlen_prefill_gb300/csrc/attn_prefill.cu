@@ -809,6 +809,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       const uint64_t dq = smem_desc_sw128(smem_u32(sQ), 16, 1024);
       const uint64_t dk0 = smem_desc_sw128(smem_u32(sK), 16, 1024);
       const uint64_t dv0 = smem_desc_sw128(smem_u32(sV), BN * 128, 1024);
+      const bool leader = elect_one();  // issues the MMAs; the commits' elect.sync picks the same lane
       bool ok = true;
       int T = 0, qn = 0;
       for (int n = 0; ok; ++n) {
@@ -830,16 +831,19 @@ __global__ void __launch_bounds__(C::THREADS, 1)
               break;
             }
             const uint32_t d = tmem + C::S_COL + C::sbuf(t) * BN;
-            const uint64_t dk = dk0 + static_cast<uint64_t>((s * C::K_BYTES) >> 4);
+            const uint64_t dk = desc_add(dk0, static_cast<uint32_t>((s * C::K_BYTES) >> 4));
+            if (leader) {
 #pragma unroll
-            for (int c = 0; c < C::QCH; ++c) {
+              for (int c = 0; c < C::QCH; ++c) {
 #pragma unroll
-              for (int k16 = 0; k16 < 4; ++k16) {
-                const uint64_t a = dq + static_cast<uint64_t>((c * (kBM * 128) + k16 * 32) >> 4);
-                const uint64_t b = dk + static_cast<uint64_t>((c * (C::KROWS * 128) + k16 * 32) >> 4);
-                mma_ss_elect<C::MMA_CTAS>(d, a, b, idesc_qk, (c | k16) != 0 ? 1u : 0u);
+                for (int k16 = 0; k16 < 4; ++k16) {
+                  const uint64_t a = desc_add(dq, static_cast<uint32_t>((c * (kBM * 128) + k16 * 32) >> 4));
+                  const uint64_t b = desc_add(dk, static_cast<uint32_t>((c * (C::KROWS * 128) + k16 * 32) >> 4));
+                  mma_ss_one<C::MMA_CTAS>(d, a, b, idesc_qk, (c | k16) != 0 ? 1u : 0u);
+                }
               }
             }
+            __syncwarp();
             if constexpr (!C::MERGED_RELEASE) {
               mma_commit_elect<C::MMA_CTAS>(&sb.k_empty[s]);
               if (j == pl.n_tiles - 1) mma_commit_elect<C::MMA_CTAS>(&sb.q_empty);  // Q free for the next item
@@ -870,13 +874,16 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             }
             tc_fence_after();  // P (softmax warps) and the O read-out (epilogue warps) are ordered before
             const uint32_t pcol = tmem + C::S_COL + C::sbuf(t) * BN;
-            const uint64_t dv = dv0 + static_cast<uint64_t>((s * C::V_STAGE) >> 4);
+            const uint64_t dv = desc_add(dv0, static_cast<uint32_t>((s * C::V_STAGE) >> 4));
             const uint32_t first = (j > LEAD) ? 1u : 0u;  // the item's first PV overwrites O
+            if (leader) {
 #pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk) {
-              const uint64_t b = dv + static_cast<uint64_t>((kk * 16 * 128) >> 4);
-              mma_ts_elect<C::MMA_CTAS>(tmem + C::O_COL, pcol + kk * 8, b, idesc_pv, kk == 0 ? first : 1u);
+              for (int kk = 0; kk < BN / 16; ++kk) {
+                const uint64_t b = desc_add(dv, static_cast<uint32_t>((kk * 16 * 128) >> 4));
+                mma_ts_one<C::MMA_CTAS>(tmem + C::O_COL, pcol + kk * 8, b, idesc_pv, kk == 0 ? first : 1u);
+              }
             }
+            __syncwarp();
             if constexpr (!C::MERGED_RELEASE) mma_commit_elect<C::MMA_CTAS>(&sb.v_empty[s]);
             mma_commit_elect<C::MMA_CTAS>(&sb.o_done[t & 1]);
           }

@@ -473,40 +473,53 @@ __device__ __forceinline__ void mma_commit_pair(uint64_t* bar) {
 
 // ------------------------------------------------------------------ elected issue
 // The MMA warp runs its issue loop with all 32 lanes converged, so the
-// descriptors and TMEM addresses are warp-uniform values; each tcgen05.mma /
-// commit is issued by the lane elect.sync picks (the same lane every time
-// for a full warp, so its commits track every MMA it issued).  Issuing from
-// a lane-0-only branch instead costs ~1.7x more time per MMA, and the single
-// issuing thread is what bounds the tensor pipe in these kernels.
+// descriptors and TMEM addresses are warp-uniform values.  One lane, picked
+// once by elect.sync, issues each tile's block of tcgen05.mma in a branch
+// (an elect.sync and a 64-bit descriptor add per MMA measured 1.4-3.5 %
+// slower over the prefill workloads: the MMA warp shares its SM
+// sub-partition with two softmax warps, and every instruction it issues is
+// one they wait for); the commits that track those MMAs use elect.sync,
+// which picks the same lane in a full warp.
+// The lane elect.sync picks in a converged warp (the same one the *_elect
+// helpers pick), for a block of single-lane MMA issues; the commit that
+// tracks them must come from the same lane.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t e;
+  asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}" : "=r"(e));
+  return e != 0;
+}
+// Single-lane forms of the MMA issues (the caller branches on elect_one()).
 template <int NCTA>
-__device__ __forceinline__ void mma_ss_elect(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+__device__ __forceinline__ void mma_ss_one(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
   if constexpr (NCTA == 2)
-    asm volatile(
-        "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-        "l"(a), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+                 "l"(a), "l"(b), "r"(idesc), "r"(acc)
+                 : "memory");
   else
-    asm volatile(
-        "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-        "l"(a), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+                 "l"(a), "l"(b), "r"(idesc), "r"(acc)
+                 : "memory");
 }
 template <int NCTA>
-__device__ __forceinline__ void mma_ts_elect(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+__device__ __forceinline__ void mma_ts_one(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
   if constexpr (NCTA == 2)
-    asm volatile(
-        "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
-        "r"(a), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+                 "r"(a), "l"(b), "r"(idesc), "r"(acc)
+                 : "memory");
   else
-    asm volatile(
-        "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
-        "r"(a), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+                 "r"(a), "l"(b), "r"(idesc), "r"(acc)
+                 : "memory");
+}
+// A shared-memory descriptor moved by `off16` 16-byte units: the start
+// address field sits in the low word and, for any shared-memory address,
+// cannot carry out of it, so only the low word changes.
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t off16) {
+  return (d & 0xffffffff00000000ull) | static_cast<uint32_t>(static_cast<uint32_t>(d) + off16);
 }
 template <int NCTA>
 __device__ __forceinline__ void mma_commit_elect(uint64_t* bar) {
