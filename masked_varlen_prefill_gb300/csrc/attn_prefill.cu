@@ -449,8 +449,11 @@ __device__ __forceinline__ void tma_load(void* dst, const CUtensorMap* map, uint
 }
 
 // PAGED: K/V rows come through a block table (compile-time, so the packed
-// kernel carries none of the paged addressing).
-template <class C, bool PAGED>
+// kernel carries none of the paged addressing).  LSE: the caller asked for
+// the log-sum-exp, so the softmax warps also sum the unrounded
+// probabilities; without it they skip that packed add per score pair (O
+// does not depend on it).
+template <class C, bool PAGED, bool LSE>
 __global__ void __launch_bounds__(C::THREADS, 1)
     attn_prefill_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                         const __grid_constant__ CUtensorMap map_v, const PrefillParams p) {
@@ -1275,7 +1278,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             add_bf16x2_halves(pk, acc_lo[i & 3], acc_hi[i & 3]);
           else if constexpr (!C::ROWSUM)  // (else the tensor core sums the rounded values)
             acc_r[i & 3] = f2_add(acc_r[i & 3], f2_pack(__uint_as_float(pk << 16), __uint_as_float(pk & 0xffff0000u)));
-          acc_e[i & 3] = f2_add(acc_e[i & 3], f2_pack(e0, e1));
+          if constexpr (LSE) acc_e[i & 3] = f2_add(acc_e[i & 3], f2_pack(e0, e1));
           s[i] = pk;
         }
         {
@@ -1288,8 +1291,10 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             f2_unpack(f2_add(f2_add(acc_r[0], acc_r[1]), f2_add(acc_r[2], acc_r[3])), a0, a1);
             l_sum += a0 + a1;
           }
-          f2_unpack(f2_add(f2_add(acc_e[0], acc_e[1]), f2_add(acc_e[2], acc_e[3])), b0, b1);
-          l_lse += b0 + b1;
+          if constexpr (LSE) {
+            f2_unpack(f2_add(f2_add(acc_e[0], acc_e[1]), f2_add(acc_e[2], acc_e[3])), b0, b1);
+            l_lse += b0 + b1;
+          }
         }
         // P (bf16 pairs) over this half's scores.  Both halves have their
         // scores in registers (the exchange above), so neither overwrites
@@ -1519,13 +1524,15 @@ template <class C>
 cudaError_t launch_cfg(const PrefillParams& p, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                        cudaStream_t stream) {
   const bool paged = p.m.block_table != nullptr;
-  auto kern = paged ? attn_prefill_kernel<C, true> : attn_prefill_kernel<C, false>;
-  static LaunchState state[2][64];
+  const bool want_lse = p.lse != nullptr;
+  auto kern = paged ? (want_lse ? attn_prefill_kernel<C, true, true> : attn_prefill_kernel<C, true, false>)
+                    : (want_lse ? attn_prefill_kernel<C, false, true> : attn_prefill_kernel<C, false, false>);
+  static LaunchState state[4][64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  LaunchState& ls = state[paged ? 1 : 0][dev];
+  LaunchState& ls = state[(paged ? 1 : 0) + (want_lse ? 2 : 0)][dev];
   const long long n_items =
       static_cast<long long>(p.n_qtiles) * (p.num_reqs - p.req_offset) * p.hkv * p.n_hgroups * C::DV_SPLIT;
   if (n_items <= 0) return cudaSuccess;
