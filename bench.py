@@ -384,6 +384,7 @@ def run_reference(args, world, rank):
         total_f += f
         nrows += n
     pool.close()
+    pool.join()
     value = total_f / total_t / 1e12
     sample = (f"{nrows // max(1, args.steps)} query rows per step (up to {rows_per_req} per request, all heads) "
               f"of the {args.workload} workload, float64 dense oracle")
@@ -956,6 +957,7 @@ def run_gpu(args, world, rank, local):
     if pool is not None:
         t_cpu, f_cpu, n_rows, cpu_s = time_oracle(w, counts, args.cpu_rows_per_req, pool, cores)
         pool.close()
+        pool.join()  # the workers' exit must not compete with the host side of the GPU timings below
         cpu_baseline = {"value": f_cpu / t_cpu / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                         "sample": f"{n_rows} query rows (up to {args.cpu_rows_per_req} per request, all heads) of "
                                   f"the {args.workload} workload, float64 dense oracle, {cpu_s:.1f} core-seconds "
