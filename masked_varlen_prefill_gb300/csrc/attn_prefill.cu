@@ -129,11 +129,13 @@ struct Cfg {
   // LSE).  A V stage is VCH blocks of BN x 128 bytes (the loaded value
   // columns) plus the ones block.
   static constexpr bool ROWSUM = ROWSUM_ != 0;
-  // Otherwise the softmax warps sum the rounded probabilities: at D = 512 by
-  // mixed-precision adds (add.rn.f32.bf16 on each bf16 half, no unpack;
-  // same bits), measured 58.5 vs 57.6 % of the bf16 peak there, while at
-  // D = 256 the shift / mask / packed add measured 0.5-1 % faster.
-  static constexpr bool MIXED_SUM = !ROWSUM && D_ == 512;
+  // Otherwise the softmax warps sum the rounded probabilities by
+  // mixed-precision adds (add.rn.f32.bf16 on each bf16 half, no unpack; the
+  // same bits as unpacking and adding): measured 58.5 vs 57.6 % of the bf16
+  // peak at D = 512 and 0.3 % faster at D = 256 than a shift / mask / packed
+  // add (once the MMA warp issued fewer instructions; before, the latter
+  // was 0.5-1 % faster there).
+  static constexpr bool MIXED_SUM = !ROWSUM;
   static constexpr int ONES = ROWSUM ? 16 : 0;
   static constexpr int V_STAGE = (VCH + (ROWSUM ? 1 : 0)) * BN * 128;  // stage stride
   static constexpr int PART = DVC + ONES;                           // accumulator columns per CTA part
@@ -812,7 +814,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       const uint64_t dq = smem_desc_sw128(smem_u32(sQ), 16, 1024);
       const uint64_t dk0 = smem_desc_sw128(smem_u32(sK), 16, 1024);
       const uint64_t dv0 = smem_desc_sw128(smem_u32(sV), BN * 128, 1024);
-      const bool leader = elect_one();  // issues the MMAs; the commits' elect.sync picks the same lane
+      const bool issuer = elect_one();  // issues the MMAs; the commits' elect.sync picks the same lane
       bool ok = true;
       int T = 0, qn = 0;
       for (int n = 0; ok; ++n) {
@@ -835,7 +837,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             }
             const uint32_t d = tmem + C::S_COL + C::sbuf(t) * BN;
             const uint64_t dk = desc_add(dk0, static_cast<uint32_t>((s * C::K_BYTES) >> 4));
-            if (leader) {
+            if (issuer) {
 #pragma unroll
               for (int c = 0; c < C::QCH; ++c) {
 #pragma unroll
@@ -879,7 +881,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             const uint32_t pcol = tmem + C::S_COL + C::sbuf(t) * BN;
             const uint64_t dv = desc_add(dv0, static_cast<uint32_t>((s * C::V_STAGE) >> 4));
             const uint32_t first = (j > LEAD) ? 1u : 0u;  // the item's first PV overwrites O
-            if (leader) {
+            if (issuer) {
 #pragma unroll
               for (int kk = 0; kk < BN / 16; ++kk) {
                 const uint64_t b = desc_add(dv, static_cast<uint32_t>((kk * 16 * 128) >> 4));
@@ -1260,11 +1262,11 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
         const uint64_t sc2 = f2_pack(sc, sc);
         const uint64_t nm2 = f2_pack(-m_use, -m_use);
-        uint64_t acc_r[4], acc_e[4];
+        uint64_t acc_e[4];
         float acc_lo[4], acc_hi[4];  // (MIXED_SUM: rounded probabilities of the even, odd columns)
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          acc_r[k] = acc_e[k] = 0ull;
+          acc_e[k] = 0ull;
           acc_lo[k] = acc_hi[k] = 0.f;
         }
 #pragma unroll
@@ -1274,10 +1276,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           const float e0 = ex2_approx(t0);
           const float e1 = ex2_approx(t1);
           const uint32_t pk = pack_bf16x2(e0, e1);
-          if constexpr (C::MIXED_SUM)
+          if constexpr (C::MIXED_SUM)  // (else the tensor core sums the rounded values)
             add_bf16x2_halves(pk, acc_lo[i & 3], acc_hi[i & 3]);
-          else if constexpr (!C::ROWSUM)  // (else the tensor core sums the rounded values)
-            acc_r[i & 3] = f2_add(acc_r[i & 3], f2_pack(__uint_as_float(pk << 16), __uint_as_float(pk & 0xffff0000u)));
           if constexpr (LSE) acc_e[i & 3] = f2_add(acc_e[i & 3], f2_pack(e0, e1));
           s[i] = pk;
         }
@@ -1286,9 +1286,6 @@ __global__ void __launch_bounds__(C::THREADS, 1)
           if constexpr (C::MIXED_SUM) {
             a0 = (acc_lo[0] + acc_lo[1]) + (acc_lo[2] + acc_lo[3]);
             a1 = (acc_hi[0] + acc_hi[1]) + (acc_hi[2] + acc_hi[3]);
-            l_sum += a0 + a1;
-          } else if constexpr (!C::ROWSUM) {
-            f2_unpack(f2_add(f2_add(acc_r[0], acc_r[1]), f2_add(acc_r[2], acc_r[3])), a0, a1);
             l_sum += a0 + a1;
           }
           if constexpr (LSE) {
