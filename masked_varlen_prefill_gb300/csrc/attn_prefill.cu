@@ -430,7 +430,8 @@ __device__ __forceinline__ bool pair_exchange(float2* slots, uint64_t* xb, int& 
                                               float2& theirs, volatile WaitCtl* abort_flag, int* err) {
   float2* slot = slots + (k & 1) * (2 * kBM);
   slot[half * kBM + row] = mine;
-  mbar_arrive(&xb[k & 1]);
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&xb[k & 1]);  // release: the warp's slots are visible
   const bool ok = mbar_wait(&xb[k & 1], (k >> 1) & 1, abort_flag, err, kDevTimeoutSoftmax);
   theirs = slot[(1 - half) * kBM + row];
   ++k;
@@ -510,8 +511,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
       mbar_init(&sb.x_empty[i], 4);  // ... and read this CTA's
     }
     for (int i = 0; i < 4; ++i) {
-      mbar_init(&sb.xchg[i][0], 64);
-      mbar_init(&sb.xchg[i][1], 64);
+      mbar_init(&sb.xchg[i][0], 2);
+      mbar_init(&sb.xchg[i][1], 2);
     }
     sb.wc.abort = 0;
     sb.wc.limit_us = p.m.wait_limit_us;
