@@ -203,12 +203,17 @@ struct KVArgs {
 // estimated time (K/V bytes at the HBM rate) is at least a third of the
 // prefill side's (FLOPs at the tensor rate).  The key counts are device
 // data, so the estimates use an average key run per request (total_k /
-// num_reqs packed, max_k_len paged) capped by the window.
+// num_reqs packed, max_k_len paged) capped by the window.  A paged cache of
+// blocks under 64 tokens loads the prefill kernel's tiles in as many boxes
+// as blocks, which slows it (mm_prefix sliding: 0.39 of the bf16 peak at 16
+// tokens against 0.65 at 64 and packed), so its rate estimate shrinks with
+// the block: x0.6 at 16 tokens, x0.8 at 32.
 constexpr double kDecodeBytesPerS = 6.0e12;
 constexpr double kPrefillFlopsPerS = 1.1e15;
 
-int mixed_prefill_sms(int num_sms, int total_q, int total_k, bool paged, int num_reqs, int decode_rows,
-                      int max_q_len, int max_k_len, int causal, int window_left, int window_right, int hq, int hkv) {
+int mixed_prefill_sms(int num_sms, int total_q, int total_k, bool paged, int block_shift, int num_reqs,
+                      int decode_rows, int max_q_len, int max_k_len, int causal, int window_left, int window_right,
+                      int hq, int hkv) {
   const double avg_k = paged ? static_cast<double>(max_k_len) : static_cast<double>(total_k) / num_reqs;
   double span = avg_k;  // keys one row sees
   if (causal) {
@@ -219,7 +224,8 @@ int mixed_prefill_sms(int num_sms, int total_q, int total_k, bool paged, int num
   const double pre_rows = std::max(0, total_q - decode_rows);
   const double pre_span = causal && window_left < 0 ? std::max(1.0, avg_k - 0.5 * max_q_len) : span;
   const double t_dec = 4.0 * hkv * decode_rows * span / kDecodeBytesPerS;    // per unit of head_dim
-  const double t_pre = 4.0 * hq * pre_rows * pre_span / kPrefillFlopsPerS;  // per unit of head_dim
+  const double box_rate = (paged && block_shift < 6) ? std::max(0.2, 0.6 + 0.2 * (block_shift - 4)) : 1.0;
+  const double t_pre = 4.0 * hq * pre_rows * pre_span / (kPrefillFlopsPerS * box_rate);  // per unit of head_dim
   if (t_dec * 3.0 < t_pre) return 0;
   const int cap = (3 * num_sms) / 4;
   int sms = static_cast<int>(std::ceil(1.2 * num_sms * t_pre / (t_pre + t_dec)));
@@ -412,8 +418,9 @@ int attn_fwd_impl(const void* q, void* out, float* lse, const int32_t* cu_seqlen
   int sms = 0;
   if (concurrent) {
     sms = share > 0 ? share
-                    : mixed_prefill_sms(num_sms, total_q, total_k, paged, num_reqs, decode_count, max_q_len,
-                                        max_k_len, causal, window_left, window_right, num_heads_q, num_heads_kv);
+                    : mixed_prefill_sms(num_sms, total_q, total_k, paged, paged ? kv.block_shift : 0, num_reqs,
+                                        decode_count, max_q_len, max_k_len, causal, window_left, window_right,
+                                        num_heads_q, num_heads_kv);
     if (sms == 0) concurrent = false;               // too little decode work to overlap
     if (sms > num_sms - 2) sms = num_sms - 2;       // leave the decode kernel at least two SMs
     if (sms < 2) sms = 2;
