@@ -45,11 +45,20 @@ __host__ __device__ constexpr int kt_for(int d) { return d == 64 ? 128 : (d == 1
 // in flight.
 __host__ __device__ constexpr int stages_for(int d) { return d == 128 ? 2 : 3; }
 __host__ __device__ constexpr int box_for(int d) { return d > 256 ? 256 : d; }
-// Compute warps per CTA (a producer warp comes on top).
+// Compute warps per CTA (a producer warp comes on top).  Eight at D = 128
+// (two CTAs per SM, 8-dim lane slices to fit the registers) measured slower
+// than four with three CTAs per SM.
 __host__ __device__ constexpr int nw_for(int) { return 4; }
-// Dims of q and K per lane in the score step (q registers: QDL * GP).
+// Dims of q and K per lane in the score step (q registers: QDL * GP): 16
+// keeps the reduce-scatter to log2(D / 16) stages; 8-dim slices at D = 128
+// and 4 heads (one more stage, fewer registers) measured ~10 % slower.
 __host__ __device__ constexpr int qdl_for(int, int gp) { return gp == 8 ? 8 : 16; }
-// (key, head) probabilities each lane owns per warp step.
+// (key, head) probabilities each lane owns per warp step.  Two at D = 128
+// with four or more heads per CTA: 16-key steps give every warp two
+// independent score chains and halve the per-step softmax overhead; on a
+// part of the SMs (beside the prefill kernel) the decode rows of the mixed
+// serving batch ran 11 % faster.  A 64-key tile then holds exactly one step
+// per compute warp.
 __host__ __device__ constexpr int pairs_for(int d, int gp) { return (d == 128 && gp >= 4) ? 2 : 1; }
 
 template <int D>
