@@ -150,7 +150,9 @@ size_t mvp_attn_workspace_size(int num_reqs, int num_heads_q, int head_dim, int 
  * q      bf16 [total_q, num_heads_q, head_dim], contiguous, 16-byte aligned.
  * k, v   bf16 [total_k, num_heads_kv, head_dim], contiguous, 16-byte aligned.
  * out    bf16 [total_q, num_heads_q, head_dim] (written for every row).
- * lse    fp32 [num_heads_q, total_q] or NULL.
+ * lse    fp32 [num_heads_q, total_q] or NULL.  NULL skips the log-sum-exp
+ *                 (the prefill kernel then runs an instantiation without its
+ *                 unrounded-sum add); out is the same bit for bit either way.
  * cu_seqlens_q, cu_seqlens_k  int32 [num_reqs + 1] packed offsets, within
  *                 total_q / total_k, with 0 <= q_len <= k_len per request.
  *                 The product library trusts them (reading them on the host
