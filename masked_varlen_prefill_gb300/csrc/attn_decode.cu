@@ -233,8 +233,9 @@ __global__ void __launch_bounds__(DCfg<D>::THREADS)
 
   // ------------------------------------------------------------------ compute
   // Scores: DS lanes share one key's dot product, each over QDL dims (two or
-  // one 16-byte chunks of the K row: chunk ds + j * DS, so the eight lanes of
-  // a quarter-warp read 128 consecutive bytes), for all GP heads at once; a
+  // one 16-byte chunks of the K row: chunk ds + j * DS, so that with DS >= 8
+  // the eight lanes of a quarter-warp read 128 consecutive bytes), for all GP
+  // heads at once; a
   // reduce-scatter over those DS lanes leaves each lane the full score of one
   // (key, head) pair, held by DUP lanes alike.  A warp step of KG keys runs
   // NSUB such sub-steps of KS keys, so that every lane owns the probabilities
@@ -249,7 +250,7 @@ __global__ void __launch_bounds__(DCfg<D>::THREADS)
   const int ds = lane % DS;   // dim slice
   const int ks = lane / DS;   // key of the sub-step
   const int hh = ds / DUP;    // head of this lane's scores
-  const int rr = ds % DUP;    // the sub-step whose score this lane keeps
+  const int rr = ds % DUP;    // this lane keeps the scores of sub-steps rr + r * DUP, r < PPL
 
   // q for this lane's dim chunks, every head of the CTA, pre-scaled to log2
   // units, as (even, odd) dim pairs for the packed fp32x2 FMAs.
